@@ -1,0 +1,86 @@
+"""Planted mistakes in the oracle must fail its pins.
+
+Each case edits one expression of a copy of ``oracle.c`` (a transposed operand, a wrong
+index, a dropped term, a flipped comparison), compiles the copy on the CPU, routes the
+oracle through it and runs the pins that should catch that kind of mistake: at least one
+of them has to fail. This shows that the pins constrain the oracle rather than restate it.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle_rules as R
+import test_oracle_sample as S
+
+
+def _enum_small():
+    S.test_exact_enumeration_is_lossless(5, 2, 1.3, 3)
+
+
+def _enum_bonus():
+    S.test_exact_enumeration_is_lossless(3, 2, 0.7, 2)
+
+
+MUTANTS = [
+    ("residual operands transposed",
+     "w[j] = p > q ? p - q : 0.0;", "w[j] = q > p ? q - p : 0.0;",
+     [_enum_small, S.test_residual_mass_identity_and_searchsorted]),
+    ("sampling uniform taken at the rejected position",
+     "(double)u[k], &smg", "(double)u[a], &smg", [_enum_small]),
+    ("temperature dropped",
+     "exp((logit_at(base, dtype, off + (size_t)j) - m) / T)",
+     "exp((logit_at(base, dtype, off + (size_t)j) - m))",
+     [lambda: R.test_softmax_matches_torch(1000, 0.7, 3.0), _enum_small]),
+    ("accept ratio inverted", "const double rho = px[i] / qx[i];",
+     "const double rho = qx[i] / px[i];", [_enum_small]),
+    ("non-strict accept test", "if (!((double)u[i] < rho)) {", "if (!((double)u[i] <= rho)) {",
+     [S.test_accept_is_strict_at_an_exact_ratio]),
+    ("non-strict inverse CDF", "if (run > target) {", "if (run >= target) {",
+     [S.test_inverse_cdf_boundaries]),
+    ("bonus drawn from the previous row", "const int bonus_row = from_residual ? -1 : a;",
+     "const int bonus_row = from_residual ? -1 : (a > 0 ? a - 1 : a);",
+     [_enum_bonus, S.test_q_equal_p_accepts_everything]),
+    ("target row stride of the draft array",
+     "size_t off = ((size_t)r * (k + 1) + i) * (size_t)V;\n      if (softmax_stats(target",
+     "size_t off = ((size_t)r * k + i) * (size_t)V;\n      if (softmax_stats(target",
+     [S.test_q_equal_p_accepts_everything, S.test_residual_mass_identity_and_searchsorted]),
+    ("greedy emits the draft token at the mismatch", "tok[a] = g[a];",
+     "tok[a] = a < n ? x[a] : g[a];", [R.test_greedy_argmax_and_walk]),
+    ("greedy argmax keeps the last tie", "if (best < 0 || z > bv) {",
+     "if (best < 0 || z >= bv) {", [R.test_greedy_argmax_and_walk]),
+    ("gate argmax keeps the last tie", "} else if (z > l1) {", "} else if (z >= l1) {",
+     [R.test_gate_truth_table]),
+    ("gate fires at gap == tau", "(gap > tau)", "(gap >= tau)", [R.test_gate_truth_table]),
+    ("gate forgets the old maximum", "l2 = l1;\n        l1 = z;", "l1 = z;",
+     [R.test_gate_matches_topk]),
+    ("n-gram tries the shortest phrase first",
+     "for (int n = n_max; n >= n_min && cnt == 0; --n) {",
+     "for (int n = n_min; n <= n_max && cnt == 0; ++n) {",
+     [lambda: R.test_ngram_brute_force(3)]),
+    ("n-gram takes the latest occurrence", "for (int s = 0; s + n <= L - 1; ++s) {",
+     "for (int s = L - 1 - n; s >= 0; --s) {", [lambda: R.test_ngram_brute_force(2)]),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory(prefix="oracle_mutants_") as d:
+        yield d
+
+
+@pytest.mark.parametrize("name,old,new,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(workdir, name, old, new, pins):
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation site not unique: {old!r}"
+    path = os.path.join(workdir, name.replace(" ", "_") + ".so")
+    oracle.compile_variant(src.replace(old, new), path)
+    failures = 0
+    with oracle.library(path):
+        for pin in pins:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failures += 1
+    assert failures >= 1, f"no pin caught the planted mistake: {name}"
