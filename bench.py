@@ -1,0 +1,531 @@
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one spec_verify_sample call (the fused verify kernel: tempered softmax of the
+k+1 target rows and k draft rows, accept tests, accepted prefix, residual or bonus draw)
+over one batch of the B=512, k=8, V=128256 bf16, T=0.7 workload, inputs resident in HBM.
+The metric is verified draft positions per second (sum of n_r per step / step time), with
+the logit bandwidth (each needed logit read once) against the measured HBM peak.
+
+Secondary rows time the other calls of the hot path on their own workloads (greedy verify,
+logit-gap gate, n-gram proposal + greedy verify, the fp32 sampled verify) with the same
+event timing; workloads that fit in L2 get an L2 flush before every timed launch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+Under torchrun every rank runs its own replica of the batch (request sharding, no
+collective on the data path): value = positions of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and logit GB/s (fraction of GB300 HBM peak)"
+HEAD = 3  # index of the headline workload in synth.WORKLOADS
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------------ helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_17_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sample_bytes(n_total: int, B: int, k: int, V: int, elem: int) -> int:
+    """Algorithmic bytes of one sampled verify: every needed logit once (sum(n_r + 1) target
+    rows, sum(n_r) draft rows) plus the small per-request I/O (draft tokens, uniforms,
+    emitted tokens, accept length, 4 bytes each)."""
+    return (2 * n_total + B) * V * elem + 4 * B * (k + (k + 1) + (k + 1) + 1)
+
+
+# ------------------------------------------------------------------------------ timing
+def time_launches(fn, steps, warmup, stream, flush=None):
+    """Per-launch CUDA-event times (ms) of fn() on `stream`, after `warmup` calls. With
+    `flush`, an L2 flush runs before every launch, outside the timed events."""
+    import torch
+
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            if flush is not None:
+                flush()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def make_flush(device):
+    import torch
+
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device)
+
+    def flush():
+        buf.fill_(1)
+
+    return flush
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def gb300_arm(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_17_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = synth.WORKLOADS[HEAD]
+    d = synth.workload_inputs(w, device=dev, seed=synth.SEED_BASE + HEAD + 7919 * rank)
+    B, k, V = d["B"], d["k"], d["V"]
+    n_total = B * k  # every request drafts k tokens in this workload
+    elem = w.elem_bytes
+    stream = torch.cuda.Stream(device=dev)
+    ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                     device=dev)
+    outs = dict(out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
+                out_accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                out_p_draft=torch.empty((B, k), dtype=torch.float32, device=dev),
+                out_q_draft=torch.empty((B, k), dtype=torch.float32, device=dev),
+                out_resid_mass=torch.empty((B,), dtype=torch.float32, device=dev))
+
+    def step():
+        sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], d["T"],
+                              d["num_draft"], workspace=ws, stream=stream, **outs)
+
+    # ---- timed region: K steps, barrier + synchronize on both sides ----
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                a.record(stream)
+                step()
+                b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    per = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(per)
+    mean_ms = total_ms / len(per)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = t.item()
+    acc = outs["out_accept_len"].float().mean().item()
+
+    # ---- end to end through the public call: pinned host inputs in, results out ----
+    h_t = d["target"].cpu().pin_memory()
+    h_d = d["draft"].cpu().pin_memory()
+    h_x = d["draft_tokens"].cpu().pin_memory()
+    h_u = d["uniforms"].cpu().pin_memory()
+    d_t, d_d = torch.empty_like(d["target"]), torch.empty_like(d["draft"])
+    d_x, d_u = torch.empty_like(d["draft_tokens"]), torch.empty_like(d["uniforms"])
+    h_out = {kk: torch.empty(v.shape, dtype=v.dtype).pin_memory() for kk, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in (h_t, h_d, h_x, h_u))
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            d_t.copy_(h_t, non_blocking=True)
+            d_d.copy_(h_d, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_u.copy_(h_u, non_blocking=True)
+            sv.spec_verify_sample(d_t, d_d, d_x, d_u, d["T"], None, workspace=ws, stream=stream,
+                                  **outs)
+            for kk, v in outs.items():
+                h_out[kk].copy_(v, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = t.item()
+    del h_t, h_d, d_t, d_d
+
+    peak, peak_kind = measured_peaks()
+    abytes = sample_bytes(n_total, B, k, V, elem)
+    achieved = abytes / (mean_ms * 1e-3) / 1e9
+    value = world * n_total * args.steps / (total_ms * 1e-3)
+    e2e_value = world * n_total * e2e_steps / (e2e_total * 1e-3)
+
+    rows = {}
+    if rank == 0 and not args.no_rows:
+        rows = secondary_rows(args, dev, stream, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(d, w, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "positions/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and value distributions of the workload)",
+            "config": {
+                "workload": f"sampled verify {w.name}: B={B}, k={k}, V={V}, bf16 logits, T={w.T}, "
+                            "z_p~N(0,2.5^2), z_q=0.6 z_p+N(0,1.5^2)",
+                "global_batch": B * world,
+                "draft_positions_per_step": n_total * world,
+                "logit_bytes_per_step": abytes,
+                "l2": "inputs 2.23 GB per step, 17x the 129 MB L2: no flush needed",
+                "parallelism": f"request-sharded replicas x{world}" if world > 1 else "single GPU",
+            },
+            "logit_gbs": achieved,
+            "mean_accept_len": acc,
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "sample_kernel<BF16>",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                               if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": profiled_traffic("sample_kernel", "b512_k8_v128256_bf16"),
+                "algorithmic_bytes_per_launch": abytes,
+                "launch_ms": mean_ms,
+            },
+            "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "wall_s_timed": wall,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if rows:
+            line["rows"] = rows
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def secondary_rows(args, dev, stream, peak):
+    """Event-timed launches of the other calls of the path on their own workloads."""
+    import torch
+
+    import speculative_decoding_verification_17_gb300 as sv
+    import synth
+
+    steps = max(5, min(args.steps, 20))
+    flush = make_flush(dev)
+    rows = {}
+
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9
+
+    # fp32 sampled verify + gate (B=256, k=4, V=151936)
+    w = synth.WORKLOADS[2]
+    d = synth.workload_inputs(w, device=dev)
+    B, k, V = d["B"], d["k"], d["V"]
+    ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_F32), dtype=torch.uint8,
+                     device=dev)
+    ms = statistics.mean(time_launches(
+        lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                      d["T"], None, workspace=ws, stream=stream),
+        steps, 3, stream))
+    nb = sample_bytes(B * k, B, k, V, 4)
+    rows["sample_b256_k4_v151936_f32"] = dict(
+        ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+        bytes=nb)
+    rows_t = d["target"].reshape(-1, V)
+    gws = torch.zeros(sv.logit_gap_gate_workspace(rows_t.shape[0], V, sv.SV_F32),
+                      dtype=torch.uint8, device=dev)
+    ms = statistics.mean(time_launches(
+        lambda: sv.logit_gap_gate(rows_t, d["tau"], d["answer_set"], workspace=gws, stream=stream),
+        steps, 3, stream))
+    nb = rows_t.numel() * 4
+    rows["gate_n1280_v151936_f32"] = dict(ms=ms, rows_per_s=rows_t.shape[0] / (ms * 1e-3),
+                                          gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak, bytes=nb)
+    del d, rows_t, ws, gws
+
+    # bf16 Zipf workload: sampled + greedy (fits in L2: flushed before every launch)
+    w = synth.WORKLOADS[1]
+    d = synth.workload_inputs(w, device=dev)
+    B, k, V = d["B"], d["k"], d["V"]
+    ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                     device=dev)
+    ms = statistics.mean(time_launches(
+        lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                      d["T"], None, workspace=ws, stream=stream),
+        steps, 3, stream, flush))
+    nb = sample_bytes(B * k, B, k, V, 2)
+    rows["sample_b64_k5_v32000_bf16_l2flushed"] = dict(
+        ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+        bytes=nb)
+    gws = torch.zeros(sv.spec_verify_greedy_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                      device=dev)
+    ms = statistics.mean(time_launches(
+        lambda: sv.spec_verify_greedy(d["target"], d["draft_tokens"], None, workspace=gws,
+                                      stream=stream),
+        steps, 3, stream, flush))
+    nb = B * (k + 1) * V * 2
+    rows["greedy_b64_k5_v32000_bf16_l2flushed"] = dict(
+        ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+        bytes=nb)
+    del d, ws, gws
+
+    # tiny fp32 case: latency
+    d = synth.workload_inputs(0, device=dev)
+    ms = statistics.mean(time_launches(
+        lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                      d["T"], None, stream=stream), steps, 3, stream, flush))
+    rows["sample_b1_k4_v1000_f32_latency"] = dict(ms=ms, us=ms * 1e3)
+
+    # n-gram proposal feeding the greedy verify (B=128, L=8192, V=32000)
+    w4 = synth.workload_inputs(4, device=dev)
+    dr, nd = sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"], w4["k"])
+    torch.cuda.synchronize()
+    tgt = synth.greedy_targets(dr, nd, w4["V"], k=w4["k"], seed=w4["seed"])
+    gws = torch.zeros(sv.spec_verify_greedy_workspace(w4["B"], w4["k"], w4["V"], sv.SV_BF16),
+                      dtype=torch.uint8, device=dev)
+    od, on = torch.empty_like(dr), torch.empty_like(nd)
+
+    def chain():
+        sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"], w4["k"],
+                         out_draft=od, out_num_draft=on, stream=stream)
+        sv.spec_verify_greedy(tgt, od, on, workspace=gws, stream=stream)
+
+    ms = statistics.mean(time_launches(chain, steps, 3, stream, flush))
+    npos = int(nd.sum().item())
+    nb = w4["history"].numel() * 4 + int((nd.clamp(min=0) + 1).sum().item()) * w4["V"] * 2
+    rows["ngram_greedy_b128_l8192_v32000_bf16_l2flushed"] = dict(
+        ms=ms, proposed_positions=npos, requests_with_proposal=int((nd > 0).sum().item()),
+        positions_per_s=npos / (ms * 1e-3), gbs=gbs(nb, ms), bytes=nb)
+    ms = statistics.mean(time_launches(
+        lambda: sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"],
+                                 w4["k"], out_draft=od, out_num_draft=on, stream=stream),
+        steps, 3, stream, flush))
+    rows["ngram_b128_l8192"] = dict(ms=ms, us=ms * 1e3)
+    return rows
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def _oracle_sample_rate(target, draft, tokens, uniforms, T, threads):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.spec_verify_sample(target, draft, tokens, None, uniforms, T, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(d, w, budget_s=15.0):
+    """The oracle, as it stands, on the host cores, over a bounded sample of the requests
+    of the same workload (inputs copied from the device)."""
+    threads = os.cpu_count() or 1
+    k = d["k"]
+    # calibrate on a few requests, then size the sample for ~budget_s of CPU time
+    n0 = min(d["B"], threads)
+    sl = slice(0, n0)
+    t = _oracle_sample_rate(d["target"][sl].cpu(), d["draft"][sl].cpu(),
+                            d["draft_tokens"][sl].cpu(), d["uniforms"][sl].cpu(), d["T"], threads)
+    cpu_per_req = t * threads / n0
+    n = int(min(d["B"], max(n0, budget_s / max(cpu_per_req, 1e-6))))
+    sl = slice(0, n)
+    t = _oracle_sample_rate(d["target"][sl].cpu(), d["draft"][sl].cpu(),
+                            d["draft_tokens"][sl].cpu(), d["uniforms"][sl].cpu(), d["T"], threads)
+    return {"value": n * k / t, "unit": "positions/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {d['B']} requests of {w.name} ({n * k} draft positions), "
+                      f"{t:.2f} s wall on {threads} threads"}
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed on the host cores on the same workload, metric and unit."""
+    if rank != 0:
+        return
+    import synth
+
+    w = synth.WORKLOADS[HEAD]
+    e = w.extra
+    threads = os.cpu_count() or 1
+    per_step = max(threads, 16)
+    d = synth.sample_inputs(per_step, w.k, w.V, w.dtype, w.T, device="cpu",
+                            seed=synth.SEED_BASE + HEAD, target_std=e["target_std"],
+                            draft_noise=e["draft_noise"], draft_scale=e["draft_scale"])
+    for _ in range(args.warmup):
+        _oracle_sample_rate(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], w.T,
+                            threads)
+    times = [_oracle_sample_rate(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], w.T,
+                                 threads) for _ in range(args.steps)]
+    total = sum(times)
+    value = per_step * w.k * args.steps / total
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; shapes and value distributions of the workload)",
+        "config": {"workload": f"sampled verify {w.name}: B={w.B}, k={w.k}, V={w.V}, bf16 logits, "
+                               f"T={w.T}; each step a bounded sample of {per_step} requests",
+                   "global_batch": per_step, "parallelism": f"{threads} host threads"},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{per_step} requests per step ({per_step * w.k} positions)"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gb300_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

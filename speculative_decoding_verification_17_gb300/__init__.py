@@ -1,0 +1,248 @@
+"""GB300-native speculative-decoding verify step.
+
+A thin Python binding over ``libspecverify.so`` (C ABI declared in
+``include/specverify.h``). Every function here only checks and marshals arguments: the
+work runs in the library's sm_103a kernels on the caller's CUDA stream. Tensors are torch
+CUDA tensors (PyTorch provides device memory and streams); the binding never computes a
+result itself and raises :class:`SVError` on any non-OK status.
+
+Calls (same names as the C ABI):
+
+- :func:`spec_verify_sample` — modified-rejection verify with residual/bonus draw.
+- :func:`spec_verify_greedy` — greedy (temperature-0) verify.
+- :func:`logit_gap_gate`     — top-1/top-2 logit-gap confidence gate.
+- :func:`ngram_propose`      — prompt-lookup n-gram draft proposer.
+
+Workspaces: pass ``workspace=`` (a zero-filled uint8 CUDA tensor of at least the size
+the matching ``*_workspace`` query returns, not shared by calls in flight at the same
+time), or let the binding keep one cached per (device, call) that it grows as needed.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _native
+
+__all__ = [
+    "SVError", "SV_F32", "SV_BF16", "SV_MAX_K", "build", "library", "version",
+    "spec_verify_sample_workspace", "spec_verify_sample",
+    "spec_verify_greedy_workspace", "spec_verify_greedy",
+    "logit_gap_gate_workspace", "logit_gap_gate", "ngram_propose",
+]
+
+SV_F32 = 0
+SV_BF16 = 1
+SV_MAX_K = 16
+
+_STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
+           4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT"}
+
+
+class SVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        L = _native.lib()
+        msg = f"{where}: {_STATUS.get(status, status)} ({L.sv_status_string(status).decode()})"
+        if status == 4:
+            msg += f", cudaError {L.sv_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    return _native.build(force=force, verbose=verbose)
+
+
+def library():
+    return _native.lib()
+
+
+def version() -> int:
+    return library().sv_version()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(name, t, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream), stream
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def _workspace(kind: str, nbytes: int, device, stream):
+    """Cached zero-filled workspace for (device, kind) of at least ``nbytes`` bytes."""
+    key = (kind, device)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            with torch.cuda.stream(stream):
+                ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+    return ws
+
+
+def _ok(status, where):
+    if status != 0:
+        raise SVError(status, where)
+
+
+# ------------------------------------------------------------------------------ sampled
+def spec_verify_sample_workspace(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_sample_workspace(B, k, V, dtype))
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
+                       num_draft=None, *, out_tokens=None, out_accept_len=None,
+                       out_p_draft=None, out_q_draft=None, out_resid_mass=None,
+                       want_probs: bool = True, workspace=None, stream=None):
+    """Sampled verify. Returns (tokens [B,k+1], accept_len [B], p_draft [B,k] | None,
+    q_draft [B,k] | None, resid_mass [B] | None)."""
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    code = _dtype_code(target_logits)
+    _check_cuda("target_logits", target_logits)
+    _check_cuda("draft_logits", draft_logits, target_logits.dtype, (B, k, V), dev)
+    _check_cuda("draft_tokens", draft_tokens, torch.int32, (B, k), dev)
+    _check_cuda("uniforms", uniforms, torch.float32, (B, k + 1), dev)
+    _check_cuda("num_draft", num_draft, torch.int32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if want_probs:
+        if out_p_draft is None:
+            out_p_draft = torch.empty((B, k), dtype=torch.float32, device=dev)
+        if out_q_draft is None:
+            out_q_draft = torch.empty((B, k), dtype=torch.float32, device=dev)
+        if out_resid_mass is None:
+            out_resid_mass = torch.empty((B,), dtype=torch.float32, device=dev)
+    _check_cuda("out_tokens", out_tokens, torch.int32, (B, k + 1), dev)
+    _check_cuda("out_accept_len", out_accept_len, torch.int32, (B,), dev)
+    _check_cuda("out_p_draft", out_p_draft, torch.float32, (B, k), dev)
+    _check_cuda("out_q_draft", out_q_draft, torch.float32, (B, k), dev)
+    _check_cuda("out_resid_mass", out_resid_mass, torch.float32, (B,), dev)
+    h, st = _stream_handle(stream)
+    need = spec_verify_sample_workspace(B, k, V, code)
+    ws = workspace if workspace is not None else _workspace("sample", need, dev, st)
+    _ok(library().spec_verify_sample(
+        _ptr(target_logits), _ptr(draft_logits), code, _ptr(draft_tokens), _ptr(num_draft),
+        _ptr(uniforms), B, k, V, float(temperature), _ptr(out_tokens), _ptr(out_accept_len),
+        _ptr(out_p_draft), _ptr(out_q_draft), _ptr(out_resid_mass), _ptr(ws), ws.numel(), h),
+        "spec_verify_sample")
+    return out_tokens, out_accept_len, out_p_draft, out_q_draft, out_resid_mass
+
+
+# ------------------------------------------------------------------------------ greedy
+def spec_verify_greedy_workspace(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_greedy_workspace(B, k, V, dtype))
+
+
+def spec_verify_greedy(target_logits, draft_tokens, num_draft=None, *, out_tokens=None,
+                       out_accept_len=None, workspace=None, stream=None):
+    """Greedy verify. Returns (tokens [B,k+1], accept_len [B])."""
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    code = _dtype_code(target_logits)
+    _check_cuda("target_logits", target_logits)
+    _check_cuda("draft_tokens", draft_tokens, torch.int32, (B, k), dev)
+    _check_cuda("num_draft", num_draft, torch.int32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check_cuda("out_tokens", out_tokens, torch.int32, (B, k + 1), dev)
+    _check_cuda("out_accept_len", out_accept_len, torch.int32, (B,), dev)
+    h, st = _stream_handle(stream)
+    need = spec_verify_greedy_workspace(B, k, V, code)
+    ws = workspace if workspace is not None else _workspace("greedy", need, dev, st)
+    _ok(library().spec_verify_greedy(
+        _ptr(target_logits), code, _ptr(draft_tokens), _ptr(num_draft), B, k, V,
+        _ptr(out_tokens), _ptr(out_accept_len), _ptr(ws), ws.numel(), h), "spec_verify_greedy")
+    return out_tokens, out_accept_len
+
+
+# ------------------------------------------------------------------------------ gate
+def logit_gap_gate_workspace(N: int, V: int, dtype: int) -> int:
+    return int(library().logit_gap_gate_workspace(N, V, dtype))
+
+
+def logit_gap_gate(logits, tau: float, answer_set=None, *, out_token=None, out_gap=None,
+                   out_fire=None, workspace=None, stream=None):
+    """Gate over the rows of ``logits`` [..., V]. Returns (token [N], gap [N], fire [N])."""
+    V = logits.shape[-1]
+    N = logits.numel() // V if V else 0
+    dev = logits.device
+    code = _dtype_code(logits)
+    _check_cuda("logits", logits)
+    if answer_set is not None:
+        _check_cuda("answer_set", answer_set, torch.int32, None, dev)
+    n_answer = 0 if answer_set is None else answer_set.numel()
+    if out_token is None:
+        out_token = torch.empty((N,), dtype=torch.int32, device=dev)
+    if out_gap is None:
+        out_gap = torch.empty((N,), dtype=torch.float32, device=dev)
+    if out_fire is None:
+        out_fire = torch.empty((N,), dtype=torch.uint8, device=dev)
+    _check_cuda("out_token", out_token, torch.int32, (N,), dev)
+    _check_cuda("out_gap", out_gap, torch.float32, (N,), dev)
+    _check_cuda("out_fire", out_fire, torch.uint8, (N,), dev)
+    h, st = _stream_handle(stream)
+    need = logit_gap_gate_workspace(N, V, code)
+    ws = workspace if workspace is not None else _workspace("gate", need, dev, st)
+    _ok(library().logit_gap_gate(
+        _ptr(logits), code, N, V, float(tau), _ptr(answer_set), n_answer, _ptr(out_token),
+        _ptr(out_gap), _ptr(out_fire), _ptr(ws), ws.numel(), h), "logit_gap_gate")
+    return out_token, out_gap, out_fire
+
+
+# ------------------------------------------------------------------------------ n-gram
+def ngram_propose(history, hist_len, n_max: int, n_min: int, k: int, *, out_draft=None,
+                  out_num_draft=None, stream=None):
+    """Prompt-lookup proposer. Returns (draft [B,k] int32, num_draft [B] int32)."""
+    B, L_max = history.shape
+    dev = history.device
+    _check_cuda("history", history, torch.int32)
+    _check_cuda("hist_len", hist_len, torch.int32, (B,), dev)
+    if out_draft is None:
+        out_draft = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if out_num_draft is None:
+        out_num_draft = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check_cuda("out_draft", out_draft, torch.int32, (B, k), dev)
+    _check_cuda("out_num_draft", out_num_draft, torch.int32, (B,), dev)
+    h, _ = _stream_handle(stream)
+    _ok(library().ngram_propose(_ptr(history), _ptr(hist_len), B, L_max, n_max, n_min, k,
+                                _ptr(out_draft), _ptr(out_num_draft), h), "ngram_propose")
+    return out_draft, out_num_draft

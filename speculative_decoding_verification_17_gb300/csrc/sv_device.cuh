@@ -1,0 +1,193 @@
+// sv_device.cuh — device building blocks shared by the verify, gate and proposer kernels.
+//
+// Work decomposition used by every row kernel: a logit row of V entries is cut into
+// chunks of kChunkBytes (32 KiB: 8192 fp32 or 16384 bf16 logits). One CTA of kThreads
+// threads reduces one (row, chunk) unit straight from HBM into registers: every thread
+// issues kVecPerThread independent 16-byte loads at once (a warp reads 512 contiguous
+// bytes per load instruction), so a CTA keeps 32 KiB in flight. Partial results go to a
+// caller-owned workspace; the CTA that finishes last for a row (an atomic counter, no
+// waiting) merges them, and the CTA that finishes last for a request finishes the
+// request. No CTA ever waits for another one.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThread = 8;
+constexpr int kChunkBytes = kThreads * kVecPerThread * 16;  // 32 KiB
+constexpr int kNoIndex = 0x7fffffff;
+
+// ---- element types -------------------------------------------------------------------------
+struct F32 {
+  using raw = float;
+  static constexpr int kPerVec = 4;                       // logits per 16-byte vector
+  static constexpr int kChunk = kChunkBytes / 4;          // logits per chunk
+  static constexpr uint32_t kNegInfBits = 0xff800000u;
+  static constexpr uint32_t kNaNBits = 0x7fc00000u;
+  __device__ static __forceinline__ float get(const uint4& v, int l) {
+    const uint32_t w = l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w;
+    return __uint_as_float(w);
+  }
+  __device__ static __forceinline__ float load1(const void* row, int64_t j) {
+    return __ldg(static_cast<const float*>(row) + j);
+  }
+  __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
+    return __float_as_uint(load1(row, j));
+  }
+};
+
+struct BF16 {
+  using raw = uint16_t;
+  static constexpr int kPerVec = 8;
+  static constexpr int kChunk = kChunkBytes / 2;
+  static constexpr uint32_t kNegInfBits = 0xff80u;
+  static constexpr uint32_t kNaNBits = 0x7fc0u;
+  // bf16 is the upper half of a binary32: widening is a shift, exact.
+  __device__ static __forceinline__ float get(const uint4& v, int l) {
+    const uint32_t w = (l >> 1) == 0 ? v.x : (l >> 1) == 1 ? v.y : (l >> 1) == 2 ? v.z : v.w;
+    return __uint_as_float((l & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  __device__ static __forceinline__ float load1(const void* row, int64_t j) {
+    const uint16_t b = __ldg(static_cast<const unsigned short*>(row) + j);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
+    return static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(row) + j));
+  }
+};
+
+// ---- loads ---------------------------------------------------------------------------------
+// Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2 fetch granularity.
+// L2 keeps its normal eviction priority so a rejected row pair is still there when the
+// request's finishing CTA re-reads it.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// Vector slot `it` of thread `tid` holds logits j0 + (it*kThreads + tid)*kPerVec + [0, kPerVec)
+// of the chunk [j0, j1). Slots past j1 are filled with `pad` (a raw bit pattern). When the
+// row start is not 16-byte aligned every logit is fetched on its own.
+template <typename E>
+__device__ __forceinline__ void load_chunk(const void* row, int64_t j0, int64_t j1,
+                                           bool aligned, uint32_t pad, uint4 (&v)[kVecPerThread]) {
+  const int tid = threadIdx.x;
+  const char* base = static_cast<const char*>(row);
+  constexpr int kEB = 16 / E::kPerVec;  // bytes per logit
+#pragma unroll
+  for (int it = 0; it < kVecPerThread; ++it) {
+    const int64_t j = j0 + (int64_t)(it * kThreads + tid) * E::kPerVec;
+    if (aligned && j + E::kPerVec <= j1) {
+      v[it] = ld_stream16(base + j * kEB);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (E::kPerVec == 4) {
+          w[q] = (j + q < j1) ? E::bits1(row, j + q) : pad;
+        } else {
+          const uint32_t lo = (j + 2 * q < j1) ? E::bits1(row, j + 2 * q) : pad;
+          const uint32_t hi = (j + 2 * q + 1 < j1) ? E::bits1(row, j + 2 * q + 1) : pad;
+          w[q] = lo | (hi << 16);
+        }
+      }
+      v[it] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// ---- arithmetic ----------------------------------------------------------------------------
+// 2^x on the SFU (the hardware ex2 instruction, flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Order-preserving map of a non-NaN float onto int32 (for integer max reductions).
+__device__ __forceinline__ int f2key(float f) {
+  const int i = __float_as_int(f);
+  return i ^ ((i >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float key2f(int k) {
+  return __int_as_float(k ^ ((k >> 31) & 0x7fffffff));
+}
+
+// Error-free sum of two floats (Knuth's TwoSum): a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Warp sum of floats carried as an unevaluated (hi, lo) pair: every level adds exactly.
+__device__ __forceinline__ void warp_sum_compensated(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    float s, e;
+    two_sum(hi, h2, s, e);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, l2), e);
+  }
+}
+
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float warp_max_f(float x) {  // x must not be NaN
+  return key2f(__reduce_max_sync(0xffffffffu, f2key(x)));
+}
+
+// Block maximum of a non-NaN float; every thread gets the result. `red` holds kWarps floats.
+__device__ __forceinline__ float block_max_f(float x, float* red) {
+  x = warp_max_f(x);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = x;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();
+  return m;
+}
+
+// Block sum of per-thread floats, compensated within warps and finished in double.
+// Every thread gets the result. `red` holds 2*kWarps floats.
+__device__ __forceinline__ double block_sum_fd(float x, float* red) {
+  float hi = x, lo = 0.0f;
+  warp_sum_compensated(hi, lo);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red[2 * w] = hi;
+    red[2 * w + 1] = lo;
+  }
+  __syncthreads();
+  double s = 0.0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) s += (double)red[2 * i] + (double)red[2 * i + 1];
+  __syncthreads();
+  return s;
+}
+
+// ---- completion counters -------------------------------------------------------------------
+// Release this CTA's partial results and count it in; true for the CTA that arrives last.
+// Called by one thread after that thread stored the partials it publishes.
+__device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int expected) {
+  __threadfence();
+  const unsigned int prev = atomicAdd(counter, 1u);
+  return prev == expected - 1;
+}
+
+}  // namespace sv

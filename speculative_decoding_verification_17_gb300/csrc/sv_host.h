@@ -1,0 +1,113 @@
+// sv_host.h — host-side helpers of the C ABI: status bookkeeping, argument checks and the
+// workspace layouts shared by each *_workspace() query and its launcher.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// Record a CUDA error for sv_last_cuda_error() and turn it into SV_ERR_CUDA.
+sv_status cuda_fail(cudaError_t e);
+
+// Status of the launch just issued on this thread.
+inline sv_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e);
+}
+
+inline bool aligned_to(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int elem_bytes(sv_dtype d) { return d == SV_F32 ? 4 : 2; }
+
+// Logits per chunk (the unit of work of one CTA): 32 KiB of logits.
+inline int64_t chunk_elems(sv_dtype d) { return d == SV_F32 ? 8192 : 16384; }
+
+inline int64_t num_chunks(int V, sv_dtype d) {
+  const int64_t c = chunk_elems(d);
+  return (static_cast<int64_t>(V) + c - 1) / c;
+}
+
+// Partial result of one (row, chunk) unit of the sampled verify.
+struct ChunkSoftmax {
+  double S;   // sum over the chunk of 2^(z*s + c), c = fp32(-m*s)
+  float m;    // chunk maximum (raw logit)
+  float pad;
+};
+
+// Merged result of one row of the sampled verify.
+struct RowSoftmax {
+  double S;   // sum over the row of 2^((z - m) * s) evaluated exactly in the exponent
+  double px;  // probability of the row's draft token (target and draft rows i < n)
+  float m;    // row maximum (raw logit)
+  int status; // 0 ok, 1 not a distribution, 2 draft token out of range
+  double pad;
+};
+
+struct ChunkArgmax {
+  float v;  // largest logit of the chunk
+  int idx;  // its lowest index, kNoIndex when the chunk holds no comparable logit
+};
+
+struct ChunkTop2 {
+  float m1;  // largest logit
+  int i1;    // lowest index holding it (kNoIndex if none)
+  float m2;  // largest logit of the chunk with one copy of m1 removed
+  int pad;
+};
+
+// Byte offsets of the workspace regions (each 256-byte aligned).
+struct SampleLayout {
+  size_t chunk, row, resid, row_cnt, req_cnt, total;
+};
+inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
+  const size_t R = 2 * static_cast<size_t>(k) + 1;
+  const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  SampleLayout L{};
+  size_t o = 0;
+  L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkSoftmax), 256);
+  L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
+  L.resid = o;   o = round_up(o + B * nch * sizeof(double), 256);
+  L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
+  L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
+  L.total = o;
+  return L;
+}
+
+struct GreedyLayout {
+  size_t chunk, row, row_cnt, req_cnt, total;
+};
+inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
+  const size_t R = static_cast<size_t>(k) + 1;
+  const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  GreedyLayout L{};
+  size_t o = 0;
+  L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkArgmax), 256);
+  L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
+  L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
+  L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
+  L.total = o;
+  return L;
+}
+
+struct GateLayout {
+  size_t chunk, row_cnt, total;
+};
+inline GateLayout gate_layout(int N, int V, sv_dtype d) {
+  const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  GateLayout L{};
+  size_t o = 0;
+  L.chunk = o;   o = round_up(o + static_cast<size_t>(N) * nch * sizeof(ChunkTop2), 256);
+  L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
+  L.total = o;
+  return L;
+}
+
+}  // namespace sv

@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every function include/*.h declares, and validates its
+arguments on the host (no GPU needed: every call here returns before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_17_gb300 as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails or returns first
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([A-Za-z_]\w*)\s*\(([^;{}()]|\([^()]*\))*\)\s*;", text):
+            if m.group(1) not in ("sizeof",):
+                names.add(m.group(1))
+    return names
+
+
+def test_every_declared_function_is_exported():
+    L = sv.library()
+    names = declared_functions()
+    assert {"spec_verify_sample", "spec_verify_greedy", "logit_gap_gate", "ngram_propose"} <= names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings():
+    L = sv.library()
+    assert L.sv_version() > 0
+    for s in range(6):
+        assert L.sv_status_string(s)
+    assert L.sv_last_cuda_error() == 0
+
+
+def test_workspace_queries():
+    assert sv.spec_verify_sample_workspace(512, 8, 128256, sv.SV_BF16) > 0
+    assert sv.spec_verify_sample_workspace(1, 17, 100, sv.SV_F32) == 0
+    assert sv.spec_verify_greedy_workspace(128, 5, 32000, sv.SV_BF16) > 0
+    assert sv.logit_gap_gate_workspace(1280, 151936, sv.SV_F32) > 0
+    for q in (sv.spec_verify_sample_workspace(0, 4, 1000, 0),
+              sv.spec_verify_greedy_workspace(0, 4, 1000, 0), sv.logit_gap_gate_workspace(0, 10, 0)):
+        assert q >= 0
+    assert sv.spec_verify_sample_workspace(1, 4, 1, 0) == 0  # V < 2
+
+
+def _sample(**kw):
+    a = dict(t=FAKE, d=FAKE, dtype=0, x=FAKE, nd=None, u=FAKE, B=4, k=3, V=100, T=1.0, ot=FAKE,
+             oa=FAKE, op=None, oq=None, orm=None, ws=ctypes.c_void_p(0x100000), wsb=1 << 30,
+             st=None)
+    a.update(kw)
+    return sv.library().spec_verify_sample(a["t"], a["d"], a["dtype"], a["x"], a["nd"], a["u"],
+                                           a["B"], a["k"], a["V"], a["T"], a["ot"], a["oa"],
+                                           a["op"], a["oq"], a["orm"], a["ws"], a["wsb"], a["st"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), INVALID), (dict(k=0), INVALID), (dict(V=1), INVALID), (dict(dtype=7), INVALID),
+    (dict(T=0.0), INVALID), (dict(T=-1.0), INVALID), (dict(T=float("nan")), INVALID),
+    (dict(T=float("inf")), INVALID), (dict(T=1e-5), INVALID), (dict(k=17), UNSUPPORTED),
+    (dict(t=None), INVALID), (dict(x=None), INVALID), (dict(u=None), INVALID),
+    (dict(ot=None), INVALID), (dict(t=ctypes.c_void_p(0x10001)), INVALID),
+    (dict(ws=None), WORKSPACE), (dict(wsb=16), WORKSPACE), (dict(ws=ctypes.c_void_p(0x100010)), WORKSPACE),
+    (dict(B=0, t=None, d=None), OK),
+])
+def test_sample_validation(kw, status):
+    assert _sample(**kw) == status
+
+
+def test_greedy_gate_ngram_validation():
+    L = sv.library()
+    ws = ctypes.c_void_p(0x100000)
+    g = lambda **kw: L.spec_verify_greedy(kw.get("t", FAKE), kw.get("dtype", 1), FAKE, None,
+                                          kw.get("B", 2), kw.get("k", 3), kw.get("V", 50), FAKE,
+                                          FAKE, kw.get("ws", ws), kw.get("wsb", 1 << 30), None)
+    assert g(B=-1) == INVALID and g(k=0) == INVALID and g(V=1) == INVALID
+    assert g(k=17) == UNSUPPORTED and g(t=None) == INVALID and g(wsb=0) == WORKSPACE
+    assert g(B=0, t=None) == OK
+    gt = lambda **kw: L.logit_gap_gate(kw.get("z", FAKE), kw.get("dtype", 0), kw.get("N", 3),
+                                       kw.get("V", 10), 1.0, kw.get("A", FAKE), kw.get("nA", 2),
+                                       FAKE, FAKE, FAKE, kw.get("ws", ws), kw.get("wsb", 1 << 30),
+                                       None)
+    assert gt(N=-1) == INVALID and gt(V=1) == INVALID and gt(nA=-1) == INVALID
+    assert gt(A=None) == INVALID and gt(z=None) == INVALID and gt(wsb=8) == WORKSPACE
+    assert gt(N=0, z=None) == OK
+    ng = lambda **kw: L.ngram_propose(kw.get("h", FAKE), FAKE, kw.get("B", 2), kw.get("L", 64),
+                                      kw.get("nmax", 4), kw.get("nmin", 2), kw.get("k", 5),
+                                      FAKE, FAKE, None)
+    assert ng(nmin=0) == INVALID and ng(nmax=1, nmin=2) == INVALID and ng(nmax=65) == INVALID
+    assert ng(k=0) == INVALID and ng(k=65) == INVALID and ng(L=0) == INVALID
+    assert ng(L=1 << 24) == INVALID and ng(h=None) == INVALID and ng(B=-1) == INVALID
+    assert ng(B=0, h=None) == OK
+
+
+def test_binding_raises_on_bad_input():
+    import torch
+
+    with pytest.raises((TypeError, ValueError)):
+        sv.spec_verify_greedy(torch.zeros(2, 3, 10), torch.zeros(2, 2, dtype=torch.int32))
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_17_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            text = open(path).read()
+            assert "oracle" not in text.lower(), path
