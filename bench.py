@@ -186,7 +186,8 @@ def gb300_arm(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     w = synth.WORKLOADS[HEAD]
-    d = synth.workload_inputs(w, device=dev, seed=synth.SEED_BASE + HEAD + 7919 * rank)
+    d = synth.workload_inputs(w, device=dev, seed=synth.SEED_BASE + HEAD + 7919 * rank,
+                              B=args.requests)
     B, k, V = d["B"], d["k"], d["V"]
     n_total = B * k  # every request drafts k tokens in this workload
     elem = w.elem_bytes
@@ -233,6 +234,9 @@ def gb300_arm(args, rank, world, local_rank):
     acc = outs["out_accept_len"].float().mean().item()
 
     # ---- end to end through the public call: pinned host inputs in, results out ----
+    if args.no_e2e:
+        return finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, acc,
+                           clk, wall, None)
     h_t = d["target"].cpu().pin_memory()
     h_d = d["draft"].cpu().pin_memory()
     h_x = d["draft_tokens"].cpu().pin_memory()
@@ -263,12 +267,22 @@ def gb300_arm(args, rank, world, local_rank):
         e2e_total = t.item()
     del h_t, h_d, d_t, d_d
 
+    e2e = {"value": world * n_total * e2e_steps / (e2e_total * 1e-3), "unit": "positions/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": e2e_total / e2e_steps}
+    return finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, acc, clk,
+                       wall, e2e)
+
+
+def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, acc, clk, wall,
+                e2e):
+    B, k, V = d["B"], d["k"], d["V"]
+    n_total = B * k
+    elem = w.elem_bytes
     peak, peak_kind = measured_peaks()
     abytes = sample_bytes(n_total, B, k, V, elem)
     achieved = abytes / (mean_ms * 1e-3) / 1e9
     value = world * n_total * args.steps / (total_ms * 1e-3)
-    e2e_value = world * n_total * e2e_steps / (e2e_total * 1e-3)
-
     rows = {}
     if rank == 0 and not args.no_rows:
         rows = secondary_rows(args, dev, stream, peak)
@@ -298,7 +312,7 @@ def gb300_arm(args, rank, world, local_rank):
                 "global_batch": B * world,
                 "draft_positions_per_step": n_total * world,
                 "logit_bytes_per_step": abytes,
-                "l2": "inputs 2.23 GB per step, 17x the 129 MB L2: no flush needed",
+                "l2": f"inputs {abytes / 1e9:.2f} GB per step vs the 129 MB L2: no flush",
                 "parallelism": f"request-sharded replicas x{world}" if world > 1 else "single GPU",
             },
             "logit_gbs": achieved,
@@ -316,8 +330,7 @@ def gb300_arm(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": abytes,
                 "launch_ms": mean_ms,
             },
-            "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / e2e_steps},
+            "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clocks,
             "wall_s_timed": wall,
@@ -516,6 +529,9 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--requests", type=int, default=None,
+                    help="batch size of the headline workload (default: its own, 512)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     rank = int(os.environ.get("RANK", "0"))

@@ -35,9 +35,9 @@
  *    of token j. -inf is a legal logit (a masked token: probability 0).
  *  - Workspaces: the sampled verify, the greedy verify and the gate need a caller-owned
  *    device workspace of at least the size their *_workspace() query returns, 256-byte
- *    aligned. It MUST be zero-filled before its first use (e.g. cudaMemsetAsync once); every
- *    call leaves it ready for the next call (its counters return to zero), so it is not
- *    cleared again. Two calls in flight at the same time must not share a workspace.
+ *    aligned. It needs no initialisation and may be reused across calls of any shape: each
+ *    call first clears the counters it uses (an asynchronous memset on `stream`, ahead of
+ *    its one kernel launch). Two calls in flight at the same time must not share one.
  *  - Nothing here is thread-unsafe on the host; the only process-wide state is the value
  *    returned by sv_last_cuda_error(), which is per host thread.
  */

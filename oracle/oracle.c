@@ -112,6 +112,19 @@ static int inverse_cdf(const double* w, int V, double W, double u, double* margi
   return last;
 }
 
+/* The token the inverse-CDF draw selects for an absolute target (clamped to the first or
+ * last token with positive weight at either end). */
+static int select_at(const double* w, int V, double target) {
+  double run = 0.0;
+  int last = -1;
+  for (int j = 0; j < V; ++j) {
+    run += w[j];
+    if (w[j] > 0.0) last = j;
+    if (run > target && w[j] > 0.0) return j;
+  }
+  return last;
+}
+
 static int uniform_ok(float u) { return u >= 0.0f && u < 1.0f; }
 
 int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
@@ -119,7 +132,8 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
                               const float* uniforms, int B, int k, int V, double T,
                               int32_t* out_tokens, int32_t* out_accept_len, double* out_p,
                               double* out_q, double* out_resid, int32_t* out_flag_pos,
-                              double* out_margin, int r0, int r1) {
+                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi, int r0,
+                              int r1) {
   if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 2 || !(T > 0.0) || !isfinite(T) ||
       (dtype != 0 && dtype != 1))
     return -1;
@@ -140,6 +154,8 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
     if (out_resid) out_resid[r] = 0.0;
     if (out_flag_pos) out_flag_pos[r] = -1;
     if (out_margin) out_margin[r] = INFINITY;
+    if (out_t_lo) out_t_lo[r] = -1;
+    if (out_t_hi) out_t_hi[r] = -1;
 
     const int n = num_draft ? num_draft[r] : k;
     int err = (n < 0 || n > k);
@@ -221,6 +237,9 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
     const int t = inverse_cdf(w, V, W, (double)u[k], &smg);
     if (smg < min_margin) min_margin = smg;
     if (smg < ORACLE_TIE_MARGIN && flag < 0) flag = a;
+    /* every token a target within the tie margin of u*W could select */
+    if (out_t_lo) out_t_lo[r] = select_at(w, V, (double)u[k] * W - ORACLE_TIE_MARGIN * W);
+    if (out_t_hi) out_t_hi[r] = select_at(w, V, (double)u[k] * W + ORACLE_TIE_MARGIN * W);
 
     for (int i = 0; i < a; ++i) tok[i] = x[i];
     tok[a] = t;

@@ -34,14 +34,18 @@ int oracle_row_softmax(const void* row, int dtype, int V, double T, double* p_ou
  *   out_resid[r]                                W when a < n_r, else 0;
  *   out_flag_pos[r]  the first position whose decision had a near tie (the accept test of
  *                    position i, or the draw that emitted token a), or -1;
- *   out_margin[r]    the smallest margin among the decisions that fixed the result.
+ *   out_margin[r]    the smallest margin among the decisions that fixed the result;
+ *   out_t_lo[r], out_t_hi[r]  the first and last token the draw selects for any target
+ *                    within ORACLE_TIE_MARGIN * W of u[r, k] * W (equal when no near tie).
+ * Every output pointer past out_accept_len may be NULL.
  * A request with a data error gets accept_len -1, tokens -1, p/q/resid NaN, flag -1. */
 int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
                               const int32_t* draft_tokens, const int32_t* num_draft,
                               const float* uniforms, int B, int k, int V, double T,
                               int32_t* out_tokens, int32_t* out_accept_len, double* out_p,
                               double* out_q, double* out_resid, int32_t* out_flag_pos,
-                              double* out_margin, int r0, int r1);
+                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi, int r0,
+                              int r1);
 
 /* Greedy verify; outputs as the library's spec_verify_greedy. */
 int oracle_spec_verify_greedy(const void* target, int dtype, const int32_t* draft_tokens,

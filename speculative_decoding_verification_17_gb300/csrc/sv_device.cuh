@@ -38,6 +38,15 @@ struct F32 {
   __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
     return __float_as_uint(load1(row, j));
   }
+  // Largest logit of the thread's vectors (NaN ignored, as fmaxf does).
+  __device__ static __forceinline__ float max_all(const uint4 (&v)[8]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int it = 0; it < 8; ++it)
+      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(v[it].x), __uint_as_float(v[it].y)),
+                         fmaxf(__uint_as_float(v[it].z), __uint_as_float(v[it].w))));
+    return m;
+  }
 };
 
 struct BF16 {
@@ -57,6 +66,24 @@ struct BF16 {
   }
   __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
     return static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(row) + j));
+  }
+  // Largest logit of the thread's vectors, reduced on packed bf16 pairs (max.bf16x2 returns
+  // the other operand when one is NaN, as fmaxf does); exact, no widening until the end.
+  __device__ static __forceinline__ float max_all(const uint4 (&v)[8]) {
+    uint32_t m = v[0].x;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      if (it > 0) m = max2(m, v[it].x);
+      m = max2(m, v[it].y);
+      m = max2(m, v[it].z);
+      m = max2(m, v[it].w);
+    }
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
   }
 };
 
@@ -163,9 +190,11 @@ __device__ __forceinline__ float block_max_f(float x, float* red) {
   return m;
 }
 
-// Block sum of per-thread floats, compensated within warps and finished in double.
-// Every thread gets the result. `red` holds 2*kWarps floats.
-__device__ __forceinline__ double block_sum_fd(float x, float* red) {
+// Block sum of per-thread floats: compensated (exact) within each warp, the kWarps warp
+// results merged in double by thread 0 only (GB300's FP64 rate is a small fraction of its
+// FP32 rate, so no other thread touches double here). The result is valid in thread 0.
+// `red` holds 2*kWarps floats. Contains one barrier; every thread must call it.
+__device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
   float hi = x, lo = 0.0f;
   warp_sum_compensated(hi, lo);
   const int w = threadIdx.x >> 5;
@@ -175,15 +204,17 @@ __device__ __forceinline__ double block_sum_fd(float x, float* red) {
   }
   __syncthreads();
   double s = 0.0;
+  if (threadIdx.x == 0) {
 #pragma unroll
-  for (int i = 0; i < kWarps; ++i) s += (double)red[2 * i] + (double)red[2 * i + 1];
-  __syncthreads();
+    for (int i = 0; i < kWarps; ++i) s += (double)red[2 * i] + (double)red[2 * i + 1];
+  }
   return s;
 }
 
 // ---- completion counters -------------------------------------------------------------------
 // Release this CTA's partial results and count it in; true for the CTA that arrives last.
-// Called by one thread after that thread stored the partials it publishes.
+// Called by one thread after that thread stored the partials it publishes. The counters
+// are cleared by the host call (an async memset on the same stream) before every launch.
 __device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int expected) {
   __threadfence();
   const unsigned int prev = atomicAdd(counter, 1u);

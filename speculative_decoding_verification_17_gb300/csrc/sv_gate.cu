@@ -141,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 4) gate_kernel(const GateArgs A) {
         A.out_gap[row] = (float)gap;
         A.out_fire[row] = fire ? 1 : 0;
       }
-      A.row_cnt[row] = 0;
     }
   }
 }
@@ -190,6 +189,8 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   A.chunk = reinterpret_cast<ChunkTop2*>(ws + L.chunk);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws + L.row_cnt, 0, L.total - L.row_cnt, st);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (dtype == SV_F32)
     gate_kernel<F32><<<(unsigned)units, kThreads, 0, st>>>(A);
   else

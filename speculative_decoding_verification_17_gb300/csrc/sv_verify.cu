@@ -270,7 +270,6 @@ __device__ void finish_sample_request(const SampleArgs& A, int r, int n, bool n_
     if (tid == 0) {
       A.out_accept_len[r] = -1;
       if (A.out_resid) A.out_resid[r] = __int_as_float(0x7fc00000);
-      A.req_cnt[r] = 0;
     }
     return;
   }
@@ -292,6 +291,7 @@ __device__ void finish_sample_request(const SampleArgs& A, int r, int n, bool n_
     wf.ip = (float)(1.0 / (tp.S * exp2((double)wf.cp + (double)tp.m * (double)s)));
     wf.iq = (float)(1.0 / (dq.S * exp2((double)wf.cq + (double)dq.m * (double)s)));
     double* rm = A.resid + (int64_t)r * A.nch;
+    double Wt0 = 0.0;  // accumulated by thread 0
     for (int c = 0; c < A.nch; ++c) {
       const int64_t j0 = (int64_t)c * E::kChunk;
       const int64_t j1 = j0 + E::kChunk < A.V ? j0 + E::kChunk : A.V;
@@ -310,11 +310,16 @@ __device__ void finish_sample_request(const SampleArgs& A, int r, int n, bool n_
             if (j + l < j1) acc += wf(E::load1(rp, j + l), E::load1(rq, j + l));
         }
       }
-      const double Rc = block_sum_fd(acc, red);
-      if (tid == 0) rm[c] = Rc;
-      W += Rc;
+      const double Rc = block_sum_fd_t0(acc, red);
+      if (tid == 0) {
+        rm[c] = Rc;
+        Wt0 += Rc;
+      }
+      __syncthreads();  // red[] is rewritten by the next chunk
     }
-    __syncthreads();  // rm[] visible to the whole block
+    if (tid == 0) fs.W = Wt0;
+    __syncthreads();  // rm[] and W visible to the whole block
+    W = fs.W;
     if (W > 0.0) {
       const double target = (double)__ldg(u + A.k) * W;
       if (tid < 32) {
@@ -384,7 +389,6 @@ __device__ void finish_sample_request(const SampleArgs& A, int r, int n, bool n_
   if (tid == 0) {
     A.out_accept_len[r] = a;
     if (A.out_resid) A.out_resid[r] = a < n ? (float)W : 0.0f;
-    A.req_cnt[r] = 0;
   }
 }
 
@@ -416,12 +420,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs A)
   // ---- pass 1: chunk maximum and chunk sum ----
   uint4 v[kVecPerThread];
   load_chunk<E>(rowp, j0, j1, A.aligned, E::kNegInfBits, v);
-  float tmax = -INFINITY;
-#pragma unroll
-  for (int it = 0; it < kVecPerThread; ++it)
-#pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) tmax = fmaxf(tmax, E::get(v[it], l));
-  const float m = block_max_f(tmax, red);
+  const float m = block_max_f(E::max_all(v), red);
   double S;
   if (m == -INFINITY || m == INFINITY) {
     // no finite logit here: a masked chunk carries no mass; NaN or +inf poison the row
@@ -441,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs A)
     for (int w = kVecPerThread / 2; w >= 1; w >>= 1)
 #pragma unroll
       for (int l = 0; l < w; ++l) part[l] = part[l] + part[l + w];
-    S = block_sum_fd(part[0], red);
+    S = block_sum_fd_t0(part[0], red);  // valid in thread 0, the only reader
   }
 
   const int64_t rid = (int64_t)r * R + slot;
@@ -487,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs A)
       rs->px = px;
       rs->m = mrow;
       rs->status = status;
-      A.row_cnt[rid] = 0;
       s_req_last = arrive_last(A.req_cnt + r, (unsigned)(2 * n + 1));
     }
   }
@@ -602,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 4) greedy_kernel(const GreedyArgs A)
     warp_argmax(bv, bi);
     if (lane == 0) {
       A.row[rid] = bi == kNoIndex ? -1 : bi;
-      A.row_cnt[rid] = 0;
       s_req_last = arrive_last(A.req_cnt + r, (unsigned)(n + 1));
     }
   }
@@ -639,7 +636,6 @@ __global__ void __launch_bounds__(kThreads, 4) greedy_kernel(const GreedyArgs A)
     }
     if (lane == 0) {
       A.out_accept_len[r] = err ? -1 : a;
-      A.req_cnt[r] = 0;
     }
   }
 }
@@ -719,6 +715,9 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // counters (the last two regions) start every call at zero
+  cudaError_t e = cudaMemsetAsync(ws + L.row_cnt, 0, L.total - L.row_cnt, st);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (dtype == SV_F32)
     sample_kernel<F32><<<(unsigned)units, kThreads, 0, st>>>(A);
   else
@@ -771,6 +770,8 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws + L.row_cnt, 0, L.total - L.row_cnt, st);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (dtype == SV_F32)
     greedy_kernel<F32><<<(unsigned)units, kThreads, 0, st>>>(A);
   else

@@ -17,7 +17,8 @@ PROB_ATOL = 1e-5
 def compare_sample(gpu: dict, orc: dict, requests) -> dict:
     """gpu: numpy arrays tokens, accept_len, p, q, resid and n (the per-request draft
     counts) over the full batch; orc: the oracle's output."""
-    stats = dict(requests=0, flagged=0, errors=0, max_p_err=0.0, max_resid_err=0.0)
+    stats = dict(requests=0, flagged=0, flagged_differ=0, errors=0, max_p_err=0.0,
+                 max_resid_err=0.0)
     for r in requests:
         stats["requests"] += 1
         oa, ga = int(orc["accept_len"][r]), int(gpu["accept_len"][r])
@@ -36,6 +37,14 @@ def compare_sample(gpu: dict, orc: dict, requests) -> dict:
             stats["flagged"] += 1
             assert np.array_equal(gpu["tokens"][r, :f], orc["tokens"][r, :f]), f"request {r}"
             assert ga >= f and oa >= f, f"request {r}: flagged at {f}, a GPU {ga} oracle {oa}"
+            if f == oa and ga == oa:
+                # a near tie in the draw: the GPU token must be one the tie window allows
+                t = int(gpu["tokens"][r, oa])
+                assert orc["t_lo"][r] <= t <= orc["t_hi"][r], (
+                    f"request {r}: drawn {t} outside the tie window "
+                    f"[{orc['t_lo'][r]}, {orc['t_hi'][r]}]")
+            if ga != oa or not np.array_equal(gpu["tokens"][r], orc["tokens"][r]):
+                stats["flagged_differ"] += 1
         n = int(gpu["n"][r])
         for key in ("p", "q"):
             if gpu.get(key) is not None:

@@ -265,6 +265,13 @@ def test_inverse_cdf_boundaries():
         out = oracle.spec_verify_sample(zt, zd, x, nd, u, 1.0)
         assert out["accept_len"][0] == 0 and out["tokens"][0, 0] == want, uk
         assert out["tokens"][0, 1] == -1
+        # the tie window spans both neighbours exactly at a CDF boundary
+        lo, hi = out["t_lo"][0], out["t_hi"][0]
+        near = min(abs(float(uk) - b) for b in (0.25, 0.5, 0.75)) < 1e-6
+        if near:
+            assert lo <= want <= hi and hi - lo == 1 and out["flag_pos"][0] == 0, uk
+        else:
+            assert (lo, hi) == (want, want) and out["flag_pos"][0] == -1, uk
 
 
 def test_masked_tokens_are_never_drawn():
