@@ -1,13 +1,15 @@
 // sv_device.cuh — device building blocks shared by the verify, gate and proposer kernels.
 //
 // Work decomposition used by every row kernel: a logit row of V entries is cut into
-// chunks of kChunkBytes (32 KiB: 8192 fp32 or 16384 bf16 logits). One CTA of kThreads
-// threads reduces one (row, chunk) unit straight from HBM into registers: every thread
-// issues kVecPerThread independent 16-byte loads at once (a warp reads 512 contiguous
-// bytes per load instruction), so a CTA keeps 32 KiB in flight. Partial results go to a
-// caller-owned workspace; the CTA that finishes last for a row (an atomic counter, no
-// waiting) merges them, and the CTA that finishes last for a request finishes the
-// request. No CTA ever waits for another one.
+// chunks of kChunkBytes (32 KiB: 8192 fp32 or 16384 bf16 logits). A group of kThreads
+// "consumer" threads reduces one (row, chunk) unit at a time from registers: thread t holds
+// the 16-byte vectors it*kThreads + t, it < kVecPerThread, of the chunk. Partial results go
+// to a caller-owned workspace; the consumer group that finishes last for a row (an atomic
+// counter, no waiting) merges them, and the one that finishes last for a request finishes
+// the request. No CTA ever waits for another one.
+//
+// Block-level synchronisation among the consumers uses named barrier 1 over kThreads
+// threads, so a kernel may add a producer warp that never joins those barriers.
 #pragma once
 
 #include <cstdint>
@@ -15,17 +17,33 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // consumer threads
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = 8;
 constexpr int kChunkBytes = kThreads * kVecPerThread * 16;  // 32 KiB
 constexpr int kNoIndex = 0x7fffffff;
 
+// ---- consumer-group barriers ---------------------------------------------------------------
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// Barrier that also returns whether any consumer thread passed pred != 0.
+__device__ __forceinline__ bool cbar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q;\n"
+      "  setp.ne.u32 p, %1, 0;\n"
+      "  bar.red.or.pred q, 1, %2, p;\n"
+      "  selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kThreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---- element types -------------------------------------------------------------------------
 struct F32 {
-  using raw = float;
-  static constexpr int kPerVec = 4;                       // logits per 16-byte vector
-  static constexpr int kChunk = kChunkBytes / 4;          // logits per chunk
+  static constexpr int kPerVec = 4;               // logits per 16-byte vector
+  static constexpr int kChunk = kChunkBytes / 4;  // logits per chunk
   static constexpr uint32_t kNegInfBits = 0xff800000u;
   static constexpr uint32_t kNaNBits = 0x7fc00000u;
   __device__ static __forceinline__ float get(const uint4& v, int l) {
@@ -38,11 +56,14 @@ struct F32 {
   __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
     return __float_as_uint(load1(row, j));
   }
+  __device__ static __forceinline__ uint4 pad_vec(uint32_t pad) {
+    return make_uint4(pad, pad, pad, pad);
+  }
   // Largest logit of the thread's vectors (NaN ignored, as fmaxf does).
-  __device__ static __forceinline__ float max_all(const uint4 (&v)[8]) {
+  __device__ static __forceinline__ float max_all(const uint4 (&v)[kVecPerThread]) {
     float m = -INFINITY;
 #pragma unroll
-    for (int it = 0; it < 8; ++it)
+    for (int it = 0; it < kVecPerThread; ++it)
       m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(v[it].x), __uint_as_float(v[it].y)),
                          fmaxf(__uint_as_float(v[it].z), __uint_as_float(v[it].w))));
     return m;
@@ -50,7 +71,6 @@ struct F32 {
 };
 
 struct BF16 {
-  using raw = uint16_t;
   static constexpr int kPerVec = 8;
   static constexpr int kChunk = kChunkBytes / 2;
   static constexpr uint32_t kNegInfBits = 0xff80u;
@@ -67,12 +87,21 @@ struct BF16 {
   __device__ static __forceinline__ uint32_t bits1(const void* row, int64_t j) {
     return static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(row) + j));
   }
+  __device__ static __forceinline__ uint4 pad_vec(uint32_t pad) {
+    const uint32_t w = pad | (pad << 16);
+    return make_uint4(w, w, w, w);
+  }
+  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
   // Largest logit of the thread's vectors, reduced on packed bf16 pairs (max.bf16x2 returns
-  // the other operand when one is NaN, as fmaxf does); exact, no widening until the end.
-  __device__ static __forceinline__ float max_all(const uint4 (&v)[8]) {
+  // the other operand when one is NaN, as fmaxf does); exact, widened only at the end.
+  __device__ static __forceinline__ float max_all(const uint4 (&v)[kVecPerThread]) {
     uint32_t m = v[0].x;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < kVecPerThread; ++it) {
       if (it > 0) m = max2(m, v[it].x);
       m = max2(m, v[it].y);
       m = max2(m, v[it].z);
@@ -80,17 +109,12 @@ struct BF16 {
     }
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
   }
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
 };
 
 // ---- loads ---------------------------------------------------------------------------------
 // Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2 fetch granularity.
 // L2 keeps its normal eviction priority so a rejected row pair is still there when the
-// request's finishing CTA re-reads it.
+// request's finishing consumers re-read it.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -99,35 +123,36 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
-// Vector slot `it` of thread `tid` holds logits j0 + (it*kThreads + tid)*kPerVec + [0, kPerVec)
-// of the chunk [j0, j1). Slots past j1 are filled with `pad` (a raw bit pattern). When the
-// row start is not 16-byte aligned every logit is fetched on its own.
+// One 16-byte vector of logits j .. j+kPerVec-1 of a row (entries at or past j1 read as
+// `pad`); fetched whole when the row is 16-byte aligned, else one logit at a time.
 template <typename E>
-__device__ __forceinline__ void load_chunk(const void* row, int64_t j0, int64_t j1,
-                                           bool aligned, uint32_t pad, uint4 (&v)[kVecPerThread]) {
-  const int tid = threadIdx.x;
-  const char* base = static_cast<const char*>(row);
-  constexpr int kEB = 16 / E::kPerVec;  // bytes per logit
+__device__ __forceinline__ uint4 load_vec(const void* row, int64_t j, int64_t j1, bool aligned,
+                                          uint32_t pad) {
+  if (aligned && j + E::kPerVec <= j1)
+    return ld_stream16(static_cast<const char*>(row) + j * (16 / E::kPerVec));
+  uint32_t w[4];
 #pragma unroll
-  for (int it = 0; it < kVecPerThread; ++it) {
-    const int64_t j = j0 + (int64_t)(it * kThreads + tid) * E::kPerVec;
-    if (aligned && j + E::kPerVec <= j1) {
-      v[it] = ld_stream16(base + j * kEB);
+  for (int q = 0; q < 4; ++q) {
+    if (E::kPerVec == 4) {
+      w[q] = (j + q < j1) ? E::bits1(row, j + q) : pad;
     } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (E::kPerVec == 4) {
-          w[q] = (j + q < j1) ? E::bits1(row, j + q) : pad;
-        } else {
-          const uint32_t lo = (j + 2 * q < j1) ? E::bits1(row, j + 2 * q) : pad;
-          const uint32_t hi = (j + 2 * q + 1 < j1) ? E::bits1(row, j + 2 * q + 1) : pad;
-          w[q] = lo | (hi << 16);
-        }
-      }
-      v[it] = make_uint4(w[0], w[1], w[2], w[3]);
+      const uint32_t lo = (j + 2 * q < j1) ? E::bits1(row, j + 2 * q) : pad;
+      const uint32_t hi = (j + 2 * q + 1 < j1) ? E::bits1(row, j + 2 * q + 1) : pad;
+      w[q] = lo | (hi << 16);
     }
   }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The chunk [j0, j1) of a row in the consumer layout, straight from global memory.
+template <typename E>
+__device__ __forceinline__ void load_chunk(const void* row, int64_t j0, int64_t j1,
+                                           bool aligned, uint32_t pad,
+                                           uint4 (&v)[kVecPerThread]) {
+#pragma unroll
+  for (int it = 0; it < kVecPerThread; ++it)
+    v[it] = load_vec<E>(row, j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec, j1,
+                        aligned, pad);
 }
 
 // ---- arithmetic ----------------------------------------------------------------------------
@@ -173,27 +198,38 @@ __device__ __forceinline__ double warp_sum_d(double x) {
   return x;
 }
 
+// Inclusive warp scan (Hillis-Steele) in double.
+__device__ __forceinline__ double warp_scan_d(double x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
 __device__ __forceinline__ float warp_max_f(float x) {  // x must not be NaN
   return key2f(__reduce_max_sync(0xffffffffu, f2key(x)));
 }
 
-// Block maximum of a non-NaN float; every thread gets the result. `red` holds kWarps floats.
+// Consumer-group maximum of a non-NaN float; every consumer gets it. `red`: kWarps floats.
 __device__ __forceinline__ float block_max_f(float x, float* red) {
   x = warp_max_f(x);
   const int w = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) red[w] = x;
-  __syncthreads();
+  cbar();
   float m = red[0];
 #pragma unroll
   for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
-  __syncthreads();
+  cbar();
   return m;
 }
 
-// Block sum of per-thread floats: compensated (exact) within each warp, the kWarps warp
-// results merged in double by thread 0 only (GB300's FP64 rate is a small fraction of its
-// FP32 rate, so no other thread touches double here). The result is valid in thread 0.
-// `red` holds 2*kWarps floats. Contains one barrier; every thread must call it.
+// Consumer-group sum of per-thread floats: compensated (exact) within each warp, the kWarps
+// warp results merged in double by thread 0 only (GB300's FP64 rate is a small fraction of
+// its FP32 rate, so no other thread touches double here). Valid in thread 0. `red` holds
+// 2*kWarps floats and must not be rewritten before the next consumer barrier.
 __device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
   float hi = x, lo = 0.0f;
   warp_sum_compensated(hi, lo);
@@ -202,7 +238,7 @@ __device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
     red[2 * w] = hi;
     red[2 * w + 1] = lo;
   }
-  __syncthreads();
+  cbar();
   double s = 0.0;
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -212,13 +248,75 @@ __device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
 }
 
 // ---- completion counters -------------------------------------------------------------------
-// Release this CTA's partial results and count it in; true for the CTA that arrives last.
-// Called by one thread after that thread stored the partials it publishes. The counters
-// are cleared by the host call (an async memset on the same stream) before every launch.
+// Release this group's partial results and count it in; true for the group that arrives
+// last. Called by one thread after that thread stored the partials it publishes. The
+// counters are cleared by the host call (an async memset on the same stream) before every
+// launch.
 __device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int expected) {
   __threadfence();
   const unsigned int prev = atomicAdd(counter, 1u);
   return prev == expected - 1;
+}
+
+// ---- mbarrier and bulk-copy (TMA) primitives ----------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the given phase parity of an mbarrier for at most limit_ns; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+// Bulk copy (TMA, non-tensor) of `bytes` (a multiple of 16) from 16-byte aligned global
+// memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
 }
 
 }  // namespace sv

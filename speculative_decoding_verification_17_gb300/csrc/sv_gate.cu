@@ -5,14 +5,16 @@
 // the argmax lies in the fast-answer set A (Eq. (12)); section 3.4, Algorithm 2 serves the
 // argmax when it fires and falls through otherwise. The page notes that this single scan of
 // the vocabulary is the whole critical path of the fast answer (section 2.2, Eq. (3)), so
-// the scan is the kernel: one CTA per (row, 32 KiB chunk), each logit read once from HBM,
-// a per-chunk (l1, argmax, l2) triple merged by the row's last-arriving CTA.
+// the scan is the kernel: every (row, 32 KiB chunk) unit is read once from HBM (through the
+// persistent TMA pipeline of sv_stream.cuh), reduced to an (l1, argmax, l2) triple, and the
+// triples of a row are merged by the consumers that finish the row's last chunk.
 #include <cmath>
 #include <cstdint>
 
 #include "specverify.h"
 #include "sv_device.cuh"
 #include "sv_host.h"
+#include "sv_stream.cuh"
 
 namespace sv {
 
@@ -65,85 +67,96 @@ __device__ __forceinline__ bool in_sorted(const int32_t* a, int n, int v) {
   return lo < n && __ldg(a + lo) == v;
 }
 
-template <typename E>
-__global__ void __launch_bounds__(kThreads, 4) gate_kernel(const GateArgs A) {
-  __shared__ float s_m1[kWarps], s_m2[kWarps];
-  __shared__ int s_i1[kWarps];
-  __shared__ int s_last;
+template <typename ET>
+struct GateOp {
+  using Args = GateArgs;
+  using E = ET;
+  static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is skipped
+  struct Smem {
+    float m1[kWarps], m2[kWarps];
+    int i1[kWarps];
+    int row_last;
+  };
 
-  const int64_t unit = blockIdx.x;
-  const int row = (int)(unit / A.nch);
-  const int c = (int)(unit - (int64_t)row * A.nch);
-  const void* rowp = static_cast<const char*>(A.logits) +
-                     (int64_t)row * A.V * (16 / E::kPerVec);
-  const int64_t j0 = (int64_t)c * E::kChunk;
-  const int64_t j1 = j0 + E::kChunk < A.V ? j0 + E::kChunk : A.V;
-  uint4 v[kVecPerThread];
-  load_chunk<E>(rowp, j0, j1, A.aligned, E::kNaNBits, v);  // NaN padding is skipped
+  __device__ static bool unit_row(const Args& A, int64_t u, const void*& row, int64_t& j0,
+                                  int64_t& j1) {
+    const int r = (int)(u / A.nch);
+    const int c = (int)(u - (int64_t)r * A.nch);
+    row = static_cast<const char*>(A.logits) + (int64_t)r * A.V * (16 / E::kPerVec);
+    j0 = (int64_t)c * E::kChunk;
+    j1 = j0 + E::kChunk < A.V ? j0 + E::kChunk : (int64_t)A.V;
+    return true;
+  }
 
-  Top2 t{-INFINITY, -INFINITY, kNoIndex};
+  __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
+                                 int64_t j1, const uint4 (&v)[kVecPerThread], Smem& sm) {
+    const int row = (int)(u / A.nch);
+    const int c = (int)(u - (int64_t)row * A.nch);
+    Top2 t{-INFINITY, -INFINITY, kNoIndex};
 #pragma unroll
-  for (int it = 0; it < kVecPerThread; ++it) {
-    const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
+    for (int it = 0; it < kVecPerThread; ++it) {
+      const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
 #pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) {
-      const float z = E::get(v[it], l);
-      if (z != z) continue;
-      if (t.i1 == kNoIndex) {
-        t.m1 = z;
-        t.i1 = jb + l;
-      } else if (z > t.m1) {
-        t.m2 = t.m1;
-        t.m1 = z;
-        t.i1 = jb + l;
-      } else {
-        t.m2 = fmaxf(t.m2, z);
+      for (int l = 0; l < E::kPerVec; ++l) {
+        const float z = E::get(v[it], l);
+        if (z != z) continue;
+        if (t.i1 == kNoIndex) {
+          t.m1 = z;
+          t.i1 = jb + l;
+        } else if (z > t.m1) {
+          t.m2 = t.m1;
+          t.m1 = z;
+          t.i1 = jb + l;
+        } else {
+          t.m2 = fmaxf(t.m2, z);
+        }
       }
     }
-  }
-  t = warp_top2(t);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    s_m1[w] = t.m1;
-    s_m2[w] = t.m2;
-    s_i1[w] = t.i1;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Top2 b{s_m1[0], s_m2[0], s_i1[0]};
-    for (int q = 1; q < kWarps; ++q) b = top2_merge(b, Top2{s_m1[q], s_m2[q], s_i1[q]});
-    ChunkTop2* p = A.chunk + (int64_t)row * A.nch + c;
-    p->m1 = b.m1;
-    p->i1 = b.i1;
-    p->m2 = b.m2;
-    s_last = arrive_last(A.row_cnt + row, (unsigned)A.nch);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  if (threadIdx.x < 32) {
-    Top2 b{-INFINITY, -INFINITY, kNoIndex};
-    for (int cc = lane; cc < A.nch; cc += 32) {
-      const ChunkTop2* p = A.chunk + (int64_t)row * A.nch + cc;
-      b = top2_merge(b, Top2{__ldcg(&p->m1), __ldcg(&p->m2), __ldcg(&p->i1)});
-    }
-    b = warp_top2(b);
+    t = warp_top2(t);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
-      if (b.i1 == kNoIndex) {
-        A.out_token[row] = -1;
-        A.out_gap[row] = __int_as_float(0x7fc00000);
-        A.out_fire[row] = 0;
-      } else {
-        const double gap = (double)b.m1 - (double)b.m2;
-        const bool fire = gap > A.tau && A.n_answer > 0 && in_sorted(A.answer, A.n_answer, b.i1);
-        A.out_token[row] = b.i1;
-        A.out_gap[row] = (float)gap;
-        A.out_fire[row] = fire ? 1 : 0;
+      sm.m1[w] = t.m1;
+      sm.m2[w] = t.m2;
+      sm.i1[w] = t.i1;
+    }
+    cbar();
+    if (threadIdx.x == 0) {
+      Top2 b{sm.m1[0], sm.m2[0], sm.i1[0]};
+      for (int q = 1; q < kWarps; ++q) b = top2_merge(b, Top2{sm.m1[q], sm.m2[q], sm.i1[q]});
+      ChunkTop2* p = A.chunk + (int64_t)row * A.nch + c;
+      p->m1 = b.m1;
+      p->i1 = b.i1;
+      p->m2 = b.m2;
+      sm.row_last = arrive_last(A.row_cnt + row, (unsigned)A.nch);
+    }
+    cbar();
+    if (!sm.row_last) return;
+    __threadfence();
+
+    if (threadIdx.x < 32) {
+      Top2 b{-INFINITY, -INFINITY, kNoIndex};
+      for (int cc = lane; cc < A.nch; cc += 32) {
+        const ChunkTop2* p = A.chunk + (int64_t)row * A.nch + cc;
+        b = top2_merge(b, Top2{__ldcg(&p->m1), __ldcg(&p->m2), __ldcg(&p->i1)});
+      }
+      b = warp_top2(b);
+      if (lane == 0) {
+        if (b.i1 == kNoIndex) {
+          A.out_token[row] = -1;
+          A.out_gap[row] = __int_as_float(0x7fc00000);
+          A.out_fire[row] = 0;
+        } else {
+          const double gap = (double)b.m1 - (double)b.m2;
+          const bool fire =
+              gap > A.tau && A.n_answer > 0 && in_sorted(A.answer, A.n_answer, b.i1);
+          A.out_token[row] = b.i1;
+          A.out_gap[row] = (float)gap;
+          A.out_fire[row] = fire ? 1 : 0;
+        }
       }
     }
   }
-}
+};
 
 }  // namespace sv
 
@@ -189,11 +202,9 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   A.chunk = reinterpret_cast<ChunkTop2*>(ws + L.chunk);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.row_cnt, 0, L.total - L.row_cnt, st);
+  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (dtype == SV_F32)
-    gate_kernel<F32><<<(unsigned)units, kThreads, 0, st>>>(A);
-  else
-    gate_kernel<BF16><<<(unsigned)units, kThreads, 0, st>>>(A);
-  return launch_status();
+  StreamCtl* ctl = reinterpret_cast<StreamCtl*>(ws + L.ctl);
+  if (dtype == SV_F32) return launch_units<GateOp<F32>>(A, units, ctl, st);
+  return launch_units<GateOp<BF16>>(A, units, ctl, st);
 }

@@ -35,6 +35,13 @@ inline int64_t num_chunks(int V, sv_dtype d) {
   return (static_cast<int64_t>(V) + c - 1) / c;
 }
 
+// Per-call control words of the persistent kernels; cleared with the counters.
+struct StreamCtl {
+  unsigned long long next_unit;  // the next unit to claim
+  unsigned int error;            // bit 0: a producer wait ran out; bit 1: a consumer wait
+  unsigned int pad;
+};
+
 // Partial result of one (row, chunk) unit of the sampled verify.
 struct ChunkSoftmax {
   double S;   // sum over the chunk of 2^(z*s + c), c = fp32(-m*s)
@@ -63,9 +70,9 @@ struct ChunkTop2 {
   int pad;
 };
 
-// Byte offsets of the workspace regions (each 256-byte aligned).
+// Workspace regions. Everything from `ctl` to `total` is cleared at the start of a call.
 struct SampleLayout {
-  size_t chunk, row, resid, row_cnt, req_cnt, total;
+  size_t chunk, row, resid, ctl, row_cnt, req_cnt, total;
 };
 inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = 2 * static_cast<size_t>(k) + 1;
@@ -74,7 +81,8 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
-  L.resid = o;   o = round_up(o + B * nch * sizeof(double), 256);
+  L.resid = o;   o = round_up(o + B * nch * 8 * sizeof(double), 256);  // [B][nch][warps]
+  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
   L.total = o;
@@ -82,7 +90,7 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
 }
 
 struct GreedyLayout {
-  size_t chunk, row, row_cnt, req_cnt, total;
+  size_t chunk, row, ctl, row_cnt, req_cnt, total;
 };
 inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = static_cast<size_t>(k) + 1;
@@ -91,6 +99,7 @@ inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkArgmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
+  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
   L.total = o;
@@ -98,13 +107,14 @@ inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
 }
 
 struct GateLayout {
-  size_t chunk, row_cnt, total;
+  size_t chunk, ctl, row_cnt, total;
 };
 inline GateLayout gate_layout(int N, int V, sv_dtype d) {
   const size_t nch = static_cast<size_t>(num_chunks(V, d));
   GateLayout L{};
   size_t o = 0;
   L.chunk = o;   o = round_up(o + static_cast<size_t>(N) * nch * sizeof(ChunkTop2), 256);
+  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
   L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
   L.total = o;
   return L;
