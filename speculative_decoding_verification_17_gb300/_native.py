@@ -23,7 +23,7 @@ SO = os.path.join(BUILD, "libspecverify.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-              "-I", CSRC]
+              "-I", CSRC] + os.environ.get("SV_NVCC_EXTRA", "").split()
 
 
 def _nvcc() -> str:

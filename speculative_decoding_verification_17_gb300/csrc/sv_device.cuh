@@ -59,14 +59,10 @@ struct F32 {
   __device__ static __forceinline__ uint4 pad_vec(uint32_t pad) {
     return make_uint4(pad, pad, pad, pad);
   }
-  // Largest logit of the thread's vectors (NaN ignored, as fmaxf does).
-  __device__ static __forceinline__ float max_all(const uint4 (&v)[kVecPerThread]) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it)
-      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(v[it].x), __uint_as_float(v[it].y)),
-                         fmaxf(__uint_as_float(v[it].z), __uint_as_float(v[it].w))));
-    return m;
+  // Largest logit of a vector (NaN ignored, as fmaxf does).
+  __device__ static __forceinline__ float max_vec(const uint4& v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
 };
 
@@ -96,17 +92,10 @@ struct BF16 {
     asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
   }
-  // Largest logit of the thread's vectors, reduced on packed bf16 pairs (max.bf16x2 returns
-  // the other operand when one is NaN, as fmaxf does); exact, widened only at the end.
-  __device__ static __forceinline__ float max_all(const uint4 (&v)[kVecPerThread]) {
-    uint32_t m = v[0].x;
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      if (it > 0) m = max2(m, v[it].x);
-      m = max2(m, v[it].y);
-      m = max2(m, v[it].z);
-      m = max2(m, v[it].w);
-    }
+  // Largest logit of a vector, reduced on packed bf16 pairs (max.bf16x2 returns the other
+  // operand when one is NaN, as fmaxf does); exact, widened only at the end.
+  __device__ static __forceinline__ float max_vec(const uint4& v) {
+    const uint32_t m = max2(max2(v.x, v.y), max2(v.z, v.w));
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
   }
 };

@@ -5,9 +5,9 @@
 // the argmax lies in the fast-answer set A (Eq. (12)); section 3.4, Algorithm 2 serves the
 // argmax when it fires and falls through otherwise. The page notes that this single scan of
 // the vocabulary is the whole critical path of the fast answer (section 2.2, Eq. (3)), so
-// the scan is the kernel: every (row, 32 KiB chunk) unit is read once from HBM (through the
-// persistent TMA pipeline of sv_stream.cuh), reduced to an (l1, argmax, l2) triple, and the
-// triples of a row are merged by the consumers that finish the row's last chunk.
+// the scan is the kernel: every (row, 32 KiB chunk) unit is read once from HBM by one bulk
+// copy (sv_stream.cuh), reduced to an (l1, argmax, l2) triple, and the triples of a row are
+// merged by the CTA that finishes the row's last chunk.
 #include <cmath>
 #include <cstdint>
 
@@ -17,6 +17,8 @@
 #include "sv_stream.cuh"
 
 namespace sv {
+
+constexpr int kPoisonedTop2 = -2;  // marks a chunk whose copy never landed
 
 struct GateArgs {
   const void* logits;
@@ -89,16 +91,18 @@ struct GateOp {
   }
 
   __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const uint4 (&v)[kVecPerThread], Smem& sm) {
+                                 int64_t j1, const unsigned char* chunk, bool poisoned,
+                                 Smem& sm) {
     const int row = (int)(u / A.nch);
     const int c = (int)(u - (int64_t)row * A.nch);
     Top2 t{-INFINITY, -INFINITY, kNoIndex};
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
+      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
       const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
-        const float z = E::get(v[it], l);
+        const float z = E::get(v, l);
         if (z != z) continue;
         if (t.i1 == kNoIndex) {
           t.m1 = z;
@@ -125,7 +129,7 @@ struct GateOp {
       for (int q = 1; q < kWarps; ++q) b = top2_merge(b, Top2{sm.m1[q], sm.m2[q], sm.i1[q]});
       ChunkTop2* p = A.chunk + (int64_t)row * A.nch + c;
       p->m1 = b.m1;
-      p->i1 = b.i1;
+      p->i1 = poisoned ? kPoisonedTop2 : b.i1;
       p->m2 = b.m2;
       sm.row_last = arrive_last(A.row_cnt + row, (unsigned)A.nch);
     }
@@ -135,13 +139,17 @@ struct GateOp {
 
     if (threadIdx.x < 32) {
       Top2 b{-INFINITY, -INFINITY, kNoIndex};
+      bool poison = false;
       for (int cc = lane; cc < A.nch; cc += 32) {
         const ChunkTop2* p = A.chunk + (int64_t)row * A.nch + cc;
-        b = top2_merge(b, Top2{__ldcg(&p->m1), __ldcg(&p->m2), __ldcg(&p->i1)});
+        const int pi = __ldcg(&p->i1);
+        poison |= pi == kPoisonedTop2;
+        if (pi != kPoisonedTop2) b = top2_merge(b, Top2{__ldcg(&p->m1), __ldcg(&p->m2), pi});
       }
       b = warp_top2(b);
+      poison = __any_sync(0xffffffffu, poison);
       if (lane == 0) {
-        if (b.i1 == kNoIndex) {
+        if (b.i1 == kNoIndex || poison) {
           A.out_token[row] = -1;
           A.out_gap[row] = __int_as_float(0x7fc00000);
           A.out_fire[row] = 0;
@@ -204,7 +212,7 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  StreamCtl* ctl = reinterpret_cast<StreamCtl*>(ws + L.ctl);
+  CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_units<GateOp<F32>>(A, units, ctl, st);
   return launch_units<GateOp<BF16>>(A, units, ctl, st);
 }

@@ -35,11 +35,11 @@ inline int64_t num_chunks(int V, sv_dtype d) {
   return (static_cast<int64_t>(V) + c - 1) / c;
 }
 
-// Per-call control words of the persistent kernels; cleared with the counters.
-struct StreamCtl {
-  unsigned long long next_unit;  // the next unit to claim
-  unsigned int error;            // bit 0: a producer wait ran out; bit 1: a consumer wait
-  unsigned int pad;
+// Per-call control word, cleared with the counters: bit 0 is set when a bounded wait for a
+// chunk copy ran out (the affected rows are then reported as data errors).
+struct CallCtl {
+  unsigned int error;
+  unsigned int pad[3];
 };
 
 // Partial result of one (row, chunk) unit of the sampled verify.
@@ -82,7 +82,7 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
   L.resid = o;   o = round_up(o + B * nch * 8 * sizeof(double), 256);  // [B][nch][warps]
-  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
+  L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
   L.total = o;
@@ -99,7 +99,7 @@ inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkArgmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
-  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
+  L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
   L.total = o;
@@ -114,7 +114,7 @@ inline GateLayout gate_layout(int N, int V, sv_dtype d) {
   GateLayout L{};
   size_t o = 0;
   L.chunk = o;   o = round_up(o + static_cast<size_t>(N) * nch * sizeof(ChunkTop2), 256);
-  L.ctl = o;     o = round_up(o + sizeof(StreamCtl), 256);
+  L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
   L.total = o;
   return L;

@@ -1,19 +1,15 @@
-// sv_stream.cuh — the two drivers that feed (row, chunk) units to a row operation.
+// sv_stream.cuh — the driver that feeds (row, chunk) units to a row operation.
 //
-// stream_kernel (rows 16-byte aligned): a persistent kernel, two CTAs per SM. Each CTA has
-// one producer warp and kWarps consumer warps. The producer claims the next unit from a
-// global counter (units are claimed in index order, so a request's units run close together
-// in time), skips units the operation does not need, and copies the unit's 32 KiB chunk
-// with one cp.async.bulk (TMA) into a kStages-deep shared-memory ring, completing on the
-// stage's "full" mbarrier. The consumers wait on that barrier, move their vectors into
-// registers, release the stage on its "empty" mbarrier and run the operation. So up to
-// kStages chunks per CTA are in flight while the consumers compute or finish a row or a
-// request, and a CTA that is busy finishing simply claims fewer units. Every wait is
-// bounded by kWaitLimitNs; a wait that runs out sets a bit in the call's control word and
-// the CTA stops.
-//
-// direct_kernel (any alignment): one CTA of kThreads threads per unit, loading straight into
-// registers (logit by logit when a row is not 16-byte aligned).
+// unit_kernel: one CTA of kThreads threads per unit, up to kCtasPerSm CTAs resident per SM.
+// For a row that starts on a 16-byte boundary, thread 0 fetches the unit's chunk (32 KiB)
+// with a single cp.async.bulk (TMA) into shared memory, completing on an mbarrier; a row
+// that does not is staged logit by logit by all threads. The operation then reads the
+// chunk from shared memory. Many small CTAs per SM keep several chunks in flight per SM
+// and hide each other's fixed costs (the barrier waits, the fence and atomic that publish a
+// partial), and the register budget of kCtasPerSm CTAs is what every code path of an
+// operation is written for. The wait on the bulk copy is bounded; a copy that never lands
+// poisons its row (the request gets the error sentinel) and sets a bit in the call's
+// control word.
 //
 // An operation Op provides:
 //   using E;                        element type (F32 / BF16)
@@ -23,11 +19,10 @@
 //   static bool unit_row(const Args&, int64_t u, const void*& row, int64_t& j0, int64_t& j1);
 //       false when unit u is not needed; else the row and the chunk [j0, j1)
 //   static void process(const Args&, int64_t u, const void* row, int64_t j0, int64_t j1,
-//                       const uint4 (&v)[kVecPerThread], Smem&);
-//       run by the kThreads consumers with the chunk in registers
+//                       const unsigned char* chunk, bool poisoned, Smem&);
+//       run by all kThreads threads; 16-byte vector s of the chunk is at chunk + 16*s
 #pragma once
 
-#include <atomic>
 #include <cuda_runtime.h>
 
 #include "sv_device.cuh"
@@ -35,149 +30,79 @@
 
 namespace sv {
 
-constexpr int kStages = 3;
-constexpr int kStreamThreads = kThreads + 32;          // consumers + one producer warp
-constexpr int kRingBytes = kStages * kChunkBytes;      // 96 KiB of dynamic shared memory
-constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: far past any legitimate wait
+// CTAs resident per SM: shared memory allows 6 (32 KiB chunk each); 5 leaves the sampled
+// verify's request-finishing code 48 registers per thread without spilling. A build may set
+// SV_CTAS_PER_SM to try another value.
+#ifndef SV_CTAS_PER_SM
+#define SV_CTAS_PER_SM 5
+#endif
+constexpr int kCtasPerSm = SV_CTAS_PER_SM;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far past any legitimate wait
 
-template <class Op>
-__global__ void __launch_bounds__(kStreamThreads, 2)
-    stream_kernel(const typename Op::Args A, long long units, StreamCtl* ctl) {
-  using E = typename Op::E;
-  extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ __align__(8) uint64_t empty[kStages];
-  __shared__ long long unit_of[kStages];
-  __shared__ typename Op::Smem sm;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  if (warp == kWarps) {  // ---- producer ----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (;;) {
-        long long u;
-        const void* src = nullptr;
-        uint32_t bytes = 0;
-        for (;;) {
-          u = (long long)atomicAdd(&ctl->next_unit, 1ull);
-          if (u >= units) {
-            u = -1;
-            break;
-          }
-          const void* row;
-          int64_t j0, j1;
-          if (Op::unit_row(A, u, row, j0, j1)) {
-            src = static_cast<const char*>(row) + j0 * (16 / E::kPerVec);
-            bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
-            break;
-          }
-        }
-        if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitLimitNs)) {
-          atomicOr(&ctl->error, 1u);
-          break;
-        }
-        unit_of[stage] = u;
-        if (u < 0) {
-          mbar_arrive(&full[stage]);  // no more work: consumers stop at this stage
-          break;
-        }
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        bulk_g2s(ring + stage * kChunkBytes, src, bytes, &full[stage]);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    return;
-  }
-
-  // ---- consumers ----
-  int stage = 0;
-  uint32_t phase = 0;
-  for (;;) {
-    if (!mbar_wait(&full[stage], phase, kWaitLimitNs)) {
-      if (lane == 0) atomicOr(&ctl->error, 2u);
-      break;
-    }
-    const long long u = unit_of[stage];
-    if (u < 0) break;
-    const void* row;
-    int64_t j0, j1;
-    Op::unit_row(A, u, row, j0, j1);
-    const unsigned char* buf = ring + stage * kChunkBytes;
-    uint4 v[kVecPerThread];
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const int slot = it * kThreads + threadIdx.x;
-      v[it] = (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(buf + slot * 16)
-                                                      : E::pad_vec(Op::kPad);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    Op::process(A, u, row, j0, j1, v, sm);
-    if (++stage == kStages) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  }
+// Vector `it` of this thread from a chunk staged in shared memory (pad past the end).
+template <typename E>
+__device__ __forceinline__ uint4 chunk_vec(const unsigned char* chunk, int it, int64_t j0,
+                                           int64_t j1, uint32_t pad) {
+  const int slot = it * kThreads + threadIdx.x;
+  return (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(chunk + slot * 16) : E::pad_vec(pad);
 }
 
 template <class Op>
-__global__ void __launch_bounds__(kThreads, 2) direct_kernel(const typename Op::Args A) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    unit_kernel(const typename Op::Args A, CallCtl* ctl) {
   using E = typename Op::E;
+  extern __shared__ __align__(128) unsigned char chunk[];
+  __shared__ __align__(8) uint64_t bar;
   __shared__ typename Op::Smem sm;
+
   const long long u = blockIdx.x;
   const void* row;
   int64_t j0, j1;
   if (!Op::unit_row(A, u, row, j0, j1)) return;
-  uint4 v[kVecPerThread];
-  load_chunk<E>(row, j0, j1, A.aligned, Op::kPad, v);
-  Op::process(A, u, row, j0, j1, v, sm);
+  bool poisoned = false;
+  if (A.aligned) {
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_barrier_init();
+      const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_g2s(chunk, static_cast<const char*>(row) + j0 * (16 / E::kPerVec), bytes, &bar);
+    }
+    __syncthreads();
+    if (!mbar_wait(&bar, 0, kWaitLimitNs)) {
+      poisoned = true;
+      if (threadIdx.x == 0) atomicOr(&ctl->error, 1u);
+    }
+    poisoned = __syncthreads_or(poisoned);
+  } else {
+#pragma unroll
+    for (int it = 0; it < kVecPerThread; ++it) {
+      const int slot = it * kThreads + threadIdx.x;
+      const int64_t j = j0 + (int64_t)slot * E::kPerVec;
+      if (j < j1) {
+        const uint4 v = load_vec<E>(row, j, j1, false, Op::kPad);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(chunk + slot * 16)),
+                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+    }
+    __syncthreads();
+  }
+  Op::process(A, u, row, j0, j1, chunk, poisoned, sm);
 }
 
-// Launch the units of a row operation: the persistent TMA kernel for aligned rows, the
-// direct kernel otherwise. `ctl` lies in the counter region the caller has just cleared.
+// Launch the units of a row operation. `ctl` lies in the region the caller has just cleared.
 template <class Op>
-sv_status launch_units(const typename Op::Args& A, long long units, StreamCtl* ctl,
+sv_status launch_units(const typename Op::Args& A, long long units, CallCtl* ctl,
                        cudaStream_t st) {
   if (units <= 0) return SV_OK;
-  if (!A.aligned) {
-    direct_kernel<Op><<<(unsigned)units, kThreads, 0, st>>>(A);
-    return launch_status();
-  }
-  static std::atomic<int> cached_grid[64];  // per device: CTAs resident at once
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // ask for the largest shared-memory carveout so kCtasPerSm CTAs fit on an SM (a host-side
+  // function attribute, no stream work; set on every call so it holds in any context)
+  cudaError_t e = cudaFuncSetAttribute(unit_kernel<Op>,
+                                       cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return cuda_fail(e);
-  // a host-side function attribute (no stream work); set on every call so it also holds
-  // in a context created after the first call
-  e = cudaFuncSetAttribute(stream_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kRingBytes);
-  if (e != cudaSuccess) return cuda_fail(e);
-  int grid = (dev >= 0 && dev < 64) ? cached_grid[dev].load(std::memory_order_relaxed) : 0;
-  if (grid == 0) {
-    int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<Op>,
-                                                      kStreamThreads, kRingBytes);
-    if (e != cudaSuccess) return cuda_fail(e);
-    grid = sms * (per_sm > 0 ? per_sm : 1);
-    if (dev >= 0 && dev < 64) cached_grid[dev].store(grid, std::memory_order_relaxed);
-  }
-  const long long g = units < grid ? units : grid;
-  stream_kernel<Op><<<(unsigned)g, kStreamThreads, kRingBytes, st>>>(A, units, ctl);
+  unit_kernel<Op><<<(unsigned)units, kThreads, kChunkBytes, st>>>(A, ctl);
   return launch_status();
 }
 

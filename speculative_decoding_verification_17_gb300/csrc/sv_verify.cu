@@ -37,6 +37,8 @@
 
 namespace sv {
 
+constexpr int kPoisoned = -2;  // a chunk index that marks a chunk whose copy never landed
+
 template <typename E>
 __device__ __forceinline__ const void* row_ptr(const void* base, int64_t row, int V) {
   return static_cast<const char*>(base) + row * (int64_t)V * (16 / E::kPerVec);
@@ -62,7 +64,7 @@ struct ScanSmem {
 // order, whose running weight exceeds `target` (chunk units); when rounding leaves the
 // target at or past the chunk's total, the last logit with positive weight. Warp w owns the
 // contiguous segment [j0 + w*kSeg, j0 + (w+1)*kSeg) and reads it in rounds of 32*kPerVec
-// logits (one coalesced 16-byte vector per lane per round, four rounds loaded at once).
+// logits (one coalesced 16-byte vector per lane per round, two rounds loaded at once).
 // Lane sums are sequential fp32, round totals come from an inclusive warp scan in double,
 // segment totals are sequential sums of round totals. The owning warp replays exactly the
 // same loads and arithmetic, so the crossing is found there.
@@ -74,7 +76,7 @@ __device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& v
   constexpr int kSeg = E::kChunk / kWarps;
   constexpr int kRound = 32 * E::kPerVec;
   constexpr int kRounds = kSeg / kRound;
-  constexpr int kBatch = 4;  // rounds loaded at once
+  constexpr int kBatch = 2;  // rounds loaded at once
   static_assert(kRounds * kRound == kSeg && kRounds % kBatch == 0, "whole rounds and batches");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t seg0 = j0 + (int64_t)warp * kSeg;
@@ -330,13 +332,15 @@ struct SampleOp {
   }
 
   __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const uint4 (&v)[kVecPerThread], Smem& sm);
+                                 int64_t j1, const unsigned char* chunk, bool poisoned,
+                                 Smem& sm);
   __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm);
 };
 
 template <typename ET>
 __device__ void SampleOp<ET>::process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                      int64_t j1, const uint4 (&v)[kVecPerThread], Smem& sm) {
+                                      int64_t j1, const unsigned char* chunk, bool poisoned,
+                                      Smem& sm) {
   int r, slot, c;
   decode(A, u, r, slot, c);
   bool n_ok;
@@ -346,25 +350,32 @@ __device__ void SampleOp<ET>::process(const Args& A, int64_t u, const void* rowp
   const int R = 2 * A.k + 1;
 
   // ---- pass 1: chunk maximum and chunk sum ----
-  const float m = block_max_f(E::max_all(v), sm.red);
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int it = 0; it < kVecPerThread; ++it)
+    tmax = fmaxf(tmax, E::max_vec(chunk_vec<E>(chunk, it, j0, j1, kPad)));
+  const float m = block_max_f(tmax, sm.red);
   double S;
-  if (m == -INFINITY || m == INFINITY) {
+  if (poisoned || m == -INFINITY || m == INFINITY) {
     // no finite logit here: a masked chunk carries no mass; NaN or +inf poison the row
     int nan = 0;
 #pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it)
+    for (int it = 0; it < kVecPerThread; ++it) {
+      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
 #pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) nan |= E::get(v[it], l) != E::get(v[it], l);
-    const bool bad = cbar_or(nan) || m == INFINITY;
+      for (int l = 0; l < E::kPerVec; ++l) nan |= E::get(v, l) != E::get(v, l);
+    }
+    const bool bad = cbar_or(nan) || m == INFINITY || poisoned;
     S = bad ? __longlong_as_double(0x7ff8000000000000ll) : 0.0;
   } else {
     const float cc = __fmul_rn(-m, s);
     float part[kVecPerThread];
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
+      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
       float e[E::kPerVec];
 #pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) e[l] = ex2(fmaf(E::get(v[it], l), s, cc));
+      for (int l = 0; l < E::kPerVec; ++l) e[l] = ex2(fmaf(E::get(v, l), s, cc));
 #pragma unroll
       for (int w = E::kPerVec / 2; w >= 1; w >>= 1)
 #pragma unroll
@@ -498,20 +509,20 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     rs.wf.ip = (float)(1.0 / (tp.S * exp2((double)rs.wf.cp + (double)tp.m * (double)s)));
     rs.wf.iq = (float)(1.0 / (dq.S * exp2((double)rs.wf.cq + (double)dq.m * (double)s)));
     double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
-    // every warp walks all chunks on its own (no barrier per chunk): 8 vectors in flight
+    // every warp walks all chunks on its own (no barrier per chunk): four vectors in flight
     // per thread at a time, one compensated warp sum per chunk
     for (int c = 0; c < A.nch; ++c) {
       const int64_t j0 = (int64_t)c * E::kChunk;
       rs.j1 = chunk_end<E>(j0, A.V);
       float acc = 0.0f;
 #pragma unroll
-      for (int h = 0; h < kVecPerThread; h += 4) {
-        typename ResidScan<E>::Raw raw[4];
+      for (int h = 0; h < kVecPerThread; h += 2) {
+        typename ResidScan<E>::Raw raw[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
           raw[q] = rs.load(j0 + (int64_t)((h + q) * kThreads + tid) * E::kPerVec);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           float w[E::kPerVec];
           rs.weights(raw[q], w);
 #pragma unroll
@@ -685,7 +696,8 @@ struct GreedyOp {
   }
 
   __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const uint4 (&v)[kVecPerThread], Smem& sm) {
+                                 int64_t j1, const unsigned char* chunk, bool poisoned,
+                                 Smem& sm) {
     int r, i, c;
     decode(A, u, r, i, c);
     bool n_ok;
@@ -697,10 +709,11 @@ struct GreedyOp {
     int bidx = kNoIndex;
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
+      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
       const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
-        const float z = E::get(v[it], l);
+        const float z = E::get(v, l);
         // in increasing j: the first comparable logit, then only strictly larger ones
         if (z > best || (bidx == kNoIndex && z == z)) {
           best = z;
@@ -721,7 +734,7 @@ struct GreedyOp {
       for (int q = 1; q < kWarps; ++q) argmax_merge(bv, bi, sm.v[q], sm.idx[q]);
       ChunkArgmax* p = A.chunk + rid * A.nch + c;
       p->v = bv;
-      p->idx = bi;
+      p->idx = poisoned ? kPoisoned : bi;
       sm.row_last = arrive_last(A.row_cnt + rid, (unsigned)A.nch);
     }
     cbar();
@@ -731,13 +744,17 @@ struct GreedyOp {
     if (threadIdx.x < 32) {
       float bv = -INFINITY;
       int bi = kNoIndex;
+      bool poison = false;
       for (int cc = lane; cc < A.nch; cc += 32) {
         const ChunkArgmax* p = A.chunk + rid * A.nch + cc;
-        argmax_merge(bv, bi, __ldcg(&p->v), __ldcg(&p->idx));
+        const int pi = __ldcg(&p->idx);
+        poison |= pi == kPoisoned;
+        argmax_merge(bv, bi, __ldcg(&p->v), pi == kPoisoned ? kNoIndex : pi);
       }
       warp_argmax(bv, bi);
+      poison = __any_sync(0xffffffffu, poison);
       if (lane == 0) {
-        A.row[rid] = bi == kNoIndex ? -1 : bi;
+        A.row[rid] = (bi == kNoIndex || poison) ? -1 : bi;
         sm.req_last = arrive_last(A.req_cnt + r, (unsigned)(n + 1));
       }
     }
@@ -854,7 +871,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   // the control word and the counters (the last regions) start every call at zero
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  StreamCtl* ctl = reinterpret_cast<StreamCtl*>(ws + L.ctl);
+  CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_units<SampleOp<F32>>(A, units, ctl, st);
   return launch_units<SampleOp<BF16>>(A, units, ctl, st);
 }
@@ -906,7 +923,7 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  StreamCtl* ctl = reinterpret_cast<StreamCtl*>(ws + L.ctl);
+  CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_units<GreedyOp<F32>>(A, units, ctl, st);
   return launch_units<GreedyOp<BF16>>(A, units, ctl, st);
 }
