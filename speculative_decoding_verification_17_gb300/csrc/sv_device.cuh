@@ -1,15 +1,8 @@
 // sv_device.cuh — device building blocks shared by the verify, gate and proposer kernels.
 //
-// Work decomposition used by every row kernel: a logit row of V entries is cut into
-// chunks of kChunkBytes (32 KiB: 8192 fp32 or 16384 bf16 logits). A group of kThreads
-// "consumer" threads reduces one (row, chunk) unit at a time from registers: thread t holds
-// the 16-byte vectors it*kThreads + t, it < kVecPerThread, of the chunk. Partial results go
-// to a caller-owned workspace; the consumer group that finishes last for a row (an atomic
-// counter, no waiting) merges them, and the one that finishes last for a request finishes
-// the request. No CTA ever waits for another one.
-//
-// Block-level synchronisation among the consumers uses named barrier 1 over kThreads
-// threads, so a kernel may add a producer warp that never joins those barriers.
+// A logit row of V entries is cut into chunks of kChunkBytes (32 KiB: 8192 fp32 or 16384
+// bf16 logits); see sv_stream.cuh for how chunks reach the kThreads threads of a CTA.
+// Block-level synchronisation uses named barrier 1 over kThreads threads (cbar).
 #pragma once
 
 #include <cstdint>
@@ -22,6 +15,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = 8;
 constexpr int kChunkBytes = kThreads * kVecPerThread * 16;  // 32 KiB
 constexpr int kNoIndex = 0x7fffffff;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
 // ---- consumer-group barriers ---------------------------------------------------------------
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
@@ -247,10 +244,19 @@ __device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int 
   return prev == expected - 1;
 }
 
-// ---- mbarrier and bulk-copy (TMA) primitives ----------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+// Shared-memory atomic add with acquire-release ordering at CTA scope: the caller's earlier
+// accesses (and, after __syncwarp, its warp's) are ordered before the add, and the thread
+// that sees the final count is ordered after every earlier add.
+__device__ __forceinline__ int atomic_add_acq_rel_cta(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_u32(p)), "r"(v)
+               : "memory");
+  return old;
 }
+
+// ---- mbarrier and bulk-copy (TMA) primitives ----------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");

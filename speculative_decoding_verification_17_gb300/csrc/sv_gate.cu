@@ -5,9 +5,9 @@
 // the argmax lies in the fast-answer set A (Eq. (12)); section 3.4, Algorithm 2 serves the
 // argmax when it fires and falls through otherwise. The page notes that this single scan of
 // the vocabulary is the whole critical path of the fast answer (section 2.2, Eq. (3)), so
-// the scan is the kernel: every (row, 32 KiB chunk) unit is read once from HBM by one bulk
-// copy (sv_stream.cuh), reduced to an (l1, argmax, l2) triple, and the triples of a row are
-// merged by the CTA that finishes the row's last chunk.
+// the scan is the kernel: every logit is read once from HBM by the bulk copies of
+// sv_stream.cuh, each 4 KiB warp slice is reduced to an (l1, argmax, l2) triple, and the
+// triples of a row are merged by the CTA that completes the row.
 #include <cmath>
 #include <cstdint>
 
@@ -22,7 +22,7 @@ constexpr int kPoisonedTop2 = -2;  // marks a chunk whose copy never landed
 
 struct GateArgs {
   const void* logits;
-  int N, V, nch;
+  int N, V, nch, nseg;
   double tau;
   const int32_t* answer;
   int n_answer;
@@ -30,7 +30,7 @@ struct GateArgs {
   int32_t* out_token;
   float* out_gap;
   uint8_t* out_fire;
-  ChunkTop2* chunk;
+  WarpTop2* part;  // [N][nch][kWarps]
   unsigned int* row_cnt;
 };
 
@@ -75,34 +75,33 @@ struct GateOp {
   using E = ET;
   static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is skipped
   struct Smem {
-    float m1[kWarps], m2[kWarps];
-    int i1[kWarps];
     int row_last;
   };
 
-  __device__ static bool unit_row(const Args& A, int64_t u, const void*& row, int64_t& j0,
-                                  int64_t& j1) {
-    const int r = (int)(u / A.nch);
-    const int c = (int)(u - (int64_t)r * A.nch);
-    row = static_cast<const char*>(A.logits) + (int64_t)r * A.V * (16 / E::kPerVec);
-    j0 = (int64_t)c * E::kChunk;
-    j1 = j0 + E::kChunk < A.V ? j0 + E::kChunk : (int64_t)A.V;
+  __device__ static bool unit(const Args& A, int64_t u, Seg& g) {
+    const int r = (int)(u / A.nseg);
+    const int seg = (int)(u - (int64_t)r * A.nseg);
+    g.row = static_cast<const char*>(A.logits) + (int64_t)r * A.V * (16 / E::kPerVec);
+    g.rid = r;
+    g.r = r;
+    g.slot = 0;
+    g.c0 = seg * kSegChunks;
+    g.c1 = min(g.c0 + kSegChunks, A.nch);
+    g.nseg = A.nseg;
     return true;
   }
 
-  __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const unsigned char* chunk, bool poisoned,
-                                 Smem& sm) {
-    const int row = (int)(u / A.nch);
-    const int c = (int)(u - (int64_t)row * A.nch);
+  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
+                                    const uint4 (&v)[kVecPerThread], bool poison) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t j0 = (int64_t)c * E::kChunk;
     Top2 t{-INFINITY, -INFINITY, kNoIndex};
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
-      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
-      const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
+      const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
-        const float z = E::get(v, l);
+        const float z = E::get(v[it], l);
         if (z != z) continue;
         if (t.i1 == kNoIndex) {
           t.m1 = z;
@@ -117,34 +116,30 @@ struct GateOp {
       }
     }
     t = warp_top2(t);
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
-      sm.m1[w] = t.m1;
-      sm.m2[w] = t.m2;
-      sm.i1[w] = t.i1;
+      WarpTop2* p = A.part + ((g.rid * A.nch + c) * kWarps + w);
+      *reinterpret_cast<float4*>(p) =
+          make_float4(t.m1, __int_as_float(poison ? kPoisonedTop2 : t.i1), t.m2, 0.0f);
     }
-    cbar();
-    if (threadIdx.x == 0) {
-      Top2 b{sm.m1[0], sm.m2[0], sm.i1[0]};
-      for (int q = 1; q < kWarps; ++q) b = top2_merge(b, Top2{sm.m1[q], sm.m2[q], sm.i1[q]});
-      ChunkTop2* p = A.chunk + (int64_t)row * A.nch + c;
-      p->m1 = b.m1;
-      p->i1 = poisoned ? kPoisonedTop2 : b.i1;
-      p->m2 = b.m2;
-      sm.row_last = arrive_last(A.row_cnt + row, (unsigned)A.nch);
-    }
-    cbar();
+  }
+
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm) {
+    const int row = g.r;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + row, (unsigned)g.nseg);
+    __syncthreads();
     if (!sm.row_last) return;
     __threadfence();
-
     if (threadIdx.x < 32) {
+      const int np = A.nch * kWarps;
+      const WarpTop2* wp = A.part + (int64_t)row * np;
       Top2 b{-INFINITY, -INFINITY, kNoIndex};
       bool poison = false;
-      for (int cc = lane; cc < A.nch; cc += 32) {
-        const ChunkTop2* p = A.chunk + (int64_t)row * A.nch + cc;
-        const int pi = __ldcg(&p->i1);
+      for (int q = lane; q < np; q += 32) {
+        const float4 pv = __ldcg(reinterpret_cast<const float4*>(wp + q));
+        const int pi = __float_as_int(pv.y);
         poison |= pi == kPoisonedTop2;
-        if (pi != kPoisonedTop2) b = top2_merge(b, Top2{__ldcg(&p->m1), __ldcg(&p->m2), pi});
+        if (pi != kPoisonedTop2) b = top2_merge(b, Top2{pv.x, pv.z, pi});
       }
       b = warp_top2(b);
       poison = __any_sync(0xffffffffu, poison);
@@ -189,7 +184,8 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
       (answer_set && !aligned_to(answer_set, 4)))
     return SV_ERR_INVALID_ARG;
   const int64_t nch = num_chunks(V, dtype);
-  const int64_t units = (int64_t)N * nch;
+  const int nseg = num_segments(nch);
+  const int64_t units = (int64_t)N * nseg;
   if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
   const GateLayout L = gate_layout(N, V, dtype);
   if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
@@ -199,6 +195,7 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   A.N = N;
   A.V = V;
   A.nch = (int)nch;
+  A.nseg = nseg;
   A.tau = (double)tau;
   A.answer = answer_set;
   A.n_answer = n_answer;
@@ -207,12 +204,12 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   A.out_gap = out_gap;
   A.out_fire = out_fire;
   char* ws = static_cast<char*>(workspace);
-  A.chunk = reinterpret_cast<ChunkTop2*>(ws + L.chunk);
+  A.part = reinterpret_cast<WarpTop2*>(ws + L.part);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
-  if (dtype == SV_F32) return launch_units<GateOp<F32>>(A, units, ctl, st);
-  return launch_units<GateOp<BF16>>(A, units, ctl, st);
+  if (dtype == SV_F32) return launch_segments<GateOp<F32>>(A, units, ctl, st);
+  return launch_segments<GateOp<BF16>>(A, units, ctl, st);
 }

@@ -42,46 +42,55 @@ struct CallCtl {
   unsigned int pad[3];
 };
 
-// Partial result of one (row, chunk) unit of the sampled verify.
-struct ChunkSoftmax {
-  double S;   // sum over the chunk of 2^(z*s + c), c = fp32(-m*s)
-  float m;    // chunk maximum (raw logit)
+// Partial results are kept per (row, chunk, warp): warp w of a CTA reduces the w-th 4 KiB
+// slice of a chunk on its own.
+constexpr int kWarpsPerChunk = 8;
+
+// Softmax partial of one warp slice: sum of 2^(z*s - K) over the slice, carried as an
+// unevaluated float pair (hi + lo), with the integer-valued reference K = ceil(m*s) of the
+// slice maximum m. K = -inf marks a slice without a finite logit (no mass), K = NaN a
+// poisoned slice (NaN or +inf logits, or a copy that never landed).
+struct WarpSoftmax {
+  float K;
+  float hi;
+  float lo;
   float pad;
 };
 
-// Merged result of one row of the sampled verify.
+// Merged softmax statistics of one row: S = sum of 2^(z*s - K) over the row in double,
+// K = the largest slice reference (an integer), px = probability of the row's draft token.
 struct RowSoftmax {
-  double S;   // sum over the row of 2^((z - m) * s) evaluated exactly in the exponent
-  double px;  // probability of the row's draft token (target and draft rows i < n)
-  float m;    // row maximum (raw logit)
-  int status; // 0 ok, 1 not a distribution, 2 draft token out of range
+  double S;
+  double px;
+  float K;
+  int status;  // 0 ok, 1 not a distribution, 2 draft token out of range
   double pad;
 };
 
-struct ChunkArgmax {
-  float v;  // largest logit of the chunk
-  int idx;  // its lowest index, kNoIndex when the chunk holds no comparable logit
+struct WarpArgmax {
+  float v;  // largest logit of the slice
+  int idx;  // its lowest index; kNoIndex when the slice holds no comparable logit, -2 poisoned
 };
 
-struct ChunkTop2 {
+struct WarpTop2 {
   float m1;  // largest logit
-  int i1;    // lowest index holding it (kNoIndex if none)
-  float m2;  // largest logit of the chunk with one copy of m1 removed
+  int i1;    // lowest index holding it (kNoIndex if none, -2 poisoned)
+  float m2;  // largest logit of the slice with one copy of m1 removed
   int pad;
 };
 
 // Workspace regions. Everything from `ctl` to `total` is cleared at the start of a call.
 struct SampleLayout {
-  size_t chunk, row, resid, ctl, row_cnt, req_cnt, total;
+  size_t part, row, resid, ctl, row_cnt, req_cnt, total;
 };
 inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = 2 * static_cast<size_t>(k) + 1;
   const size_t nch = static_cast<size_t>(num_chunks(V, d));
   SampleLayout L{};
   size_t o = 0;
-  L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkSoftmax), 256);
+  L.part = o;    o = round_up(o + B * R * nch * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
-  L.resid = o;   o = round_up(o + B * nch * 8 * sizeof(double), 256);  // [B][nch][warps]
+  L.resid = o;   o = round_up(o + B * nch * kWarpsPerChunk * sizeof(double), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
@@ -90,14 +99,14 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
 }
 
 struct GreedyLayout {
-  size_t chunk, row, ctl, row_cnt, req_cnt, total;
+  size_t part, row, ctl, row_cnt, req_cnt, total;
 };
 inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = static_cast<size_t>(k) + 1;
   const size_t nch = static_cast<size_t>(num_chunks(V, d));
   GreedyLayout L{};
   size_t o = 0;
-  L.chunk = o;   o = round_up(o + B * R * nch * sizeof(ChunkArgmax), 256);
+  L.part = o;    o = round_up(o + B * R * nch * kWarpsPerChunk * sizeof(WarpArgmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
@@ -107,13 +116,13 @@ inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
 }
 
 struct GateLayout {
-  size_t chunk, ctl, row_cnt, total;
+  size_t part, ctl, row_cnt, total;
 };
 inline GateLayout gate_layout(int N, int V, sv_dtype d) {
   const size_t nch = static_cast<size_t>(num_chunks(V, d));
   GateLayout L{};
   size_t o = 0;
-  L.chunk = o;   o = round_up(o + static_cast<size_t>(N) * nch * sizeof(ChunkTop2), 256);
+  L.part = o;    o = round_up(o + static_cast<size_t>(N) * nch * kWarpsPerChunk * sizeof(WarpTop2), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
   L.total = o;

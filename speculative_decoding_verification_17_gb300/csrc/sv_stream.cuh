@@ -1,26 +1,31 @@
-// sv_stream.cuh — the driver that feeds (row, chunk) units to a row operation.
+// sv_stream.cuh — the driver that feeds logit chunks to a row operation.
 //
-// unit_kernel: one CTA of kThreads threads per unit, up to kCtasPerSm CTAs resident per SM.
-// For a row that starts on a 16-byte boundary, thread 0 fetches the unit's chunk (32 KiB)
-// with a single cp.async.bulk (TMA) into shared memory, completing on an mbarrier; a row
-// that does not is staged logit by logit by all threads. The operation then reads the
-// chunk from shared memory. Many small CTAs per SM keep several chunks in flight per SM
-// and hide each other's fixed costs (the barrier waits, the fence and atomic that publish a
-// partial), and the register budget of kCtasPerSm CTAs is what every code path of an
-// operation is written for. The wait on the bulk copy is bounded; a copy that never lands
+// A row of V logits is cut into chunks of kChunkBytes (32 KiB). The unit of work of one
+// CTA (kThreads threads, kCtasPerSm CTAs per SM) is a row segment of up to kSegChunks
+// consecutive chunks. Warp w always owns the contiguous 4 KiB slice w of a chunk, so a
+// chunk is reduced by eight independent warps and each warp stores its own partial; pass 1
+// has no CTA-wide barrier at all.
+//
+// For a row that starts on a 16-byte boundary the segment's chunks stream through a
+// two-stage shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each
+// completing on that stage's mbarrier; the last warp to finish reading a stage (a shared
+// counter) starts the copy of the chunk two ahead into it, so the next chunk lands while
+// the current one is reduced. Rows that are not 16-byte aligned are read straight from
+// global memory, logit by logit. Every mbarrier wait is bounded: a copy that never lands
 // poisons its row (the request gets the error sentinel) and sets a bit in the call's
 // control word.
 //
+// After the segment, thread 0 publishes the segment (fence, then an atomic on the row's
+// counter); the CTA that completes a row merges its partials, and the one that completes a
+// request finishes the request. No CTA ever waits for another one.
+//
 // An operation Op provides:
-//   using E;                        element type (F32 / BF16)
-//   static constexpr uint32_t kPad; bit pattern read for logits past the end of a row
-//   struct Smem;                    its shared-memory state
-//   struct Args;                    kernel arguments (with a bool `aligned`)
-//   static bool unit_row(const Args&, int64_t u, const void*& row, int64_t& j0, int64_t& j1);
-//       false when unit u is not needed; else the row and the chunk [j0, j1)
-//   static void process(const Args&, int64_t u, const void* row, int64_t j0, int64_t j1,
-//                       const unsigned char* chunk, bool poisoned, Smem&);
-//       run by all kThreads threads; 16-byte vector s of the chunk is at chunk + 16*s
+//   using E; static constexpr uint32_t kPad; struct Smem; struct Args (with bool aligned);
+//   static bool unit(const Args&, int64_t u, Seg& g);       false: unit not needed
+//   static void warp_chunk(const Args&, const Seg&, int c, const uint4 (&v)[8], bool poison);
+//       one warp, chunk c of the row, the warp's 8 vectors v (lane l holds vector
+//       w*256 + it*32 + l of the chunk in v[it]); stores the warp's partial
+//   static void finish(const Args&, const Seg&, Smem&);     all threads, after the segment
 #pragma once
 
 #include <cuda_runtime.h>
@@ -30,80 +35,128 @@
 
 namespace sv {
 
-// CTAs resident per SM: shared memory allows 6 (32 KiB chunk each); 5 leaves the sampled
-// verify's request-finishing code 48 registers per thread without spilling. A build may set
-// SV_CTAS_PER_SM to try another value.
+constexpr int kSegChunks = 4;  // chunks per CTA
+constexpr int kStages = 2;     // ring depth
 #ifndef SV_CTAS_PER_SM
-#define SV_CTAS_PER_SM 5
+#define SV_CTAS_PER_SM 3
 #endif
-constexpr int kCtasPerSm = SV_CTAS_PER_SM;
+constexpr int kCtasPerSm = SV_CTAS_PER_SM;  // 3 x 64 KiB of ring per SM
+constexpr int kRingBytes = kStages * kChunkBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far past any legitimate wait
 
-// Vector `it` of this thread from a chunk staged in shared memory (pad past the end).
+// A row segment: the row (its first logit), its slot, and its chunks [c0, c1).
+struct Seg {
+  const void* row;
+  int64_t rid;  // row id in the workspace tables
+  int r;        // request (or gate row)
+  int slot;     // row slot inside the request
+  int c0, c1;
+  int nseg;     // segments of this row
+};
+
+// Index of the 16-byte vector lane `lane` of warp `w` holds in slot `it` of a chunk.
+__device__ __forceinline__ int warp_vec_slot(int w, int it, int lane) {
+  return w * (kVecPerThread * 32) + it * 32 + lane;
+}
+
 template <typename E>
-__device__ __forceinline__ uint4 chunk_vec(const unsigned char* chunk, int it, int64_t j0,
-                                           int64_t j1, uint32_t pad) {
-  const int slot = it * kThreads + threadIdx.x;
-  return (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(chunk + slot * 16) : E::pad_vec(pad);
+__device__ __forceinline__ void issue_chunk(const Seg& g, int c, int V, unsigned char* dst,
+                                            uint64_t* bar) {
+  const int64_t j0 = (int64_t)c * E::kChunk;
+  const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
+  const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
+  // the warps' shared-memory reads of this stage come before the async copy that overwrites it
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s(dst, static_cast<const char*>(g.row) + j0 * (16 / E::kPerVec), bytes, bar);
 }
 
 template <class Op>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    unit_kernel(const typename Op::Args A, CallCtl* ctl) {
+    segment_kernel(const typename Op::Args A, CallCtl* ctl) {
   using E = typename Op::E;
-  extern __shared__ __align__(128) unsigned char chunk[];
-  __shared__ __align__(8) uint64_t bar;
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ int released[kStages];
   __shared__ typename Op::Smem sm;
 
-  const long long u = blockIdx.x;
-  const void* row;
-  int64_t j0, j1;
-  if (!Op::unit_row(A, u, row, j0, j1)) return;
-  bool poisoned = false;
+  Seg g;
+  if (!Op::unit(A, (int64_t)blockIdx.x, g)) return;
+  const int nc = g.c1 - g.c0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int V = A.V;
+
   if (A.aligned) {
     if (threadIdx.x == 0) {
-      mbar_init(&bar, 1);
-      fence_barrier_init();
-      const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(chunk, static_cast<const char*>(row) + j0 * (16 / E::kPerVec), bytes, &bar);
-    }
-    __syncthreads();
-    if (!mbar_wait(&bar, 0, kWaitLimitNs)) {
-      poisoned = true;
-      if (threadIdx.x == 0) atomicOr(&ctl->error, 1u);
-    }
-    poisoned = __syncthreads_or(poisoned);
-  } else {
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const int slot = it * kThreads + threadIdx.x;
-      const int64_t j = j0 + (int64_t)slot * E::kPerVec;
-      if (j < j1) {
-        const uint4 v = load_vec<E>(row, j, j1, false, Op::kPad);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(chunk + slot * 16)),
-                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                     : "memory");
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full[s], 1);
+        released[s] = 0;
       }
+      fence_barrier_init();
+      for (int q = 0; q < kStages && q < nc; ++q)
+        issue_chunk<E>(g, g.c0 + q, V, ring + q * kChunkBytes, &full[q]);
     }
     __syncthreads();
+    for (int ci = 0; ci < nc; ++ci) {
+      const int s = ci & (kStages - 1);
+      const bool ok = mbar_wait(&full[s], (uint32_t)((ci / kStages) & 1), kWaitLimitNs);
+      const bool poison = __any_sync(0xffffffffu, !ok);
+      if (poison && lane == 0) atomicOr(&ctl->error, 1u);
+      const int c = g.c0 + ci;
+      const int64_t j0 = (int64_t)c * E::kChunk;
+      const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
+      const unsigned char* buf = ring + s * kChunkBytes;
+      uint4 v[kVecPerThread];
+#pragma unroll
+      for (int it = 0; it < kVecPerThread; ++it) {
+        const int slot = warp_vec_slot(warp, it, lane);
+        v[it] = (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(buf + slot * 16)
+                                                        : E::pad_vec(Op::kPad);
+      }
+      __syncwarp();
+      if (lane == 0) {  // the last warp out of a stage refills it with the chunk two ahead
+        if (atomic_add_acq_rel_cta(&released[s], 1) == kWarps - 1) {
+          released[s] = 0;
+          if (ci + kStages < nc)
+            issue_chunk<E>(g, g.c0 + ci + kStages, V, ring + s * kChunkBytes, &full[s]);
+        }
+      }
+      Op::warp_chunk(A, g, c, v, poison);
+    }
+  } else {
+    for (int ci = 0; ci < nc; ++ci) {
+      const int c = g.c0 + ci;
+      const int64_t j0 = (int64_t)c * E::kChunk;
+      const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
+      uint4 v[kVecPerThread];
+#pragma unroll
+      for (int it = 0; it < kVecPerThread; ++it)
+        v[it] = load_vec<E>(g.row, j0 + (int64_t)warp_vec_slot(warp, it, lane) * E::kPerVec,
+                            j1, false, Op::kPad);
+      Op::warp_chunk(A, g, c, v, false);
+    }
   }
-  Op::process(A, u, row, j0, j1, chunk, poisoned, sm);
+  __syncthreads();  // every warp partial of the segment is stored
+  Op::finish(A, g, sm);
 }
 
-// Launch the units of a row operation. `ctl` lies in the region the caller has just cleared.
+// Launch the segments of a row operation. `ctl` lies in the region the caller just cleared.
 template <class Op>
-sv_status launch_units(const typename Op::Args& A, long long units, CallCtl* ctl,
-                       cudaStream_t st) {
+sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* ctl,
+                          cudaStream_t st) {
   if (units <= 0) return SV_OK;
-  // ask for the largest shared-memory carveout so kCtasPerSm CTAs fit on an SM (a host-side
-  // function attribute, no stream work; set on every call so it holds in any context)
-  cudaError_t e = cudaFuncSetAttribute(unit_kernel<Op>,
-                                       cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       cudaSharedmemCarveoutMaxShared);
+  // host-side function attributes (no stream work), set on every call so they hold in any
+  // context: 64 KiB of dynamic shared memory, and the carveout that fits kCtasPerSm CTAs
+  cudaError_t e = cudaFuncSetAttribute(segment_kernel<Op>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
   if (e != cudaSuccess) return cuda_fail(e);
-  unit_kernel<Op><<<(unsigned)units, kThreads, kChunkBytes, st>>>(A, ctl);
+  e = cudaFuncSetAttribute(segment_kernel<Op>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e);
+  segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
   return launch_status();
 }
+
+inline int num_segments(int64_t nch) { return (int)((nch + kSegChunks - 1) / kSegChunks); }
 
 }  // namespace sv

@@ -10,23 +10,24 @@
 // works" (accept while the draft token is the target's own pick, then emit the target's
 // pick).
 //
-// One kernel launch per call (after a small memset of the call's counters). Unit =
-// (request r, row slot, chunk c); a request has 2k+1 row slots in the sampled verify
-// (target rows 0..k, then draft rows 0..k-1) and k+1 in the greedy verify. Units of rows a
-// request does not need (past its n_r) are skipped.
+// One kernel launch per call (after a small memset of the call's counters). Unit = (request
+// r, row slot, segment of up to four 32 KiB chunks), one CTA each (sv_stream.cuh); a request
+// has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows 0..k-1) and k+1
+// in the greedy verify. Units of rows a request does not need (past its n_r) exit at once.
 //
-//  pass 1 (every unit)      chunk max m_c (exact, raw logits) and, in the sampled verify,
-//                           S_c = sum_j 2^(z_j*s + c_c) with s = log2(e)/T in fp32 and
-//                           c_c = fp32(-m_c*s); in the greedy verify the chunk argmax.
-//  row finish (last chunk)  m = max m_c; S = sum_c S_c * 2^(-c_c - m*s) in double (the
-//                           exponent is exact, so every chunk is rescaled to the same
-//                           reference); p(x) = 2^(z_x*s - m*s) / S in double.
-//  request finish (last row)  ratios p_i(x_i)/q_i(x_i) in double against the uniforms, the
-//                           accepted prefix a, then one draw: the residual max(0, p_a - q_a)
-//                           (one extra pass over the rejected row pair, which L2 still
-//                           holds, for per-chunk residual masses, then one chunk scanned in
-//                           vocabulary order), or the bonus from p_n (chunk masses are the
-//                           pass-1 partials, one chunk scanned).
+//  pass 1 (every warp slice of 4 KiB)  the slice maximum m, the integer-valued reference
+//                           K = ceil(m*s) with s = log2(e)/T in fp32, and the sum of
+//                           2^(z*s - K) in fp32 (compensated across the warp); in the greedy
+//                           verify the slice argmax.
+//  row finish (the CTA that completes the row)  K_row = max K; S = sum of slice sums times
+//                           2^(K - K_row), exact powers of two, in double; p(x) =
+//                           2^(z_x*s - K_row) / S in double.
+//  request finish (the CTA that completes the request)  ratios p_i(x_i)/q_i(x_i) in double
+//                           against the uniforms, the accepted prefix a, then one draw: the
+//                           residual max(0, p_a - q_a) (one extra pass over the rejected row
+//                           pair, which L2 still holds, for per-chunk residual masses, then one
+//                           chunk scanned in vocabulary order), or the bonus from p_n (chunk
+//                           masses from the pass-1 partials, one chunk scanned).
 #include <cmath>
 #include <cstdint>
 
@@ -37,7 +38,7 @@
 
 namespace sv {
 
-constexpr int kPoisoned = -2;  // a chunk index that marks a chunk whose copy never landed
+constexpr int kPoisoned = -2;  // an index that marks a slice whose copy never landed
 
 template <typename E>
 __device__ __forceinline__ const void* row_ptr(const void* base, int64_t row, int V) {
@@ -205,7 +206,7 @@ struct SampleArgs {
   const int32_t* tokens;
   const int32_t* num_draft;
   const float* uniforms;
-  int B, k, V, nch;
+  int B, k, V, nch, nseg;
   float s;       // log2(e) / T, rounded to fp32
   bool aligned;  // every row starts on a 16-byte boundary
   int32_t* out_tokens;
@@ -213,12 +214,17 @@ struct SampleArgs {
   float* out_p;
   float* out_q;
   float* out_resid;
-  ChunkSoftmax* chunk;
+  WarpSoftmax* part;  // [B * (2k+1)][nch][kWarps]
   RowSoftmax* row;
-  double* resid;  // [B][nch][kWarps] residual partial masses
+  double* resid;      // [B][nch][kWarps] residual partial masses
   unsigned int* row_cnt;
   unsigned int* req_cnt;
 };
+
+// 2^d for an integer d <= 0, exactly (0 below the double range).
+__device__ __forceinline__ double pow2i(int d) {
+  return d < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + d) << 52);
+}
 
 // Residual weight max(0, p_j - q_j) with both normalisers folded in (row units).
 struct ResidW {
@@ -255,37 +261,35 @@ struct BonusScan {
   const void* row;
   int64_t j1;
   bool aligned;
-  float s, cc;
+  float s, c;  // weight 2^(z*s + c), c = -K of the row
   using Raw = uint4;
   __device__ __forceinline__ Raw load(int64_t j) const {
     return load_vec<E>(row, j, j1, aligned, E::kNegInfBits);
   }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
 #pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, cc));
+    for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, c));
   }
 };
 
-__device__ __forceinline__ ChunkSoftmax ld_chunk(const ChunkSoftmax* p) {
-  ChunkSoftmax c;
-  c.S = __ldcg(&p->S);
-  c.m = __ldcg(&p->m);
-  return c;
+__device__ __forceinline__ WarpSoftmax ld_part(const WarpSoftmax* p) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  return {v.x, v.y, v.z, v.w};
 }
 
 __device__ __forceinline__ RowSoftmax ld_row(const RowSoftmax* p) {
   RowSoftmax r;
   r.S = __ldcg(&p->S);
   r.px = __ldcg(&p->px);
-  r.m = __ldcg(&p->m);
+  r.K = __ldcg(&p->K);
   r.status = __ldcg(&p->status);
   return r;
 }
 
-// Exponent that rescales a chunk's partial sum onto its row's reference m*s (exact).
-__device__ __forceinline__ double chunk_to_row(float mc, float s, double ms) {
-  const float cc = __fmul_rn(-mc, s);
-  return -(double)cc - ms;
+// Mass of a warp slice in units of 2^K (K the row reference): exact power-of-two scaling.
+__device__ __forceinline__ double part_mass(const WarpSoftmax& w, float K) {
+  if (!(w.K > -INFINITY)) return w.K == -INFINITY ? 0.0 : w.hi;  // empty, or NaN (poisoned)
+  return ((double)w.hi + (double)w.lo) * pow2i((int)(w.K - K));
 }
 
 template <typename ET>
@@ -301,141 +305,140 @@ struct SampleOp {
     ScanSmem scan;
   };
 
-  __device__ static __forceinline__ void decode(const Args& A, int64_t u, int& r, int& slot,
-                                                int& c) {
-    const int R = 2 * A.k + 1;
-    r = (int)(u / ((int64_t)R * A.nch));
-    const int rem = (int)(u - (int64_t)r * R * A.nch);
-    slot = rem / A.nch;
-    c = rem - slot * A.nch;
-  }
   __device__ static __forceinline__ int n_of(const Args& A, int r, bool& ok) {
     const int nraw = A.num_draft ? __ldg(A.num_draft + r) : A.k;
     ok = nraw >= 0 && nraw <= A.k;
     return ok ? nraw : A.k;
   }
 
-  __device__ static bool unit_row(const Args& A, int64_t u, const void*& row, int64_t& j0,
-                                  int64_t& j1) {
-    int r, slot, c;
-    decode(A, u, r, slot, c);
+  __device__ static bool unit(const Args& A, int64_t u, Seg& g) {
+    const int R = 2 * A.k + 1;
+    const int r = (int)(u / ((int64_t)R * A.nseg));
+    const int rem = (int)(u - (int64_t)r * R * A.nseg);
+    const int slot = rem / A.nseg;
+    const int seg = rem - slot * A.nseg;
     bool ok;
     const int n = n_of(A, r, ok);
     const bool is_target = slot <= A.k;
     const int i = is_target ? slot : slot - A.k - 1;
     if (is_target ? i > n : i >= n) return false;
-    row = is_target ? row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + i, A.V)
-                    : row_ptr<E>(A.draft, (int64_t)r * A.k + i, A.V);
-    j0 = (int64_t)c * E::kChunk;
-    j1 = chunk_end<E>(j0, A.V);
+    g.row = is_target ? row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + i, A.V)
+                      : row_ptr<E>(A.draft, (int64_t)r * A.k + i, A.V);
+    g.rid = (int64_t)r * R + slot;
+    g.r = r;
+    g.slot = slot;
+    g.c0 = seg * kSegChunks;
+    g.c1 = min(g.c0 + kSegChunks, A.nch);
+    g.nseg = A.nseg;
     return true;
   }
 
-  __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const unsigned char* chunk, bool poisoned,
-                                 Smem& sm);
+  // Pass 1 for one warp slice: its maximum m, the integer reference K = ceil(m*s) and the
+  // sum of 2^(z*s - K) (pairwise in fp32 per lane, compensated across the warp).
+  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
+                                    const uint4 (&v)[kVecPerThread], bool poison) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int it = 0; it < kVecPerThread; ++it) tmax = fmaxf(tmax, E::max_vec(v[it]));
+    const float m = warp_max_f(tmax);
+    WarpSoftmax out;
+    if (poison || !(m > -INFINITY && m < INFINITY)) {
+      // no finite logit: a masked slice carries no mass; NaN or +inf poison the row
+      bool nan = false;
+#pragma unroll
+      for (int it = 0; it < kVecPerThread; ++it)
+#pragma unroll
+        for (int l = 0; l < E::kPerVec; ++l) nan |= E::get(v[it], l) != E::get(v[it], l);
+      nan = __any_sync(0xffffffffu, nan);
+      const float bad = __int_as_float(0x7fc00000);
+      out = (poison || nan || m == INFINITY) ? WarpSoftmax{bad, bad, 0.0f, 0.0f}
+                                             : WarpSoftmax{-INFINITY, 0.0f, 0.0f, 0.0f};
+    } else {
+      const float s = A.s;
+      const float K = ceilf(m * s);
+      const float cK = -K;
+      float part[kVecPerThread];
+#pragma unroll
+      for (int it = 0; it < kVecPerThread; ++it) {
+        float e[E::kPerVec];
+#pragma unroll
+        for (int l = 0; l < E::kPerVec; ++l) e[l] = ex2(fmaf(E::get(v[it], l), s, cK));
+#pragma unroll
+        for (int q = E::kPerVec / 2; q >= 1; q >>= 1)
+#pragma unroll
+          for (int l = 0; l < q; ++l) e[l] = e[l] + e[l + q];
+        part[it] = e[0];
+      }
+#pragma unroll
+      for (int q = kVecPerThread / 2; q >= 1; q >>= 1)
+#pragma unroll
+        for (int l = 0; l < q; ++l) part[l] = part[l] + part[l + q];
+      float hi = part[0], lo = 0.0f;
+      warp_sum_compensated(hi, lo);
+      out = WarpSoftmax{K, hi, lo, 0.0f};
+    }
+    if (lane == 0) {
+      float4* p = reinterpret_cast<float4*>(A.part + ((g.rid * A.nch + c) * kWarps + w));
+      *p = make_float4(out.K, out.hi, out.lo, 0.0f);
+    }
+  }
+
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm);
   __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm);
 };
 
 template <typename ET>
-__device__ void SampleOp<ET>::process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                      int64_t j1, const unsigned char* chunk, bool poisoned,
-                                      Smem& sm) {
-  int r, slot, c;
-  decode(A, u, r, slot, c);
+__device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm) {
+  const int r = g.r;
   bool n_ok;
   const int n = n_of(A, r, n_ok);
-  const int i = slot <= A.k ? slot : slot - A.k - 1;
+  const int i = g.slot <= A.k ? g.slot : g.slot - A.k - 1;
   const float s = A.s;
-  const int R = 2 * A.k + 1;
-
-  // ---- pass 1: chunk maximum and chunk sum ----
-  float tmax = -INFINITY;
-#pragma unroll
-  for (int it = 0; it < kVecPerThread; ++it)
-    tmax = fmaxf(tmax, E::max_vec(chunk_vec<E>(chunk, it, j0, j1, kPad)));
-  const float m = block_max_f(tmax, sm.red);
-  double S;
-  if (poisoned || m == -INFINITY || m == INFINITY) {
-    // no finite logit here: a masked chunk carries no mass; NaN or +inf poison the row
-    int nan = 0;
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
-#pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) nan |= E::get(v, l) != E::get(v, l);
-    }
-    const bool bad = cbar_or(nan) || m == INFINITY || poisoned;
-    S = bad ? __longlong_as_double(0x7ff8000000000000ll) : 0.0;
-  } else {
-    const float cc = __fmul_rn(-m, s);
-    float part[kVecPerThread];
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
-      float e[E::kPerVec];
-#pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) e[l] = ex2(fmaf(E::get(v, l), s, cc));
-#pragma unroll
-      for (int w = E::kPerVec / 2; w >= 1; w >>= 1)
-#pragma unroll
-        for (int l = 0; l < w; ++l) e[l] = e[l] + e[l + w];
-      part[it] = e[0];
-    }
-#pragma unroll
-    for (int w = kVecPerThread / 2; w >= 1; w >>= 1)
-#pragma unroll
-      for (int l = 0; l < w; ++l) part[l] = part[l] + part[l + w];
-    S = block_sum_fd_t0(part[0], sm.red);  // valid in thread 0, the only reader
-  }
-
-  const int64_t rid = (int64_t)r * R + slot;
-  if (threadIdx.x == 0) {
-    ChunkSoftmax* p = A.chunk + rid * A.nch + c;
-    p->S = S;
-    p->m = m;
-    sm.row_last = arrive_last(A.row_cnt + rid, (unsigned)A.nch);
-  }
-  cbar();
+  if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
+  __syncthreads();
   if (!sm.row_last) return;
   __threadfence();
 
-  // ---- row finish: merge the chunk partials (warp 0) ----
+  // ---- row finish: merge the warp partials of the row (warp 0) ----
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    const ChunkSoftmax* cs = A.chunk + rid * A.nch;
-    float mrow = -INFINITY;
-    for (int cc = lane; cc < A.nch; cc += 32) mrow = fmaxf(mrow, __ldcg(&cs[cc].m));
-    mrow = warp_max_f(mrow);
-    const double ms = (double)mrow * (double)s;
-    double Srow = 0.0;
-    for (int cc = lane; cc < A.nch; cc += 32) {
-      const ChunkSoftmax q = ld_chunk(cs + cc);
-      if (q.m == -INFINITY) Srow += q.S;  // 0, or NaN for a poisoned chunk
-      else Srow += q.S * exp2(chunk_to_row(q.m, s, ms));
+    const int np = A.nch * kWarps;
+    const WarpSoftmax* wp = A.part + g.rid * np;
+    float K = -INFINITY;
+    bool poison = false;
+    for (int q = lane; q < np; q += 32) {
+      const WarpSoftmax w = ld_part(wp + q);
+      poison |= (w.K != w.K) || (w.hi != w.hi);
+      if (w.K > K) K = w.K;
     }
-    Srow = warp_sum_d(Srow);
+    poison = __any_sync(0xffffffffu, poison);
+    K = warp_max_f(K);
+    double S = 0.0;
+    if (K > -INFINITY)
+      for (int q = lane; q < np; q += 32) S += part_mass(ld_part(wp + q), K);
+    S = warp_sum_d(S);
     if (lane == 0) {
-      int status = (isfinite(mrow) && isfinite(Srow) && Srow > 0.0) ? 0 : 1;
+      int status = (!poison && K > -INFINITY && isfinite(S) && S > 0.0) ? 0 : 1;
       double px = 0.0;
       if (i < n) {
         const int32_t xi = __ldg(A.tokens + (int64_t)r * A.k + i);
         if (xi < 0 || xi >= A.V) {
           status = status ? status : 2;
         } else if (status == 0) {
-          const float zx = E::load1(rowp, xi);
-          px = exp2((double)zx * (double)s - ms) / Srow;
+          const float zx = E::load1(g.row, xi);
+          px = exp2((double)zx * (double)s - (double)K) / S;
         }
       }
-      RowSoftmax* rs = A.row + rid;
-      rs->S = Srow;
+      RowSoftmax* rs = A.row + g.rid;
+      rs->S = S;
       rs->px = px;
-      rs->m = mrow;
+      rs->K = K;
       rs->status = status;
       sm.req_last = arrive_last(A.req_cnt + r, (unsigned)(2 * n + 1));
     }
   }
-  cbar();
+  __syncthreads();
   if (!sm.req_last) return;
   __threadfence();
   finish_request(A, r, n, n_ok, sm);
@@ -480,7 +483,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       sm.err = err;
     }
   }
-  cbar();
+  __syncthreads();
   const int a = sm.a;
   if (sm.err) {
     if (tid <= A.k) A.out_tokens[(int64_t)r * (A.k + 1) + tid] = -1;
@@ -504,10 +507,10 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
     const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
     rs.wf.s = s;
-    rs.wf.cp = __fmul_rn(-tp.m, s);
-    rs.wf.cq = __fmul_rn(-dq.m, s);
-    rs.wf.ip = (float)(1.0 / (tp.S * exp2((double)rs.wf.cp + (double)tp.m * (double)s)));
-    rs.wf.iq = (float)(1.0 / (dq.S * exp2((double)rs.wf.cq + (double)dq.m * (double)s)));
+    rs.wf.cp = -tp.K;
+    rs.wf.cq = -dq.K;
+    rs.wf.ip = (float)(1.0 / tp.S);
+    rs.wf.iq = (float)(1.0 / dq.S);
     double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
     // every warp walks all chunks on its own (no barrier per chunk): four vectors in flight
     // per thread at a time, one compensated warp sum per chunk
@@ -533,7 +536,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       warp_sum_compensated(hi, lo);
       if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
     }
-    cbar();
+    __syncthreads();
     // chunk masses R_c = sum over warps (fixed order) and W = sum_c R_c (warp 0)
     if (tid < 32) {
       double wsum = 0.0;
@@ -547,7 +550,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       wsum = warp_sum_d(wsum);
       if (lane == 0) sm.W = wsum;
     }
-    cbar();
+    __syncthreads();
     W = sm.W;
     if (W > 0.0) {
       const double target = (double)__ldg(u + A.k) * W;
@@ -562,7 +565,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
           sm.take_last = tl;
         }
       }
-      cbar();
+      __syncthreads();
       const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
       rs.j1 = chunk_end<E>(j0, A.V);
       t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, rs, sm.scan);
@@ -571,12 +574,11 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   }
   if (!drew) {
     // ---- bonus draw from p_row (row n after full acceptance; row a if the residual
-    //      vanished through rounding) ----
+    //      vanished through rounding); everything in units of 2^K of that row ----
     const int brow = a;
     const int64_t rid = (int64_t)r * R + brow;
     const RowSoftmax rsw = ld_row(A.row + rid);
-    const double ms = (double)rsw.m * (double)s;
-    const ChunkSoftmax* cs = A.chunk + rid * A.nch;
+    const WarpSoftmax* wp = A.part + rid * A.nch * kWarps;
     const double target = (double)__ldg(u + A.k) * rsw.S;
     if (tid < 32) {
       double before;
@@ -584,8 +586,10 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       const int c = pick_chunk(
           A.nch, target,
           [&](int cc) {
-            const ChunkSoftmax q = ld_chunk(cs + cc);
-            return q.m == -INFINITY ? 0.0 : q.S * exp2(chunk_to_row(q.m, s, ms));
+            double mass = 0.0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mass += part_mass(ld_part(wp + cc * kWarps + w), rsw.K);
+            return mass;
           },
           before, tl);
       if (lane == 0) {
@@ -594,18 +598,15 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
         sm.take_last = tl;
       }
     }
-    cbar();
-    const int c = sm.chunk;
-    const ChunkSoftmax q = ld_chunk(cs + c);
-    const double scale = exp2(chunk_to_row(q.m, s, ms));
+    __syncthreads();
     BonusScan<E> bs;
     bs.row = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + brow, A.V);
     bs.aligned = A.aligned;
     bs.s = s;
-    bs.cc = __fmul_rn(-q.m, s);
-    const int64_t j0 = (int64_t)c * E::kChunk;
+    bs.c = -rsw.K;
+    const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
     bs.j1 = chunk_end<E>(j0, A.V);
-    t = scan_chunk<E>(j0, (target - sm.before) / scale, sm.take_last != 0, bs, sm.scan);
+    t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, bs, sm.scan);
   }
 
   // ---- emit ----
@@ -628,11 +629,11 @@ struct GreedyArgs {
   const void* target;
   const int32_t* tokens;
   const int32_t* num_draft;
-  int B, k, V, nch;
+  int B, k, V, nch, nseg;
   bool aligned;
   int32_t* out_tokens;
   int32_t* out_accept_len;
-  ChunkArgmax* chunk;
+  WarpArgmax* part;  // [B * (k+1)][nch][kWarps]
   int* row;
   unsigned int* row_cnt;
   unsigned int* req_cnt;
@@ -663,57 +664,46 @@ struct GreedyOp {
   using E = ET;
   static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is never chosen
   struct Smem {
-    float v[kWarps];
-    int idx[kWarps];
     int row_last, req_last;
     int g[SV_MAX_K + 1];
   };
 
-  __device__ static __forceinline__ void decode(const Args& A, int64_t u, int& r, int& i,
-                                                int& c) {
-    const int R = A.k + 1;
-    r = (int)(u / ((int64_t)R * A.nch));
-    const int rem = (int)(u - (int64_t)r * R * A.nch);
-    i = rem / A.nch;
-    c = rem - i * A.nch;
-  }
   __device__ static __forceinline__ int n_of(const Args& A, int r, bool& ok) {
     const int nraw = A.num_draft ? __ldg(A.num_draft + r) : A.k;
     ok = nraw >= 0 && nraw <= A.k;
     return ok ? nraw : A.k;
   }
 
-  __device__ static bool unit_row(const Args& A, int64_t u, const void*& row, int64_t& j0,
-                                  int64_t& j1) {
-    int r, i, c;
-    decode(A, u, r, i, c);
+  __device__ static bool unit(const Args& A, int64_t u, Seg& g) {
+    const int R = A.k + 1;
+    const int r = (int)(u / ((int64_t)R * A.nseg));
+    const int rem = (int)(u - (int64_t)r * R * A.nseg);
+    const int i = rem / A.nseg;
+    const int seg = rem - i * A.nseg;
     bool ok;
     if (i > n_of(A, r, ok)) return false;
-    row = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + i, A.V);
-    j0 = (int64_t)c * E::kChunk;
-    j1 = chunk_end<E>(j0, A.V);
+    g.row = row_ptr<E>(A.target, (int64_t)r * R + i, A.V);
+    g.rid = (int64_t)r * R + i;
+    g.r = r;
+    g.slot = i;
+    g.c0 = seg * kSegChunks;
+    g.c1 = min(g.c0 + kSegChunks, A.nch);
+    g.nseg = A.nseg;
     return true;
   }
 
-  __device__ static void process(const Args& A, int64_t u, const void* rowp, int64_t j0,
-                                 int64_t j1, const unsigned char* chunk, bool poisoned,
-                                 Smem& sm) {
-    int r, i, c;
-    decode(A, u, r, i, c);
-    bool n_ok;
-    const int n = n_of(A, r, n_ok);
-    const int R = A.k + 1;
+  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
+                                    const uint4 (&v)[kVecPerThread], bool poison) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-
+    const int64_t j0 = (int64_t)c * E::kChunk;
     float best = -INFINITY;
     int bidx = kNoIndex;
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
-      const uint4 v = chunk_vec<E>(chunk, it, j0, j1, kPad);
-      const int jb = (int)(j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec);
+      const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
-        const float z = E::get(v, l);
+        const float z = E::get(v[it], l);
         // in increasing j: the first comparable logit, then only strictly larger ones
         if (z > best || (bidx == kNoIndex && z == z)) {
           best = z;
@@ -723,42 +713,42 @@ struct GreedyOp {
     }
     warp_argmax(best, bidx);
     if (lane == 0) {
-      sm.v[w] = best;
-      sm.idx[w] = bidx;
+      WarpArgmax* p = A.part + ((g.rid * A.nch + c) * kWarps + w);
+      *reinterpret_cast<float2*>(p) = make_float2(best, __int_as_float(poison ? kPoisoned : bidx));
     }
-    cbar();
-    const int64_t rid = (int64_t)r * R + i;
-    if (threadIdx.x == 0) {
-      float bv = sm.v[0];
-      int bi = sm.idx[0];
-      for (int q = 1; q < kWarps; ++q) argmax_merge(bv, bi, sm.v[q], sm.idx[q]);
-      ChunkArgmax* p = A.chunk + rid * A.nch + c;
-      p->v = bv;
-      p->idx = poisoned ? kPoisoned : bi;
-      sm.row_last = arrive_last(A.row_cnt + rid, (unsigned)A.nch);
-    }
-    cbar();
+  }
+
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm) {
+    const int r = g.r;
+    bool n_ok;
+    const int n = n_of(A, r, n_ok);
+    const int R = A.k + 1;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
+    __syncthreads();
     if (!sm.row_last) return;
     __threadfence();
 
     if (threadIdx.x < 32) {
+      const int np = A.nch * kWarps;
+      const WarpArgmax* wp = A.part + g.rid * np;
       float bv = -INFINITY;
       int bi = kNoIndex;
       bool poison = false;
-      for (int cc = lane; cc < A.nch; cc += 32) {
-        const ChunkArgmax* p = A.chunk + rid * A.nch + cc;
-        const int pi = __ldcg(&p->idx);
+      for (int q = lane; q < np; q += 32) {
+        const float2 pv = __ldcg(reinterpret_cast<const float2*>(wp + q));
+        const int pi = __float_as_int(pv.y);
         poison |= pi == kPoisoned;
-        argmax_merge(bv, bi, __ldcg(&p->v), pi == kPoisoned ? kNoIndex : pi);
+        argmax_merge(bv, bi, pv.x, pi == kPoisoned ? kNoIndex : pi);
       }
       warp_argmax(bv, bi);
       poison = __any_sync(0xffffffffu, poison);
       if (lane == 0) {
-        A.row[rid] = (bi == kNoIndex || poison) ? -1 : bi;
+        A.row[g.rid] = (bi == kNoIndex || poison) ? -1 : bi;
         sm.req_last = arrive_last(A.req_cnt + r, (unsigned)(n + 1));
       }
     }
-    cbar();
+    __syncthreads();
     if (!sm.req_last) return;
     __threadfence();
 
@@ -767,14 +757,14 @@ struct GreedyOp {
       bool bad = !n_ok;
       bool mism = false;
       if (n_ok && lane <= n) {
-        const int g = __ldcg(A.row + (int64_t)r * R + lane);
-        bad = g < 0;
+        const int gi = __ldcg(A.row + (int64_t)r * R + lane);
+        bad = gi < 0;
         if (lane < n) {
           const int32_t xi = __ldg(A.tokens + (int64_t)r * A.k + lane);
           bad = bad || xi < 0 || xi >= A.V;
-          mism = xi != g;
+          mism = xi != gi;
         }
-        sm.g[lane] = g;
+        sm.g[lane] = gi;
       }
       const bool err = __any_sync(0xffffffffu, bad);
       const unsigned mm = __ballot_sync(0xffffffffu, mism);
@@ -838,7 +828,8 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
       (out_resid_mass && !aligned_to(out_resid_mass, 4)))
     return SV_ERR_INVALID_ARG;
   const int64_t nch = num_chunks(V, dtype);
-  const int64_t units = (int64_t)B * (2 * k + 1) * nch;
+  const int nseg = num_segments(nch);
+  const int64_t units = (int64_t)B * (2 * k + 1) * nseg;
   if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
   const SampleLayout L = sample_layout(B, k, V, dtype);
   if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
@@ -854,6 +845,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.k = k;
   A.V = V;
   A.nch = (int)nch;
+  A.nseg = nseg;
   A.s = (float)(1.4426950408889634074 / (double)temperature);
   A.aligned = rows_aligned(target_logits, V, dtype) && rows_aligned(draft_logits, V, dtype);
   A.out_tokens = out_tokens;
@@ -862,7 +854,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.out_q = out_q_draft;
   A.out_resid = out_resid_mass;
   char* ws = static_cast<char*>(workspace);
-  A.chunk = reinterpret_cast<ChunkSoftmax*>(ws + L.chunk);
+  A.part = reinterpret_cast<WarpSoftmax*>(ws + L.part);
   A.row = reinterpret_cast<RowSoftmax*>(ws + L.row);
   A.resid = reinterpret_cast<double*>(ws + L.resid);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
@@ -872,8 +864,8 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
-  if (dtype == SV_F32) return launch_units<SampleOp<F32>>(A, units, ctl, st);
-  return launch_units<SampleOp<BF16>>(A, units, ctl, st);
+  if (dtype == SV_F32) return launch_segments<SampleOp<F32>>(A, units, ctl, st);
+  return launch_segments<SampleOp<BF16>>(A, units, ctl, st);
 }
 
 extern "C" size_t spec_verify_greedy_workspace(int B, int k, int V, sv_dtype dtype) {
@@ -898,7 +890,8 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
       (num_draft && !aligned_to(num_draft, 4)))
     return SV_ERR_INVALID_ARG;
   const int64_t nch = num_chunks(V, dtype);
-  const int64_t units = (int64_t)B * (k + 1) * nch;
+  const int nseg = num_segments(nch);
+  const int64_t units = (int64_t)B * (k + 1) * nseg;
   if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
   const GreedyLayout L = greedy_layout(B, k, V, dtype);
   if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
@@ -912,11 +905,12 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   A.k = k;
   A.V = V;
   A.nch = (int)nch;
+  A.nseg = nseg;
   A.aligned = rows_aligned(target_logits, V, dtype);
   A.out_tokens = out_tokens;
   A.out_accept_len = out_accept_len;
   char* ws = static_cast<char*>(workspace);
-  A.chunk = reinterpret_cast<ChunkArgmax*>(ws + L.chunk);
+  A.part = reinterpret_cast<WarpArgmax*>(ws + L.part);
   A.row = reinterpret_cast<int*>(ws + L.row);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
@@ -924,6 +918,6 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
-  if (dtype == SV_F32) return launch_units<GreedyOp<F32>>(A, units, ctl, st);
-  return launch_units<GreedyOp<BF16>>(A, units, ctl, st);
+  if (dtype == SV_F32) return launch_segments<GreedyOp<F32>>(A, units, ctl, st);
+  return launch_segments<GreedyOp<BF16>>(A, units, ctl, st);
 }
