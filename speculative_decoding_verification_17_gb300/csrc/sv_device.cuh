@@ -56,6 +56,11 @@ struct F32 {
   __device__ static __forceinline__ uint4 pad_vec(uint32_t pad) {
     return make_uint4(pad, pad, pad, pad);
   }
+  // Logits 2p and 2p+1 of a vector.
+  __device__ static __forceinline__ float2 get2(const uint4& v, int p) {
+    return p == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
   // Largest logit of a vector (NaN ignored, as fmaxf does).
   __device__ static __forceinline__ float max_vec(const uint4& v) {
     return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
@@ -83,6 +88,11 @@ struct BF16 {
   __device__ static __forceinline__ uint4 pad_vec(uint32_t pad) {
     const uint32_t w = pad | (pad << 16);
     return make_uint4(w, w, w, w);
+  }
+  // Logits 2p and 2p+1 of a vector (one packed bf16 pair, widened exactly).
+  __device__ static __forceinline__ float2 get2(const uint4& v, int p) {
+    const uint32_t w = p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
   __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -234,13 +244,17 @@ __device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
 }
 
 // ---- completion counters -------------------------------------------------------------------
-// Release this group's partial results and count it in; true for the group that arrives
-// last. Called by one thread after that thread stored the partials it publishes. The
-// counters are cleared by the host call (an async memset on the same stream) before every
-// launch.
+// Count this CTA in on a completion counter; true for the CTA that arrives last. Called by
+// one thread after a CTA barrier that follows the stores the CTA publishes: the add is a
+// release at GPU scope (cumulative over what the barrier ordered before it) and an acquire
+// for the arriving thread. The counters are cleared by the host call (an async memset on the
+// same stream) before every launch.
 __device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int expected) {
-  __threadfence();
-  const unsigned int prev = atomicAdd(counter, 1u);
+  unsigned int prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+               : "=r"(prev)
+               : "l"(counter)
+               : "memory");
   return prev == expected - 1;
 }
 

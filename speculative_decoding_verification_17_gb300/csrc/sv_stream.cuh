@@ -7,17 +7,17 @@
 // has no CTA-wide barrier at all.
 //
 // For a row that starts on a 16-byte boundary the segment's chunks stream through a
-// two-stage shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each
+// kStages-deep shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each
 // completing on that stage's mbarrier; the last warp to finish reading a stage (a shared
-// counter) starts the copy of the chunk two ahead into it, so the next chunk lands while
+// counter) starts the copy of the chunk kStages ahead into it, so the next chunks land while
 // the current one is reduced. Rows that are not 16-byte aligned are read straight from
 // global memory, logit by logit. Every mbarrier wait is bounded: a copy that never lands
 // poisons its row (the request gets the error sentinel) and sets a bit in the call's
 // control word.
 //
-// After the segment, thread 0 publishes the segment (fence, then an atomic on the row's
-// counter); the CTA that completes a row merges its partials, and the one that completes a
-// request finishes the request. No CTA ever waits for another one.
+// After the segment, thread 0 publishes the segment (one acquire-release atomic on the row's
+// counter, after a CTA barrier); the CTA that completes a row merges its partials, and the
+// one that completes a request finishes the request. No CTA ever waits for another one.
 //
 // An operation Op provides:
 //   using E; static constexpr uint32_t kPad; struct Smem; struct Args (with bool aligned);
@@ -35,12 +35,20 @@
 
 namespace sv {
 
-constexpr int kSegChunks = 4;  // chunks per CTA
-constexpr int kStages = 2;     // ring depth
+// Tuning constants (a build may override them to try other values): chunks per CTA, ring
+// depth, and CTAs resident per SM (shared memory: kCtasPerSm * kStages * 32 KiB <= 227 KiB).
+#ifndef SV_SEG_CHUNKS
+#define SV_SEG_CHUNKS 8
+#endif
+#ifndef SV_STAGES
+#define SV_STAGES 2
+#endif
 #ifndef SV_CTAS_PER_SM
 #define SV_CTAS_PER_SM 3
 #endif
-constexpr int kCtasPerSm = SV_CTAS_PER_SM;  // 3 x 64 KiB of ring per SM
+constexpr int kSegChunks = SV_SEG_CHUNKS;
+constexpr int kStages = SV_STAGES;
+constexpr int kCtasPerSm = SV_CTAS_PER_SM;
 constexpr int kRingBytes = kStages * kChunkBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far past any legitimate wait
 
@@ -98,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     __syncthreads();
     for (int ci = 0; ci < nc; ++ci) {
-      const int s = ci & (kStages - 1);
+      const int s = ci % kStages;
       const bool ok = mbar_wait(&full[s], (uint32_t)((ci / kStages) & 1), kWaitLimitNs);
       const bool poison = __any_sync(0xffffffffu, !ok);
       if (poison && lane == 0) atomicOr(&ctl->error, 1u);
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                                         : E::pad_vec(Op::kPad);
       }
       __syncwarp();
-      if (lane == 0) {  // the last warp out of a stage refills it with the chunk two ahead
+      if (lane == 0) {  // the last warp out of a stage refills it with the chunk kStages ahead
         if (atomic_add_acq_rel_cta(&released[s], 1) == kWarps - 1) {
           released[s] = 0;
           if (ci + kStages < nc)
@@ -146,7 +154,7 @@ sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* 
                           cudaStream_t st) {
   if (units <= 0) return SV_OK;
   // host-side function attributes (no stream work), set on every call so they hold in any
-  // context: 64 KiB of dynamic shared memory, and the carveout that fits kCtasPerSm CTAs
+  // context: the ring's dynamic shared memory, and the carveout that fits kCtasPerSm CTAs
   cudaError_t e = cudaFuncSetAttribute(segment_kernel<Op>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
   if (e != cudaSuccess) return cuda_fail(e);

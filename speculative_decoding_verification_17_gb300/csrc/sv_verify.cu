@@ -357,24 +357,28 @@ struct SampleOp {
     } else {
       const float s = A.s;
       const float K = ceilf(m * s);
-      const float cK = -K;
-      float part[kVecPerThread];
+      // logits two at a time: packed fp32x2 FMA and adds, two SFU exp2 per pair
+      const float2 s2 = make_float2(s, s), c2 = make_float2(-K, -K);
+      float2 part[kVecPerThread];
 #pragma unroll
       for (int it = 0; it < kVecPerThread; ++it) {
-        float e[E::kPerVec];
+        float2 e[E::kPerVec / 2];
 #pragma unroll
-        for (int l = 0; l < E::kPerVec; ++l) e[l] = ex2(fmaf(E::get(v[it], l), s, cK));
+        for (int p = 0; p < E::kPerVec / 2; ++p) {
+          const float2 x = __ffma2_rn(E::get2(v[it], p), s2, c2);
+          e[p] = make_float2(ex2(x.x), ex2(x.y));
+        }
 #pragma unroll
-        for (int q = E::kPerVec / 2; q >= 1; q >>= 1)
+        for (int q = E::kPerVec / 4; q >= 1; q >>= 1)
 #pragma unroll
-          for (int l = 0; l < q; ++l) e[l] = e[l] + e[l + q];
+          for (int p = 0; p < q; ++p) e[p] = __fadd2_rn(e[p], e[p + q]);
         part[it] = e[0];
       }
 #pragma unroll
       for (int q = kVecPerThread / 2; q >= 1; q >>= 1)
 #pragma unroll
-        for (int l = 0; l < q; ++l) part[l] = part[l] + part[l + q];
-      float hi = part[0], lo = 0.0f;
+        for (int l = 0; l < q; ++l) part[l] = __fadd2_rn(part[l], part[l + q]);
+      float hi = part[0].x + part[0].y, lo = 0.0f;
       warp_sum_compensated(hi, lo);
       out = WarpSoftmax{K, hi, lo, 0.0f};
     }
