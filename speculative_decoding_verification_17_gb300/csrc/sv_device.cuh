@@ -312,13 +312,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 // Bulk copy (TMA, non-tensor) of `bytes` (a multiple of 16) from 16-byte aligned global
-// memory into this CTA's shared memory, completing on `bar`.
+// memory into this CTA's shared memory, completing on `bar`. SV_L2_POLICY picks the L2
+// eviction priority of the copied lines: 0 leaves the copy's default, 1 normal, 2 last.
+#ifndef SV_L2_POLICY
+#define SV_L2_POLICY 0
+#endif
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                         uint64_t* bar) {
+#if SV_L2_POLICY == 0
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+#else
+  uint64_t policy;
+#if SV_L2_POLICY == 1
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(policy));
+#else
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+#endif
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+#endif
 }
 __device__ __forceinline__ uint4 lds16(const void* p) {
   uint4 v;

@@ -123,7 +123,7 @@ struct GateOp {
     }
   }
 
-  __device__ static void finish(const Args& A, const Seg& g, Smem& sm) {
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring&) {
     const int row = g.r;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + row, (unsigned)g.nseg);

@@ -25,7 +25,7 @@
 //   static void warp_chunk(const Args&, const Seg&, int c, const uint4 (&v)[8], bool poison);
 //       one warp, chunk c of the row, the warp's 8 vectors v (lane l holds vector
 //       w*256 + it*32 + l of the chunk in v[it]); stores the warp's partial
-//   static void finish(const Args&, const Seg&, Smem&);     all threads, after the segment
+//   static void finish(const Args&, const Seg&, Smem&, Ring&);  all threads, after the segment
 #pragma once
 
 #include <cuda_runtime.h>
@@ -60,6 +60,18 @@ struct Seg {
   int slot;     // row slot inside the request
   int c0, c1;
   int nseg;     // segments of this row
+};
+
+// The CTA's shared-memory ring as the finishing code may reuse it once pass 1 is done:
+// its buffer, the stage barriers and release counters, how many phases each stage's barrier
+// has completed, and the call's control word. `usable` is false for rows read without TMA.
+struct Ring {
+  unsigned char* buf;
+  uint64_t* full;
+  int* released;
+  uint32_t used[kStages];
+  CallCtl* ctl;
+  bool usable;
 };
 
 // Index of the 16-byte vector lane `lane` of warp `w` holds in slot `it` of a chunk.
@@ -145,7 +157,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   }
   __syncthreads();  // every warp partial of the segment is stored
-  Op::finish(A, g, sm);
+  Ring ring_state;
+  ring_state.buf = ring;
+  ring_state.full = full;
+  ring_state.released = released;
+  for (int q = 0; q < kStages; ++q) ring_state.used[q] = A.aligned ? (nc - q + kStages - 1) / kStages : 0;
+  ring_state.ctl = ctl;
+  ring_state.usable = A.aligned;
+  Op::finish(A, g, sm, ring_state);
 }
 
 // Launch the segments of a row operation. `ctl` lies in the region the caller just cleared.

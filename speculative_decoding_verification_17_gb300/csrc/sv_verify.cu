@@ -388,12 +388,15 @@ struct SampleOp {
     }
   }
 
-  __device__ static void finish(const Args& A, const Seg& g, Smem& sm);
-  __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm);
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring& ring);
+  __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
+                                        Ring& ring);
+  __device__ static void residual_masses(const Args& A, const ResidScan<E>& rs, double* part,
+                                         Smem& sm, Ring& ring);
 };
 
 template <typename ET>
-__device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm) {
+__device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring& ring) {
   const int r = g.r;
   bool n_ok;
   const int n = n_of(A, r, n_ok);
@@ -445,11 +448,113 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm) {
   __syncthreads();
   if (!sm.req_last) return;
   __threadfence();
-  finish_request(A, r, n, n_ok, sm);
+  finish_request(A, r, n, n_ok, sm, ring);
+}
+
+// Per-warp residual masses of every chunk of the rejected pair (rs), into part[c][warp].
+// With the TMA ring (aligned rows) the pair streams through the two stages half a chunk at a
+// time: a stage holds 16 KiB of the target row and the same 16 KiB of the draft row, two bulk
+// copies completing on the stage barrier, and the last warp out of a stage starts the copy
+// of the half two ahead. Without it, every thread loads its vectors from global memory.
+template <typename ET>
+__device__ void SampleOp<ET>::residual_masses(const Args& A, const ResidScan<E>& rs,
+                                              double* part, Smem& sm, Ring& ring) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!ring.usable) {
+    for (int c = 0; c < A.nch; ++c) {
+      const int64_t j0 = (int64_t)c * E::kChunk;
+      ResidScan<E> q = rs;
+      q.j1 = chunk_end<E>(j0, A.V);
+      float acc = 0.0f;
+#pragma unroll
+      for (int h = 0; h < kVecPerThread; h += 2) {
+        typename ResidScan<E>::Raw raw[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          raw[t] = q.load(j0 + (int64_t)((h + t) * kThreads + tid) * E::kPerVec);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float w[E::kPerVec];
+          q.weights(raw[t], w);
+#pragma unroll
+          for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
+        }
+      }
+      float hi = acc, lo = 0.0f;
+      warp_sum_compensated(hi, lo);
+      if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
+    }
+    return;
+  }
+  constexpr int kHalf = E::kChunk / 2;           // logits per half chunk
+  constexpr int kHalfBytes = kChunkBytes / 2;    // 16 KiB
+  constexpr int kHalfVecPerLane = kVecPerThread / 2;
+  const int nh = 2 * A.nch;
+  auto issue = [&](int h) {
+    const int st = h % kStages;
+    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
+    const int64_t e = b + kHalf < A.V ? b + kHalf : (int64_t)A.V;
+    const uint32_t bytes = e > b ? (uint32_t)((e - b) * (16 / E::kPerVec)) : 0u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (bytes == 0) {
+      mbar_arrive(&ring.full[st]);
+      return;
+    }
+    mbar_arrive_expect_tx(&ring.full[st], 2 * bytes);
+    bulk_g2s(ring.buf + st * kChunkBytes, static_cast<const char*>(rs.rp) + b * (16 / E::kPerVec),
+             bytes, &ring.full[st]);
+    bulk_g2s(ring.buf + st * kChunkBytes + kHalfBytes,
+             static_cast<const char*>(rs.rq) + b * (16 / E::kPerVec), bytes, &ring.full[st]);
+  };
+  if (tid == 0)
+    for (int h = 0; h < kStages && h < nh; ++h) issue(h);
+  // every thread follows the same barrier phases
+  float acc = 0.0f;
+  bool timed_out = false;
+  for (int h = 0; h < nh; ++h) {
+    const int st = h % kStages;
+    const uint32_t par = (ring.used[st] + (uint32_t)(h / kStages)) & 1u;
+    if (!mbar_wait(&ring.full[st], par, kWaitLimitNs)) timed_out = true;
+    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
+    const int64_t e = b + kHalf < A.V ? b + kHalf : (int64_t)A.V;
+    const unsigned char* buf = ring.buf + st * kChunkBytes;
+    uint4 vp[kHalfVecPerLane], vq[kHalfVecPerLane];
+#pragma unroll
+    for (int it = 0; it < kHalfVecPerLane; ++it) {
+      const int slot = warp * (kHalfVecPerLane * 32) + it * 32 + lane;
+      const bool in = b + (int64_t)slot * E::kPerVec < e;
+      vp[it] = in ? lds16(buf + slot * 16) : E::pad_vec(E::kNegInfBits);
+      vq[it] = in ? lds16(buf + kHalfBytes + slot * 16) : E::pad_vec(E::kNegInfBits);
+    }
+    __syncwarp();
+    if (lane == 0 && atomic_add_acq_rel_cta(&ring.released[st], 1) == kWarps - 1) {
+      ring.released[st] = 0;
+      if (h + kStages < nh) issue(h + kStages);
+    }
+#pragma unroll
+    for (int it = 0; it < kHalfVecPerLane; ++it) {
+      float w[E::kPerVec];
+      rs.weights(typename ResidScan<E>::Raw{vp[it], vq[it]}, w);
+#pragma unroll
+      for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
+    }
+    if (h & 1) {  // both halves of chunk h/2 are in
+      float hi = acc, lo = 0.0f;
+      warp_sum_compensated(hi, lo);
+      if (lane == 0) part[(int64_t)(h >> 1) * kWarps + warp] = (double)hi + (double)lo;
+      acc = 0.0f;
+    }
+  }
+  for (int st = 0; st < kStages; ++st) ring.used[st] += (uint32_t)((nh - st + kStages - 1) / kStages);
+  if (__any_sync(0xffffffffu, timed_out) && lane == 0) {
+    atomicOr(&ring.ctl->error, 1u);
+    for (int c = 0; c < A.nch; ++c) part[(int64_t)c * kWarps + warp] = __longlong_as_double(0x7ff8000000000000ll);
+  }
 }
 
 template <typename ET>
-__device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm) {
+__device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
+                                             Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = 2 * A.k + 1;
   const int32_t* x = A.tokens + (int64_t)r * A.k;
@@ -516,30 +621,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     rs.wf.ip = (float)(1.0 / tp.S);
     rs.wf.iq = (float)(1.0 / dq.S);
     double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
-    // every warp walks all chunks on its own (no barrier per chunk): four vectors in flight
-    // per thread at a time, one compensated warp sum per chunk
-    for (int c = 0; c < A.nch; ++c) {
-      const int64_t j0 = (int64_t)c * E::kChunk;
-      rs.j1 = chunk_end<E>(j0, A.V);
-      float acc = 0.0f;
-#pragma unroll
-      for (int h = 0; h < kVecPerThread; h += 2) {
-        typename ResidScan<E>::Raw raw[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          raw[q] = rs.load(j0 + (int64_t)((h + q) * kThreads + tid) * E::kPerVec);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float w[E::kPerVec];
-          rs.weights(raw[q], w);
-#pragma unroll
-          for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
-        }
-      }
-      float hi = acc, lo = 0.0f;
-      warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
-    }
+    residual_masses(A, rs, part, sm, ring);
     __syncthreads();
     // chunk masses R_c = sum over warps (fixed order) and W = sum_c R_c (warp 0)
     if (tid < 32) {
@@ -722,7 +804,7 @@ struct GreedyOp {
     }
   }
 
-  __device__ static void finish(const Args& A, const Seg& g, Smem& sm) {
+  __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring&) {
     const int r = g.r;
     bool n_ok;
     const int n = n_of(A, r, n_ok);
