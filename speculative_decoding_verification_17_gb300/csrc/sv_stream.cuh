@@ -69,10 +69,18 @@ struct Ring {
   unsigned char* buf;
   uint64_t* full;
   int* released;
-  uint32_t used[kStages];
+  uint32_t phase;  // bit s: parity of the next wait on stage s
   CallCtl* ctl;
   bool usable;
 };
+
+// Wait (bounded) for the next phase of stage s; every thread of the CTA calls this for every
+// use of the stage, in the same order, so all keep the same phase bits.
+__device__ __forceinline__ bool ring_wait(Ring& R, int s) {
+  const bool ok = mbar_wait(&R.full[s], (R.phase >> s) & 1u, kWaitLimitNs);
+  R.phase ^= 1u << s;
+  return ok;
+}
 
 // Index of the 16-byte vector lane `lane` of warp `w` holds in slot `it` of a chunk.
 __device__ __forceinline__ int warp_vec_slot(int w, int it, int lane) {
@@ -161,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   ring_state.buf = ring;
   ring_state.full = full;
   ring_state.released = released;
-  for (int q = 0; q < kStages; ++q) ring_state.used[q] = A.aligned ? (nc - q + kStages - 1) / kStages : 0;
+  ring_state.phase = 0;
+  if (A.aligned)
+    for (int q = 0; q < kStages; ++q) ring_state.phase |= (uint32_t)(((nc - q + kStages - 1) / kStages) & 1) << q;
   ring_state.ctl = ctl;
   ring_state.usable = A.aligned;
   Op::finish(A, g, sm, ring_state);

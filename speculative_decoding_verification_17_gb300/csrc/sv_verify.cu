@@ -36,6 +36,10 @@
 #include "sv_host.h"
 #include "sv_stream.cuh"
 
+#ifndef SV_RESID_RING
+#define SV_RESID_RING 1  // residual pass through the TMA ring (0: register loads)
+#endif
+
 namespace sv {
 
 constexpr int kPoisoned = -2;  // an index that marks a slice whose copy never landed
@@ -272,6 +276,58 @@ struct BonusScan {
   }
 };
 
+// The same weights read from a chunk staged in shared memory (vector i of the chunk at
+// p + 16*i, likewise q), for the in-chunk scan after a bulk copy of the chosen chunk.
+template <typename E>
+struct ResidScanSmem {
+  const unsigned char* p;
+  const unsigned char* q;
+  int64_t j0, j1;
+  ResidW wf;
+  struct Raw {
+    uint4 p, q;
+  };
+  __device__ __forceinline__ Raw load(int64_t j) const {
+    if (j >= j1) return {E::pad_vec(E::kNegInfBits), E::pad_vec(E::kNegInfBits)};
+    const int i = (int)((j - j0) / E::kPerVec);
+    return {lds16(p + i * 16), lds16(q + i * 16)};
+  }
+  __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
+#pragma unroll
+    for (int l = 0; l < E::kPerVec; ++l) w[l] = wf(E::get(r.p, l), E::get(r.q, l));
+  }
+};
+
+template <typename E>
+struct BonusScanSmem {
+  const unsigned char* p;
+  int64_t j0, j1;
+  float s, c;
+  using Raw = uint4;
+  __device__ __forceinline__ Raw load(int64_t j) const {
+    if (j >= j1) return E::pad_vec(E::kNegInfBits);
+    return lds16(p + (int)((j - j0) / E::kPerVec) * 16);
+  }
+  __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
+#pragma unroll
+    for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, c));
+  }
+};
+
+// Stage chunk [j0, j1) of a row into ring stage `st` with one bulk copy (thread 0), then wait
+// for it (every thread). False if the copy never landed.
+template <typename E>
+__device__ bool stage_chunk(Ring& ring, int st, const void* row, int64_t j0, int64_t j1) {
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(&ring.full[st], bytes);
+    bulk_g2s(ring.buf + st * kChunkBytes, static_cast<const char*>(row) + j0 * (16 / E::kPerVec),
+             bytes, &ring.full[st]);
+  }
+  return ring_wait(ring, st);
+}
+
 __device__ __forceinline__ WarpSoftmax ld_part(const WarpSoftmax* p) {
   const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
   return {v.x, v.y, v.z, v.w};
@@ -460,7 +516,7 @@ template <typename ET>
 __device__ void SampleOp<ET>::residual_masses(const Args& A, const ResidScan<E>& rs,
                                               double* part, Smem& sm, Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!ring.usable) {
+  if (!ring.usable || !SV_RESID_RING) {
     for (int c = 0; c < A.nch; ++c) {
       const int64_t j0 = (int64_t)c * E::kChunk;
       ResidScan<E> q = rs;
@@ -513,8 +569,7 @@ __device__ void SampleOp<ET>::residual_masses(const Args& A, const ResidScan<E>&
   bool timed_out = false;
   for (int h = 0; h < nh; ++h) {
     const int st = h % kStages;
-    const uint32_t par = (ring.used[st] + (uint32_t)(h / kStages)) & 1u;
-    if (!mbar_wait(&ring.full[st], par, kWaitLimitNs)) timed_out = true;
+    if (!ring_wait(ring, st)) timed_out = true;
     const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
     const int64_t e = b + kHalf < A.V ? b + kHalf : (int64_t)A.V;
     const unsigned char* buf = ring.buf + st * kChunkBytes;
@@ -545,7 +600,6 @@ __device__ void SampleOp<ET>::residual_masses(const Args& A, const ResidScan<E>&
       acc = 0.0f;
     }
   }
-  for (int st = 0; st < kStages; ++st) ring.used[st] += (uint32_t)((nh - st + kStages - 1) / kStages);
   if (__any_sync(0xffffffffu, timed_out) && lane == 0) {
     atomicOr(&ring.ctl->error, 1u);
     for (int c = 0; c < A.nch; ++c) part[(int64_t)c * kWarps + warp] = __longlong_as_double(0x7ff8000000000000ll);
@@ -654,7 +708,17 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       __syncthreads();
       const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
       rs.j1 = chunk_end<E>(j0, A.V);
-      t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, rs, sm.scan);
+      if (ring.usable) {
+        // the chosen chunk of both rows into the two stages, then the scan from shared memory
+        __syncthreads();  // nobody still reads the ring
+        const bool ok0 = stage_chunk<E>(ring, 0, rs.rp, j0, rs.j1);
+        const bool ok1 = stage_chunk<E>(ring, 1, rs.rq, j0, rs.j1);
+        ResidScanSmem<E> ss{ring.buf, ring.buf + kChunkBytes, j0, rs.j1, rs.wf};
+        t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
+        if (!__syncthreads_and(ok0 && ok1)) t = -1;
+      } else {
+        t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, rs, sm.scan);
+      }
       drew = true;
     }
   }
@@ -692,7 +756,15 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     bs.c = -rsw.K;
     const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
     bs.j1 = chunk_end<E>(j0, A.V);
-    t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, bs, sm.scan);
+    if (ring.usable) {
+      __syncthreads();  // nobody still reads the ring
+      const bool ok = stage_chunk<E>(ring, 0, bs.row, j0, bs.j1);
+      BonusScanSmem<E> ss{ring.buf, j0, bs.j1, s, bs.c};
+      t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
+      if (!__syncthreads_and(ok)) t = -1;
+    } else {
+      t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, bs, sm.scan);
+    }
   }
 
   // ---- emit ----
