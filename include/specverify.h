@@ -152,6 +152,31 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
                              void* workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Greedy verify for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a convenience of the library. Some callers cannot
+ * allocate device memory at all, for example an engine that has handed the whole device to
+ * its own memory pool, or code on a path where cudaMalloc's implicit synchronisation is not
+ * allowed. This call computes exactly what spec_verify_greedy computes (same arguments,
+ * outputs and error sentinels) but takes no workspace: it uses a fixed 8 MiB scratch array
+ * that lives in the library's device image, which every GPU that loads the library keeps
+ * until the process exits.
+ *   - Limit: spec_verify_greedy_workspace(B, k, V, dtype) must be at most 8 MiB (8388608
+ *     bytes); a larger shape returns SV_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   - Every call on a device shares the one array: it clears the counters it needs at the
+ *     start (an asynchronous memset on `stream`), and calls whose work overlaps on the GPU
+ *     (on different streams, or from different host threads) race and give wrong results.
+ *     Issue them on one stream, or order them.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ * ---------------------------------------------------------------------------------------- */
+sv_status spec_verify_greedy_noalloc(const void* target_logits, sv_dtype dtype,
+                                     const int32_t* draft_tokens, const int32_t* num_draft,
+                                     int B, int k, int V, int32_t* out_tokens,
+                                     int32_t* out_accept_len, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Logit-gap confidence gate.
  *
  * Defined by: "Speculative Pre-Positioning", section 2.4, Eq. (11) (gamma = l(1) - l(2), the

@@ -10,12 +10,14 @@ Calls (same names as the C ABI):
 
 - :func:`spec_verify_sample` — modified-rejection verify with residual/bonus draw.
 - :func:`spec_verify_greedy` — greedy (temperature-0) verify.
+- :func:`spec_verify_greedy_noalloc` — the same without a workspace (fixed library scratch).
 - :func:`logit_gap_gate`     — top-1/top-2 logit-gap confidence gate.
 - :func:`ngram_propose`      — prompt-lookup n-gram draft proposer.
 
-Workspaces: pass ``workspace=`` (a zero-filled uint8 CUDA tensor of at least the size
-the matching ``*_workspace`` query returns, not shared by calls in flight at the same
-time), or let the binding keep one cached per (device, call) that it grows as needed.
+Workspaces: pass ``workspace=`` (a uint8 CUDA tensor of at least the size the matching
+``*_workspace`` query returns, 256-byte aligned, not shared by calls in flight at the same
+time; it needs no initialisation), or let the binding keep one cached per (device, call)
+that it grows as needed.
 """
 from __future__ import annotations
 
@@ -29,7 +31,7 @@ from . import _native
 __all__ = [
     "SVError", "SV_F32", "SV_BF16", "SV_MAX_K", "build", "library", "version",
     "spec_verify_sample_workspace", "spec_verify_sample",
-    "spec_verify_greedy_workspace", "spec_verify_greedy",
+    "spec_verify_greedy_workspace", "spec_verify_greedy", "spec_verify_greedy_noalloc",
     "logit_gap_gate_workspace", "logit_gap_gate", "ngram_propose",
 ]
 
@@ -191,6 +193,31 @@ def spec_verify_greedy(target_logits, draft_tokens, num_draft=None, *, out_token
     _ok(library().spec_verify_greedy(
         _ptr(target_logits), code, _ptr(draft_tokens), _ptr(num_draft), B, k, V,
         _ptr(out_tokens), _ptr(out_accept_len), _ptr(ws), ws.numel(), h), "spec_verify_greedy")
+    return out_tokens, out_accept_len
+
+
+def spec_verify_greedy_noalloc(target_logits, draft_tokens, num_draft=None, *, out_tokens=None,
+                               out_accept_len=None, stream=None):
+    """Greedy verify without a workspace, for callers that cannot allocate device memory:
+    it uses the library's fixed 8 MiB scratch array (shapes needing more are rejected).
+    Calls that overlap on the GPU share that array and race. Returns (tokens, accept_len)."""
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    code = _dtype_code(target_logits)
+    _check_cuda("target_logits", target_logits)
+    _check_cuda("draft_tokens", draft_tokens, torch.int32, (B, k), dev)
+    _check_cuda("num_draft", num_draft, torch.int32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check_cuda("out_tokens", out_tokens, torch.int32, (B, k + 1), dev)
+    _check_cuda("out_accept_len", out_accept_len, torch.int32, (B,), dev)
+    h, _ = _stream_handle(stream)
+    _ok(library().spec_verify_greedy_noalloc(
+        _ptr(target_logits), code, _ptr(draft_tokens), _ptr(num_draft), B, k, V,
+        _ptr(out_tokens), _ptr(out_accept_len), h), "spec_verify_greedy_noalloc")
     return out_tokens, out_accept_len
 
 

@@ -113,6 +113,8 @@ def _declare(L):
     L.spec_verify_greedy_workspace.argtypes = [I, I, I, I]
     L.spec_verify_greedy.restype = I
     L.spec_verify_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, Z, P]
+    L.spec_verify_greedy_noalloc.restype = I
+    L.spec_verify_greedy_noalloc.argtypes = [P, I, P, P, I, I, I, P, P, P]
     L.logit_gap_gate_workspace.restype = Z
     L.logit_gap_gate_workspace.argtypes = [I, I, I]
     L.logit_gap_gate.restype = I

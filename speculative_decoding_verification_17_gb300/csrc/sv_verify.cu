@@ -30,6 +30,7 @@
 //                           masses from the pass-1 partials, one chunk scanned).
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "specverify.h"
 #include "sv_device.cuh"
@@ -1078,4 +1079,59 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_segments<GreedyOp<F32>>(A, units, ctl, st);
   return launch_segments<GreedyOp<BF16>>(A, units, ctl, st);
+}
+
+// ============================================================================================
+// Greedy verify without caller-provided scratch
+// ============================================================================================
+// Some callers cannot allocate device memory at all: an engine that has handed every byte of
+// the device to its own pool, or code on a path where cudaMalloc's implicit synchronisation
+// is not allowed. For them the greedy verify can use a scratch buffer that lives in this
+// library's own device image: a fixed array every GPU that loads the library holds until the
+// process exits. Its device address is looked up once per device, on the first call made with
+// that device current.
+namespace {
+
+constexpr size_t kGreedyScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr int kMaxScratchDevices = 64;
+
+static __device__ __align__(256) unsigned char g_greedy_scratch[kGreedyScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_greedy_scratch on the current device (looked up on first use).
+sv_status greedy_scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxScratchDevices) return SV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_greedy_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" sv_status spec_verify_greedy_noalloc(const void* target_logits, sv_dtype dtype,
+                                                const int32_t* draft_tokens,
+                                                const int32_t* num_draft, int B, int k, int V,
+                                                int32_t* out_tokens, int32_t* out_accept_len,
+                                                sv_stream_t stream) {
+  if (B < 0 || k < 1 || V < 2) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (k > SV_MAX_K) return SV_ERR_UNSUPPORTED;
+  if (B == 0) return SV_OK;
+  if (greedy_layout(B, k, V, dtype).total > kGreedyScratchBytes) return SV_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const sv_status st = greedy_scratch_address(&scratch);
+  if (st != SV_OK) return st;
+  return spec_verify_greedy(target_logits, dtype, draft_tokens, num_draft, B, k, V, out_tokens,
+                            out_accept_len, scratch, kGreedyScratchBytes, stream);
 }
