@@ -70,35 +70,42 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock and throttle reasons, each stamped with the host time
+    it arrived; summary(t0, t1) keeps the samples taken inside the timed window [t0, t1]
+    (or, for a window shorter than the sampling period, the nearest sample on each side)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 10):
         self.gpu = gpu_index
+        self.period = period_ms
         self.proc = None
-        self.lines = []
+        self.samples = []  # (host time, line)
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 5.0  # wait for the first sample, so the window is covered
+            while not self.samples and time.time() < deadline:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.time(), line.strip()))
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc is not None:
+            time.sleep(2 * self.period / 1000.0)  # one more sample past the window
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -106,10 +113,17 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0: float, t1: float):
+        inside = [l for t, l in self.samples if t0 <= t <= t1]
+        mode = "inside"
+        if not inside:
+            before = [l for t, l in self.samples if t < t0][-1:]
+            after = [l for t, l in self.samples if t > t1][:1]
+            inside = before + after
+            mode = "bracketing"
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -124,7 +138,8 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": mode,
+                "period_ms": self.period}
 
 
 def sample_bytes(n_total: int, B: int, k: int, V: int, elem: int) -> int:
@@ -205,6 +220,7 @@ def gb300_arm(args, rank, world, local_rank):
                               d["num_draft"], workspace=ws, stream=stream, **outs)
 
     # ---- timed region: K steps, barrier + synchronize on both sides ----
+    clk = ClockSampler(torch.cuda.current_device()).start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -213,15 +229,17 @@ def gb300_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for a, b in ev:
-                a.record(stream)
-                step()
-                b.record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    wall = t1 - t0
+    clk.stop()
+    clk.window = (t0, t1)
     if dist:
         dist.barrier()
     per = [a.elapsed_time(b) for a, b in ev]
@@ -292,7 +310,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
         cpu = cpu_baseline(d, w, budget_s=args.cpu_seconds)
 
     if rank == 0:
-        clocks = clk.summary()
+        clocks = clk.summary(*clk.window)
         line = {
             "metric": METRIC,
             "value": value,
@@ -319,14 +337,14 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
             "mean_accept_len": acc,
             "roofline": {
                 "bound": "hbm",
-                "kernel": "sample_kernel<BF16>",
+                "kernel": "segment_kernel<SampleOp<BF16>>",
                 "achieved": achieved,
                 "peak": peak,
                 "unit": "GB/s",
                 "frac": achieved / peak,
                 "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "traffic": profiled_traffic("sample_kernel", "b512_k8_v128256_bf16"),
+                "traffic": profiled_traffic("segment_kernel_sample", "b512_k8_v128256_bf16"),
                 "algorithmic_bytes_per_launch": abytes,
                 "launch_ms": mean_ms,
             },
