@@ -184,6 +184,46 @@ def make_flush(device):
     return flush
 
 
+# ------------------------------------------------------------------------------ ranks
+def init_ranks(world: int, device):
+    """The process group of a multi-rank run (None for one rank): NCCL between GPUs, gloo when
+    the ranks run on host cores. It carries only the barriers and the max-over-ranks timing;
+    the data path has no collective."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if device.type == "cuda":
+        dist.init_process_group("nccl", device_id=device)
+    else:
+        dist.init_process_group("gloo")
+    return dist
+
+
+def rank_seed(rank: int) -> int:
+    """Seed of a rank's shard of requests: every rank verifies its own batch."""
+    import synth
+
+    return synth.SEED_BASE + HEAD + 7919 * rank
+
+
+def max_over_ranks(dist, x: float, device) -> float:
+    """The largest value of x over all ranks (x itself for one rank)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: int, steps: int, max_total_ms: float) -> float:
+    """Units of all ranks per second of the slowest rank (weak scaling: each rank does the
+    same work)."""
+    return world * units_per_rank * steps / (max_total_ms * 1e-3)
+
+
 # ------------------------------------------------------------------------------ GPU arm
 def gb300_arm(args, rank, world, local_rank):
     import numpy as np
@@ -194,15 +234,10 @@ def gb300_arm(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
+    dist = init_ranks(world, dev)
 
     w = synth.WORKLOADS[HEAD]
-    d = synth.workload_inputs(w, device=dev, seed=synth.SEED_BASE + HEAD + 7919 * rank,
-                              B=args.requests)
+    d = synth.workload_inputs(w, device=dev, seed=rank_seed(rank), B=args.requests)
     B, k, V = d["B"], d["k"], d["V"]
     n_total = B * k  # every request drafts k tokens in this workload
     elem = w.elem_bytes
@@ -245,10 +280,7 @@ def gb300_arm(args, rank, world, local_rank):
     per = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(per)
     mean_ms = total_ms / len(per)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(dist, total_ms, dev)
     acc = outs["out_accept_len"].float().mean().item()
 
     # ---- end to end through the public call: pinned host inputs in, results out ----
@@ -278,14 +310,10 @@ def gb300_arm(args, rank, world, local_rank):
 
     e2e_steps = max(3, min(args.steps, 10))
     e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
-    e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = t.item()
+    e2e_total = max_over_ranks(dist, sum(e2e_ms), dev)
     del h_t, h_d, d_t, d_d
 
-    e2e = {"value": world * n_total * e2e_steps / (e2e_total * 1e-3), "unit": "positions/s",
+    e2e = {"value": whole_job_rate(world, n_total, e2e_steps, e2e_total), "unit": "positions/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": e2e_total / e2e_steps}
     return finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, acc, clk,
@@ -300,7 +328,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
     peak, peak_kind = measured_peaks()
     abytes = sample_bytes(n_total, B, k, V, elem)
     achieved = abytes / (mean_ms * 1e-3) / 1e9
-    value = world * n_total * args.steps / (total_ms * 1e-3)
+    value = whole_job_rate(world, n_total, args.steps, total_ms)
     rows = {}
     if rank == 0 and not args.no_rows:
         rows = secondary_rows(args, dev, stream, peak)
