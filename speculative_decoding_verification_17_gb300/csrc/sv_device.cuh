@@ -66,6 +66,22 @@ struct F32 {
     return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                  fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
+  // Largest logit of N vectors (NaN ignored), as a balanced tree.
+  template <int N>
+  __device__ static __forceinline__ float max_lane(const uint4 (&v)[N]) {
+    float m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = max_vec(v[i]);
+#pragma unroll
+    for (int q = N / 2; q >= 1; q >>= 1)
+#pragma unroll
+      for (int i = 0; i < q; ++i) m[i] = fmaxf(m[i], m[i + q]);
+    return m[0];
+  }
+  __device__ static __forceinline__ bool has_nan(const uint4& v) {
+    return ((v.x & 0x7fffffffu) > 0x7f800000u) | ((v.y & 0x7fffffffu) > 0x7f800000u) |
+           ((v.z & 0x7fffffffu) > 0x7f800000u) | ((v.w & 0x7fffffffu) > 0x7f800000u);
+  }
 };
 
 struct BF16 {
@@ -104,6 +120,24 @@ struct BF16 {
   __device__ static __forceinline__ float max_vec(const uint4& v) {
     const uint32_t m = max2(max2(v.x, v.y), max2(v.z, v.w));
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+  // Largest logit of N vectors: a balanced tree of packed pair maxima, widened once.
+  template <int N>
+  __device__ static __forceinline__ float max_lane(const uint4 (&v)[N]) {
+    uint32_t m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = max2(max2(v[i].x, v[i].y), max2(v[i].z, v[i].w));
+#pragma unroll
+    for (int q = N / 2; q >= 1; q >>= 1)
+#pragma unroll
+      for (int i = 0; i < q; ++i) m[i] = max2(m[i], m[i + q]);
+    return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xffff0000u));
+  }
+  __device__ static __forceinline__ bool nan2(uint32_t w) {
+    return ((w & 0x7fffu) > 0x7f80u) | (((w >> 16) & 0x7fffu) > 0x7f80u);
+  }
+  __device__ static __forceinline__ bool has_nan(const uint4& v) {
+    return nan2(v.x) | nan2(v.y) | nan2(v.z) | nan2(v.w);
   }
 };
 
@@ -157,6 +191,12 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^d for an integer-valued d <= 0, built from its exponent bits (exact; 0 for d < -126,
+// including d = -inf).
+__device__ __forceinline__ float pow2_nonpos(float d) {
+  return __uint_as_float((uint32_t)((int)fmaxf(d, -127.0f) + 127) << 23);
 }
 
 // Order-preserving map of a non-NaN float onto int32 (for integer max reductions).
@@ -312,31 +352,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 // Bulk copy (TMA, non-tensor) of `bytes` (a multiple of 16) from 16-byte aligned global
-// memory into this CTA's shared memory, completing on `bar`. SV_L2_POLICY picks the L2
-// eviction priority of the copied lines: 0 leaves the copy's default, 1 normal, 2 last.
-#ifndef SV_L2_POLICY
-#define SV_L2_POLICY 0
-#endif
+// memory into this CTA's shared memory, completing on `bar`, with the copy's default L2
+// eviction priority, or with the priority of an L2 cache policy made by l2_policy().
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                         uint64_t* bar) {
-#if SV_L2_POLICY == 0
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-#else
-  uint64_t policy;
-#if SV_L2_POLICY == 1
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(policy));
-#else
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-#endif
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                        uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
       "[%0], [%1], %2, [%3], %4;"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
-#endif
+}
+// An L2 cache policy for every line a copy touches: evicted last (keep) or first.
+__device__ __forceinline__ uint64_t l2_policy(bool keep) {
+  uint64_t p;
+  if (keep)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ uint4 lds16(const void* p) {
   uint4 v;

@@ -6,8 +6,9 @@
 // argmax when it fires and falls through otherwise. The page notes that this single scan of
 // the vocabulary is the whole critical path of the fast answer (section 2.2, Eq. (3)), so
 // the scan is the kernel: every logit is read once from HBM by the bulk copies of
-// sv_stream.cuh, each 4 KiB warp slice is reduced to an (l1, argmax, l2) triple, and the
-// triples of a row are merged by the CTA that completes the row.
+// sv_stream.cuh, each lane keeps a running (l1, argmax, l2) triple over its share of a row
+// segment, each warp reduces its lanes once per segment, and the triples of a row are merged
+// by the CTA that completes the row.
 #include <cmath>
 #include <cstdint>
 
@@ -18,7 +19,7 @@
 
 namespace sv {
 
-constexpr int kPoisonedTop2 = -2;  // marks a chunk whose copy never landed
+constexpr int kPoisonedTop2 = -2;  // marks a share of which a copy never landed
 
 struct GateArgs {
   const void* logits;
@@ -30,7 +31,7 @@ struct GateArgs {
   int32_t* out_token;
   float* out_gap;
   uint8_t* out_fire;
-  WarpTop2* part;  // [N][nch][kWarps]
+  WarpTop2* part;  // [N][nseg][kWarps]
   unsigned int* row_cnt;
 };
 
@@ -85,17 +86,32 @@ struct GateOp {
     g.rid = r;
     g.r = r;
     g.slot = 0;
+    g.seg = seg;
+    g.keep = false;
     g.c0 = seg * kSegChunks;
     g.c1 = min(g.c0 + kSegChunks, A.nch);
     g.nseg = A.nseg;
     return true;
   }
 
-  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
-                                    const uint4 (&v)[kVecPerThread], bool poison) {
+  // One lane's running top-2 over the segment, in increasing logit index.
+  struct Acc {
+    Top2 t;
+    bool poison;
+  };
+
+  __device__ static __forceinline__ void seg_begin(Acc& a) {
+    a.t = Top2{-INFINITY, -INFINITY, kNoIndex};
+    a.poison = false;
+  }
+
+  __device__ static __forceinline__ void warp_chunk(const Args&, const Seg&, int c,
+                                                    const uint4 (&v)[kVecPerThread],
+                                                    bool poison, Acc& acc) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t j0 = (int64_t)c * E::kChunk;
-    Top2 t{-INFINITY, -INFINITY, kNoIndex};
+    acc.poison |= poison;
+    Top2& t = acc.t;
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
       const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
@@ -115,9 +131,14 @@ struct GateOp {
         }
       }
     }
-    t = warp_top2(t);
+  }
+
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool poison = __any_sync(0xffffffffu, acc.poison);
+    const Top2 t = warp_top2(acc.t);
     if (lane == 0) {
-      WarpTop2* p = A.part + ((g.rid * A.nch + c) * kWarps + w);
+      WarpTop2* p = A.part + ((g.rid * A.nseg + g.seg) * kWarps + w);
       *reinterpret_cast<float4*>(p) =
           make_float4(t.m1, __int_as_float(poison ? kPoisonedTop2 : t.i1), t.m2, 0.0f);
     }
@@ -131,7 +152,7 @@ struct GateOp {
     if (!sm.row_last) return;
     __threadfence();
     if (threadIdx.x < 32) {
-      const int np = A.nch * kWarps;
+      const int np = A.nseg * kWarps;
       const WarpTop2* wp = A.part + (int64_t)row * np;
       Top2 b{-INFINITY, -INFINITY, kNoIndex};
       bool poison = false;

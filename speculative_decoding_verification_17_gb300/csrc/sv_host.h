@@ -42,14 +42,23 @@ struct CallCtl {
   unsigned int pad[3];
 };
 
-// Partial results are kept per (row, chunk, warp): warp w of a CTA reduces the w-th 4 KiB
-// slice of a chunk on its own.
+// A CTA handles a row segment of up to kSegChunks consecutive chunks (a build may override
+// the count to try other values).
+#ifndef SV_SEG_CHUNKS
+#define SV_SEG_CHUNKS 8
+#endif
+constexpr int kSegChunks = SV_SEG_CHUNKS;
+
+inline int num_segments(int64_t nch) { return (int)((nch + kSegChunks - 1) / kSegChunks); }
+
+// Partial results are kept per (row, segment, warp): warp w of a CTA reduces the w-th 4 KiB
+// slice of every chunk of its segment on its own.
 constexpr int kWarpsPerChunk = 8;
 
-// Softmax partial of one warp slice: sum of 2^(z*s - K) over the slice, carried as an
-// unevaluated float pair (hi + lo), with the integer-valued reference K = ceil(m*s) of the
-// slice maximum m. K = -inf marks a slice without a finite logit (no mass), K = NaN a
-// poisoned slice (NaN or +inf logits, or a copy that never landed).
+// Softmax partial of one warp's share of a segment: sum of 2^(z*s - K) over it, carried as
+// an unevaluated float pair (hi + lo), with an integer-valued reference K >= m*s for its
+// maximum m. K = -inf marks a share without a finite logit (no mass), K = NaN a poisoned
+// share (NaN or +inf logits, or a copy that never landed).
 struct WarpSoftmax {
   float K;
   float hi;
@@ -68,14 +77,14 @@ struct RowSoftmax {
 };
 
 struct WarpArgmax {
-  float v;  // largest logit of the slice
-  int idx;  // its lowest index; kNoIndex when the slice holds no comparable logit, -2 poisoned
+  float v;  // largest logit of the warp's share
+  int idx;  // its lowest index; kNoIndex when the share holds no comparable logit, -2 poisoned
 };
 
 struct WarpTop2 {
   float m1;  // largest logit
   int i1;    // lowest index holding it (kNoIndex if none, -2 poisoned)
-  float m2;  // largest logit of the slice with one copy of m1 removed
+  float m2;  // largest logit of the share with one copy of m1 removed
   int pad;
 };
 
@@ -86,9 +95,10 @@ struct SampleLayout {
 inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = 2 * static_cast<size_t>(k) + 1;
   const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  const size_t nseg = static_cast<size_t>(num_segments(num_chunks(V, d)));
   SampleLayout L{};
   size_t o = 0;
-  L.part = o;    o = round_up(o + B * R * nch * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
+  L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
   L.resid = o;   o = round_up(o + B * nch * kWarpsPerChunk * sizeof(double), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
@@ -103,10 +113,10 @@ struct GreedyLayout {
 };
 inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = static_cast<size_t>(k) + 1;
-  const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  const size_t nseg = static_cast<size_t>(num_segments(num_chunks(V, d)));
   GreedyLayout L{};
   size_t o = 0;
-  L.part = o;    o = round_up(o + B * R * nch * kWarpsPerChunk * sizeof(WarpArgmax), 256);
+  L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpArgmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
@@ -119,10 +129,10 @@ struct GateLayout {
   size_t part, ctl, row_cnt, total;
 };
 inline GateLayout gate_layout(int N, int V, sv_dtype d) {
-  const size_t nch = static_cast<size_t>(num_chunks(V, d));
+  const size_t nseg = static_cast<size_t>(num_segments(num_chunks(V, d)));
   GateLayout L{};
   size_t o = 0;
-  L.part = o;    o = round_up(o + static_cast<size_t>(N) * nch * kWarpsPerChunk * sizeof(WarpTop2), 256);
+  L.part = o;    o = round_up(o + static_cast<size_t>(N) * nseg * kWarpsPerChunk * sizeof(WarpTop2), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
   L.total = o;

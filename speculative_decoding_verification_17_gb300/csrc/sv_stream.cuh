@@ -2,18 +2,19 @@
 //
 // A row of V logits is cut into chunks of kChunkBytes (32 KiB). The unit of work of one
 // CTA (kThreads threads, kCtasPerSm CTAs per SM) is a row segment of up to kSegChunks
-// consecutive chunks. Warp w always owns the contiguous 4 KiB slice w of a chunk, so a
-// chunk is reduced by eight independent warps and each warp stores its own partial; pass 1
-// has no CTA-wide barrier at all.
+// consecutive chunks. Warp w always owns the contiguous 4 KiB slice w of a chunk. Each lane
+// folds its share of every chunk of the segment into a running accumulator of its own, and
+// the warp reduces the lanes once, at the end of the segment, into one partial per (row,
+// segment, warp); pass 1 has no CTA-wide barrier at all.
 //
 // For a row that starts on a 16-byte boundary the segment's chunks stream through a
 // kStages-deep shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each
 // completing on that stage's mbarrier; the last warp to finish reading a stage (a shared
 // counter) starts the copy of the chunk kStages ahead into it, so the next chunks land while
-// the current one is reduced. Rows that are not 16-byte aligned are read straight from
-// global memory, logit by logit. Every mbarrier wait is bounded: a copy that never lands
-// poisons its row (the request gets the error sentinel) and sets a bit in the call's
-// control word.
+// the current one is reduced. For rows that are not 16-byte aligned the CTA stages each
+// chunk into the ring with plain loads, logit by logit. Every mbarrier wait is bounded: a
+// copy that never lands poisons its row (the request gets the error sentinel) and sets a bit
+// in the call's control word.
 //
 // After the segment, thread 0 publishes the segment (one acquire-release atomic on the row's
 // counter, after a CTA barrier); the CTA that completes a row merges its partials, and the
@@ -21,10 +22,15 @@
 //
 // An operation Op provides:
 //   using E; static constexpr uint32_t kPad; struct Smem; struct Args (with bool aligned);
+//   struct Acc (one lane's running state over the segment);
 //   static bool unit(const Args&, int64_t u, Seg& g);       false: unit not needed
-//   static void warp_chunk(const Args&, const Seg&, int c, const uint4 (&v)[8], bool poison);
+//   static void seg_begin(Acc&);
+//   static void warp_chunk(const Args&, const Seg&, int c, const uint4 (&v)[8], bool poison,
+//                          Acc&);
 //       one warp, chunk c of the row, the warp's 8 vectors v (lane l holds vector
-//       w*256 + it*32 + l of the chunk in v[it]); stores the warp's partial
+//       w*256 + it*32 + l of the chunk in v[it], logits past the row's end set to kPad);
+//       folds them into the lane's accumulator
+//   static void seg_end(const Args&, const Seg&, Acc&);  one warp: reduce and store its partial
 //   static void finish(const Args&, const Seg&, Smem&, Ring&);  all threads, after the segment
 #pragma once
 
@@ -35,18 +41,21 @@
 
 namespace sv {
 
-// Tuning constants (a build may override them to try other values): chunks per CTA, ring
-// depth, and CTAs resident per SM (shared memory: kCtasPerSm * kStages * 32 KiB <= 227 KiB).
-#ifndef SV_SEG_CHUNKS
-#define SV_SEG_CHUNKS 8
-#endif
+// Tuning constants (a build may override them to try other values): ring depth, and CTAs
+// resident per SM (shared memory: kCtasPerSm * kStages * 32 KiB <= 227 KiB). The chunks per
+// segment, kSegChunks, are set in sv_host.h, since the workspace layouts depend on them.
 #ifndef SV_STAGES
 #define SV_STAGES 2
 #endif
 #ifndef SV_CTAS_PER_SM
 #define SV_CTAS_PER_SM 3
 #endif
-constexpr int kSegChunks = SV_SEG_CHUNKS;
+// L2 priority of the pass-1 copies: with SV_L2_KEEP_POS = p > 0 the rows an operation marks
+// as likely to be read again (Seg::keep) are copied with evict_last and all others with
+// evict_first; with 0 every copy keeps its default priority.
+#ifndef SV_L2_KEEP_POS
+#define SV_L2_KEEP_POS 0
+#endif
 constexpr int kStages = SV_STAGES;
 constexpr int kCtasPerSm = SV_CTAS_PER_SM;
 constexpr int kRingBytes = kStages * kChunkBytes;
@@ -59,7 +68,9 @@ struct Seg {
   int r;        // request (or gate row)
   int slot;     // row slot inside the request
   int c0, c1;
+  int seg;      // index of this segment in the row
   int nseg;     // segments of this row
+  bool keep;    // likely to be read again soon (a hint for the L2)
 };
 
 // The CTA's shared-memory ring as the finishing code may reuse it once pass 1 is done:
@@ -96,7 +107,11 @@ __device__ __forceinline__ void issue_chunk(const Seg& g, int c, int V, unsigned
   // the warps' shared-memory reads of this stage come before the async copy that overwrites it
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_arrive_expect_tx(bar, bytes);
-  bulk_g2s(dst, static_cast<const char*>(g.row) + j0 * (16 / E::kPerVec), bytes, bar);
+  const void* src = static_cast<const char*>(g.row) + j0 * (16 / E::kPerVec);
+  if (SV_L2_KEEP_POS > 0)
+    bulk_g2s(dst, src, bytes, bar, l2_policy(g.keep));
+  else
+    bulk_g2s(dst, src, bytes, bar);
 }
 
 template <class Op>
@@ -114,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int V = A.V;
 
+  typename Op::Acc acc;
+  Op::seg_begin(acc);
   if (A.aligned) {
     if (threadIdx.x == 0) {
       for (int s = 0; s < kStages; ++s) {
@@ -135,11 +152,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
       const unsigned char* buf = ring + s * kChunkBytes;
       uint4 v[kVecPerThread];
+      if (j1 - j0 == E::kChunk) {  // a whole chunk (CTA-uniform): no per-vector bound
 #pragma unroll
-      for (int it = 0; it < kVecPerThread; ++it) {
-        const int slot = warp_vec_slot(warp, it, lane);
-        v[it] = (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(buf + slot * 16)
-                                                        : E::pad_vec(Op::kPad);
+        for (int it = 0; it < kVecPerThread; ++it)
+          v[it] = lds16(buf + warp_vec_slot(warp, it, lane) * 16);
+      } else {
+#pragma unroll
+        for (int it = 0; it < kVecPerThread; ++it) {
+          const int slot = warp_vec_slot(warp, it, lane);
+          v[it] = (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(buf + slot * 16)
+                                                          : E::pad_vec(Op::kPad);
+        }
       }
       __syncwarp();
       if (lane == 0) {  // the last warp out of a stage refills it with the chunk kStages ahead
@@ -149,21 +172,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             issue_chunk<E>(g, g.c0 + ci + kStages, V, ring + s * kChunkBytes, &full[s]);
         }
       }
-      Op::warp_chunk(A, g, c, v, poison);
+      Op::warp_chunk(A, g, c, v, poison, acc);
     }
   } else {
+    // rows off the 16-byte grid: the CTA stages each chunk into the ring with plain loads
+    // (logit by logit, coalesced), then every warp reads its vectors as above
     for (int ci = 0; ci < nc; ++ci) {
       const int c = g.c0 + ci;
       const int64_t j0 = (int64_t)c * E::kChunk;
       const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
+      __syncthreads();  // the previous chunk has been read
+#pragma unroll 1
+      for (int i = threadIdx.x; i < kChunkBytes / 16; i += kThreads) {
+        const uint4 w = load_vec<E>(g.row, j0 + (int64_t)i * E::kPerVec, j1, false, Op::kPad);
+        *reinterpret_cast<uint4*>(ring + i * 16) = w;
+      }
+      __syncthreads();
       uint4 v[kVecPerThread];
 #pragma unroll
       for (int it = 0; it < kVecPerThread; ++it)
-        v[it] = load_vec<E>(g.row, j0 + (int64_t)warp_vec_slot(warp, it, lane) * E::kPerVec,
-                            j1, false, Op::kPad);
-      Op::warp_chunk(A, g, c, v, false);
+        v[it] = lds16(ring + warp_vec_slot(warp, it, lane) * 16);
+      Op::warp_chunk(A, g, c, v, false, acc);
     }
   }
+  Op::seg_end(A, g, acc);
   __syncthreads();  // every warp partial of the segment is stored
   Ring ring_state;
   ring_state.buf = ring;
@@ -193,7 +225,5 @@ sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* 
   segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
   return launch_status();
 }
-
-inline int num_segments(int64_t nch) { return (int)((nch + kSegChunks - 1) / kSegChunks); }
 
 }  // namespace sv

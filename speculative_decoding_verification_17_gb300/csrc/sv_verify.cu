@@ -11,23 +11,24 @@
 // pick).
 //
 // One kernel launch per call (after a small memset of the call's counters). Unit = (request
-// r, row slot, segment of up to four 32 KiB chunks), one CTA each (sv_stream.cuh); a request
-// has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows 0..k-1) and k+1
-// in the greedy verify. Units of rows a request does not need (past its n_r) exit at once.
+// r, row slot, segment of up to kSegChunks 32 KiB chunks), one CTA each (sv_stream.cuh); a
+// request has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows
+// 0..k-1) and k+1 in the greedy verify. Units of rows a request does not need (past its n_r)
+// exit at once.
 //
-//  pass 1 (every warp slice of 4 KiB)  the slice maximum m, the integer-valued reference
-//                           K = ceil(m*s) with s = log2(e)/T in fp32, and the sum of
-//                           2^(z*s - K) in fp32 (compensated across the warp); in the greedy
-//                           verify the slice argmax.
-//  row finish (the CTA that completes the row)  K_row = max K; S = sum of slice sums times
+//  pass 1 (each lane, over its share of the segment)  per chunk the lane maximum m, the
+//                           integer-valued reference K = ceil(m*s) with s = log2(e)/T in
+//                           fp32 and the sum of 2^(z*s - K) in fp32, folded into a running
+//                           compensated pair; per segment one warp reduction to a partial
+//                           (K, hi, lo); in the greedy verify the running argmax.
+//  row finish (the CTA that completes the row)  K_row = max K; S = sum of partial sums times
 //                           2^(K - K_row), exact powers of two, in double; p(x) =
 //                           2^(z_x*s - K_row) / S in double.
 //  request finish (the CTA that completes the request)  ratios p_i(x_i)/q_i(x_i) in double
 //                           against the uniforms, the accepted prefix a, then one draw: the
-//                           residual max(0, p_a - q_a) (one extra pass over the rejected row
-//                           pair, which L2 still holds, for per-chunk residual masses, then one
-//                           chunk scanned in vocabulary order), or the bonus from p_n (chunk
-//                           masses from the pass-1 partials, one chunk scanned).
+//                           residual max(0, p_a - q_a) or the bonus p_n, each as one pass
+//                           over its row (pair) for per-chunk masses, then one chunk scanned
+//                           in vocabulary order.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -219,9 +220,9 @@ struct SampleArgs {
   float* out_p;
   float* out_q;
   float* out_resid;
-  WarpSoftmax* part;  // [B * (2k+1)][nch][kWarps]
+  WarpSoftmax* part;  // [B * (2k+1)][nseg][kWarps]
   RowSoftmax* row;
-  double* resid;      // [B][nch][kWarps] residual partial masses
+  double* resid;      // [B][nch][kWarps] per-warp chunk masses of the request's draw
   unsigned int* row_cnt;
   unsigned int* req_cnt;
 };
@@ -241,8 +242,14 @@ struct ResidW {
   }
 };
 
+// The weights of a draw: over a row pair, the residual (kRows = 2), or over one row, the
+// bonus 2^(z*s + c) with c = -K of the row (kRows = 1). Each gives its rows, the load of one
+// 16-byte vector of every row from global memory (load, zero weight past j1) or from shared
+// memory holding the rows `stride` bytes apart (lds), the padding, and the weights of a
+// loaded vector.
 template <typename E>
 struct ResidScan {
+  static constexpr int kRows = 2;
   const void* rp;
   const void* rq;
   int64_t j1;
@@ -251,9 +258,16 @@ struct ResidScan {
   struct Raw {
     uint4 p, q;
   };
+  __device__ __forceinline__ const void* row(int i) const { return i == 0 ? rp : rq; }
   __device__ __forceinline__ Raw load(int64_t j) const {
     return {load_vec<E>(rp, j, j1, aligned, E::kNegInfBits),
             load_vec<E>(rq, j, j1, aligned, E::kNegInfBits)};
+  }
+  __device__ __forceinline__ Raw lds(const unsigned char* base, int stride, int vec) const {
+    return {lds16(base + vec * 16), lds16(base + stride + vec * 16)};
+  }
+  __device__ __forceinline__ Raw pad() const {
+    return {E::pad_vec(E::kNegInfBits), E::pad_vec(E::kNegInfBits)};
   }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
 #pragma unroll
@@ -263,70 +277,151 @@ struct ResidScan {
 
 template <typename E>
 struct BonusScan {
-  const void* row;
+  static constexpr int kRows = 1;
+  const void* rp;
   int64_t j1;
   bool aligned;
-  float s, c;  // weight 2^(z*s + c), c = -K of the row
-  using Raw = uint4;
-  __device__ __forceinline__ Raw load(int64_t j) const {
-    return load_vec<E>(row, j, j1, aligned, E::kNegInfBits);
-  }
-  __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
-#pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, c));
-  }
-};
-
-// The same weights read from a chunk staged in shared memory (vector i of the chunk at
-// p + 16*i, likewise q), for the in-chunk scan after a bulk copy of the chosen chunk.
-template <typename E>
-struct ResidScanSmem {
-  const unsigned char* p;
-  const unsigned char* q;
-  int64_t j0, j1;
-  ResidW wf;
-  struct Raw {
-    uint4 p, q;
-  };
-  __device__ __forceinline__ Raw load(int64_t j) const {
-    if (j >= j1) return {E::pad_vec(E::kNegInfBits), E::pad_vec(E::kNegInfBits)};
-    const int i = (int)((j - j0) / E::kPerVec);
-    return {lds16(p + i * 16), lds16(q + i * 16)};
-  }
-  __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
-#pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) w[l] = wf(E::get(r.p, l), E::get(r.q, l));
-  }
-};
-
-template <typename E>
-struct BonusScanSmem {
-  const unsigned char* p;
-  int64_t j0, j1;
   float s, c;
   using Raw = uint4;
+  __device__ __forceinline__ const void* row(int) const { return rp; }
   __device__ __forceinline__ Raw load(int64_t j) const {
-    if (j >= j1) return E::pad_vec(E::kNegInfBits);
-    return lds16(p + (int)((j - j0) / E::kPerVec) * 16);
+    return load_vec<E>(rp, j, j1, aligned, E::kNegInfBits);
   }
+  __device__ __forceinline__ Raw lds(const unsigned char* base, int, int vec) const {
+    return lds16(base + vec * 16);
+  }
+  __device__ __forceinline__ Raw pad() const { return E::pad_vec(E::kNegInfBits); }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
 #pragma unroll
     for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, c));
   }
 };
 
-// Stage chunk [j0, j1) of a row into ring stage `st` with one bulk copy (thread 0), then wait
-// for it (every thread). False if the copy never landed.
-template <typename E>
-__device__ bool stage_chunk(Ring& ring, int st, const void* row, int64_t j0, int64_t j1) {
-  if (threadIdx.x == 0) {
-    const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(&ring.full[st], bytes);
-    bulk_g2s(ring.buf + st * kChunkBytes, static_cast<const char*>(row) + j0 * (16 / E::kPerVec),
-             bytes, &ring.full[st]);
+// The chunk [j0, j1) of the rows of VW staged in the ring, row i in stage i, read back for
+// the in-chunk scan with the same weights.
+template <typename E, class VW>
+struct StagedScan {
+  const VW* vw;
+  const unsigned char* buf;
+  int64_t j0, j1;
+  using Raw = typename VW::Raw;
+  __device__ __forceinline__ Raw load(int64_t j) const {
+    if (j >= j1) return vw->pad();
+    return vw->lds(buf, kChunkBytes, (int)((j - j0) / E::kPerVec));
   }
-  return ring_wait(ring, st);
+  __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
+    vw->weights(r, w);
+  }
+};
+
+// Per-warp masses of every chunk of the rows of VW, into part[c][warp]; false if a copy
+// never landed (the masses are then NaN). With the TMA ring (aligned rows) the rows stream
+// through the two stages half a chunk at a time: a stage holds the same 16 KiB of every row,
+// one bulk copy each, completing on the stage barrier, and the last warp out of a stage
+// starts the copy of the half kStages ahead. Without it, every thread loads its vectors from
+// global memory. Every thread calls this.
+template <typename E, class VW>
+__device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& ring) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!ring.usable || !SV_RESID_RING) {
+    for (int c = 0; c < nch; ++c) {
+      const int64_t j0 = (int64_t)c * E::kChunk;
+      VW q = vw;
+      q.j1 = chunk_end<E>(j0, V);
+      float acc = 0.0f;
+#pragma unroll
+      for (int h = 0; h < kVecPerThread; h += 2) {
+        typename VW::Raw raw[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          raw[t] = q.load(j0 + (int64_t)((h + t) * kThreads + tid) * E::kPerVec);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float w[E::kPerVec];
+          q.weights(raw[t], w);
+#pragma unroll
+          for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
+        }
+      }
+      float hi = acc, lo = 0.0f;
+      warp_sum_compensated(hi, lo);
+      if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
+    }
+    return true;
+  }
+  constexpr int kHalf = E::kChunk / 2;         // logits per half chunk
+  constexpr int kHalfBytes = kChunkBytes / 2;  // 16 KiB
+  constexpr int kHalfVecPerLane = kVecPerThread / 2;
+  const int nh = 2 * nch;
+  auto issue = [&](int h) {
+    const int st = h % kStages;
+    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
+    const int64_t e = b + kHalf < V ? b + kHalf : (int64_t)V;
+    const uint32_t bytes = e > b ? (uint32_t)((e - b) * (16 / E::kPerVec)) : 0u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (bytes == 0) {
+      mbar_arrive(&ring.full[st]);
+      return;
+    }
+    mbar_arrive_expect_tx(&ring.full[st], VW::kRows * bytes);
+#pragma unroll
+    for (int i = 0; i < VW::kRows; ++i) {
+      void* dst = ring.buf + st * kChunkBytes + i * kHalfBytes;
+      const void* src = static_cast<const char*>(vw.row(i)) + b * (16 / E::kPerVec);
+      if (SV_L2_KEEP_POS > 0)
+        bulk_g2s(dst, src, bytes, &ring.full[st], l2_policy(false));  // the rows' last read
+      else
+        bulk_g2s(dst, src, bytes, &ring.full[st]);
+    }
+  };
+  if (tid == 0)
+    for (int h = 0; h < kStages && h < nh; ++h) issue(h);
+  // every thread follows the same barrier phases
+  float acc = 0.0f;
+  bool timed_out = false;
+  for (int h = 0; h < nh; ++h) {
+    const int st = h % kStages;
+    if (!ring_wait(ring, st)) timed_out = true;
+    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
+    const int64_t e = b + kHalf < V ? b + kHalf : (int64_t)V;
+    const unsigned char* buf = ring.buf + st * kChunkBytes;
+    typename VW::Raw raw[kHalfVecPerLane];
+#pragma unroll
+    for (int it = 0; it < kHalfVecPerLane; ++it) {
+      const int slot = warp * (kHalfVecPerLane * 32) + it * 32 + lane;
+      if (b + (int64_t)slot * E::kPerVec < e)
+        raw[it] = vw.lds(buf, kHalfBytes, slot);
+      else
+        raw[it] = vw.pad();
+    }
+    __syncwarp();
+    if (lane == 0 && atomic_add_acq_rel_cta(&ring.released[st], 1) == kWarps - 1) {
+      ring.released[st] = 0;
+      if (h + kStages < nh) issue(h + kStages);
+    }
+#pragma unroll
+    for (int it = 0; it < kHalfVecPerLane; ++it) {
+      float w[E::kPerVec];
+      vw.weights(raw[it], w);
+#pragma unroll
+      for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
+    }
+    if (h & 1) {  // both halves of chunk h/2 are in
+      float hi = acc, lo = 0.0f;
+      warp_sum_compensated(hi, lo);
+      if (lane == 0) part[(int64_t)(h >> 1) * kWarps + warp] = (double)hi + (double)lo;
+      acc = 0.0f;
+    }
+  }
+  if (__any_sync(0xffffffffu, timed_out)) {
+    if (lane == 0) {
+      atomicOr(&ring.ctl->error, 1u);
+      for (int c = 0; c < nch; ++c)
+        part[(int64_t)c * kWarps + warp] = __longlong_as_double(0x7ff8000000000000ll);
+    }
+    return false;
+  }
+  return true;
 }
 
 __device__ __forceinline__ WarpSoftmax ld_part(const WarpSoftmax* p) {
@@ -343,11 +438,13 @@ __device__ __forceinline__ RowSoftmax ld_row(const RowSoftmax* p) {
   return r;
 }
 
-// Mass of a warp slice in units of 2^K (K the row reference): exact power-of-two scaling.
+// Mass of a warp partial in units of 2^K (K the row reference): exact power-of-two scaling.
 __device__ __forceinline__ double part_mass(const WarpSoftmax& w, float K) {
   if (!(w.K > -INFINITY)) return w.K == -INFINITY ? 0.0 : w.hi;  // empty, or NaN (poisoned)
   return ((double)w.hi + (double)w.lo) * pow2i((int)(w.K - K));
 }
+
+enum DrawStatus { kDrawOk = 0, kDrawNoMass = 1, kDrawFailed = 2 };
 
 template <typename ET>
 struct SampleOp {
@@ -355,11 +452,17 @@ struct SampleOp {
   using E = ET;
   static constexpr uint32_t kPad = E::kNegInfBits;
   struct Smem {
-    float red[2 * kWarps];
     int row_last, req_last;
     int a, err, chunk, take_last;
     double W, before;
     ScanSmem scan;
+  };
+  // One lane's running softmax sum over the segment: hi + lo (an unevaluated pair) in units
+  // of 2^K, K an integer with K >= s * (the largest logit seen), and whether it saw a NaN,
+  // +inf or a copy that never landed.
+  struct Acc {
+    float K, hi, lo;
+    bool bad;
   };
 
   __device__ static __forceinline__ int n_of(const Args& A, int r, bool& ok) {
@@ -384,37 +487,33 @@ struct SampleOp {
     g.rid = (int64_t)r * R + slot;
     g.r = r;
     g.slot = slot;
+    g.seg = seg;
+    g.keep = i < SV_L2_KEEP_POS;  // the early positions hold most rejections
     g.c0 = seg * kSegChunks;
     g.c1 = min(g.c0 + kSegChunks, A.nch);
     g.nseg = A.nseg;
     return true;
   }
 
-  // Pass 1 for one warp slice: its maximum m, the integer reference K = ceil(m*s) and the
-  // sum of 2^(z*s - K) (pairwise in fp32 per lane, compensated across the warp).
-  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
-                                    const uint4 (&v)[kVecPerThread], bool poison) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) tmax = fmaxf(tmax, E::max_vec(v[it]));
-    const float m = warp_max_f(tmax);
-    WarpSoftmax out;
-    if (poison || !(m > -INFINITY && m < INFINITY)) {
-      // no finite logit: a masked slice carries no mass; NaN or +inf poison the row
-      bool nan = false;
-#pragma unroll
-      for (int it = 0; it < kVecPerThread; ++it)
-#pragma unroll
-        for (int l = 0; l < E::kPerVec; ++l) nan |= E::get(v[it], l) != E::get(v[it], l);
-      nan = __any_sync(0xffffffffu, nan);
-      const float bad = __int_as_float(0x7fc00000);
-      out = (poison || nan || m == INFINITY) ? WarpSoftmax{bad, bad, 0.0f, 0.0f}
-                                             : WarpSoftmax{-INFINITY, 0.0f, 0.0f, 0.0f};
-    } else {
+  __device__ static __forceinline__ void seg_begin(Acc& a) {
+    a.K = -INFINITY;
+    a.hi = 0.0f;
+    a.lo = 0.0f;
+    a.bad = false;
+  }
+
+  // Pass 1, one chunk: the lane's maximum m over its 8 vectors, the integer reference
+  // K = ceil(m*s), the sum of 2^(z*s - K) (logits two at a time: packed fp32x2 FMA and adds,
+  // two SFU exp2 per pair, a pairwise tree), then folded into the lane's running pair after
+  // rescaling the side with the smaller reference by an exact power of two.
+  __device__ static __forceinline__ void warp_chunk(const Args& A, const Seg&, int,
+                                                    const uint4 (&v)[kVecPerThread],
+                                                    bool poison, Acc& acc) {
+    const float m = E::max_lane(v);
+    acc.bad |= poison;
+    if (m > -INFINITY && m < INFINITY) {
       const float s = A.s;
       const float K = ceilf(m * s);
-      // logits two at a time: packed fp32x2 FMA and adds, two SFU exp2 per pair
       const float2 s2 = make_float2(s, s), c2 = make_float2(-K, -K);
       float2 part[kVecPerThread];
 #pragma unroll
@@ -435,21 +534,53 @@ struct SampleOp {
       for (int q = kVecPerThread / 2; q >= 1; q >>= 1)
 #pragma unroll
         for (int l = 0; l < q; ++l) part[l] = __fadd2_rn(part[l], part[l + q]);
-      float hi = part[0].x + part[0].y, lo = 0.0f;
+      const float Kn = fmaxf(K, acc.K);
+      const float sa = pow2_nonpos(acc.K - Kn);
+      const float sum = (part[0].x + part[0].y) * pow2_nonpos(K - Kn);
+      float hi, e;
+      two_sum(acc.hi * sa, sum, hi, e);
+      acc.lo = fmaf(acc.lo, sa, e);
+      acc.hi = hi;
+      acc.K = Kn;
+    } else if (m == -INFINITY) {
+      // no finite logit here: masked entries carry no mass, a NaN poisons the row
+      bool nan = false;
+#pragma unroll
+      for (int it = 0; it < kVecPerThread; ++it) nan |= E::has_nan(v[it]);
+      acc.bad |= nan;
+    } else {
+      acc.bad = true;  // +inf, or nothing but NaN
+    }
+  }
+
+  // End of the segment: the warp's reference K = the largest lane reference, every lane's
+  // pair scaled to it (exact), and the compensated warp sum; lane 0 stores the partial.
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool bad = __any_sync(0xffffffffu, acc.bad);
+    const float K = warp_max_f(acc.K);
+    float4 out;
+    if (bad) {
+      const float nan = __int_as_float(0x7fc00000);
+      out = make_float4(nan, nan, 0.0f, 0.0f);
+    } else if (!(K > -INFINITY)) {
+      out = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+    } else {
+      const float sc = pow2_nonpos(acc.K - K);
+      float hi = acc.hi * sc, lo = acc.lo * sc;
       warp_sum_compensated(hi, lo);
-      out = WarpSoftmax{K, hi, lo, 0.0f};
+      out = make_float4(K, hi, lo, 0.0f);
     }
-    if (lane == 0) {
-      float4* p = reinterpret_cast<float4*>(A.part + ((g.rid * A.nch + c) * kWarps + w));
-      *p = make_float4(out.K, out.hi, out.lo, 0.0f);
-    }
+    if (lane == 0)
+      *reinterpret_cast<float4*>(A.part + ((g.rid * A.nseg + g.seg) * kWarps + w)) = out;
   }
 
   __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring& ring);
   __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
                                         Ring& ring);
-  __device__ static void residual_masses(const Args& A, const ResidScan<E>& rs, double* part,
-                                         Smem& sm, Ring& ring);
+  template <class VW>
+  __device__ static int draw(const Args& A, const VW& vw, double* part, float u, Smem& sm,
+                             Ring& ring, int& t, double& W);
 };
 
 template <typename ET>
@@ -467,7 +598,7 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   // ---- row finish: merge the warp partials of the row (warp 0) ----
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    const int np = A.nch * kWarps;
+    const int np = A.nseg * kWarps;
     const WarpSoftmax* wp = A.part + g.rid * np;
     float K = -INFINITY;
     bool poison = false;
@@ -508,109 +639,82 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   finish_request(A, r, n, n_ok, sm, ring);
 }
 
-// Per-warp residual masses of every chunk of the rejected pair (rs), into part[c][warp].
-// With the TMA ring (aligned rows) the pair streams through the two stages half a chunk at a
-// time: a stage holds 16 KiB of the target row and the same 16 KiB of the draft row, two bulk
-// copies completing on the stage barrier, and the last warp out of a stage starts the copy
-// of the half two ahead. Without it, every thread loads its vectors from global memory.
+// One inverse-CDF draw with the weights vw: per-chunk masses, their total W, the chunk in
+// which u*W falls (one warp scans the chunk masses), then that chunk scanned in vocabulary
+// order, from the ring when the rows are aligned (the chunk of row i staged into stage i by
+// one bulk copy each). Every thread calls this. Returns a DrawStatus; t is the drawn token.
 template <typename ET>
-__device__ void SampleOp<ET>::residual_masses(const Args& A, const ResidScan<E>& rs,
-                                              double* part, Smem& sm, Ring& ring) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!ring.usable || !SV_RESID_RING) {
-    for (int c = 0; c < A.nch; ++c) {
-      const int64_t j0 = (int64_t)c * E::kChunk;
-      ResidScan<E> q = rs;
-      q.j1 = chunk_end<E>(j0, A.V);
-      float acc = 0.0f;
+template <class VW>
+__device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, double* part, float u, Smem& sm,
+                                  Ring& ring, int& t, double& W) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool landed = chunk_masses<E>(A.nch, A.V, vw, part, ring);
+  __syncthreads();
+  // chunk masses M_c = sum over warps (fixed order), and W = sum_c M_c (warp 0)
+  if (tid < 32) {
+    double wsum = 0.0;
+    for (int c = lane; c < A.nch; c += 32) {
+      double mc = 0.0;
 #pragma unroll
-      for (int h = 0; h < kVecPerThread; h += 2) {
-        typename ResidScan<E>::Raw raw[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          raw[t] = q.load(j0 + (int64_t)((h + t) * kThreads + tid) * E::kPerVec);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float w[E::kPerVec];
-          q.weights(raw[t], w);
-#pragma unroll
-          for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
-        }
-      }
-      float hi = acc, lo = 0.0f;
-      warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
+      for (int w = 0; w < kWarps; ++w) mc += part[(int64_t)c * kWarps + w];
+      part[(int64_t)c * kWarps] = mc;
+      wsum += mc;
     }
-    return;
+    wsum = warp_sum_d(wsum);
+    if (lane == 0) sm.W = wsum;
   }
-  constexpr int kHalf = E::kChunk / 2;           // logits per half chunk
-  constexpr int kHalfBytes = kChunkBytes / 2;    // 16 KiB
-  constexpr int kHalfVecPerLane = kVecPerThread / 2;
-  const int nh = 2 * A.nch;
-  auto issue = [&](int h) {
-    const int st = h % kStages;
-    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
-    const int64_t e = b + kHalf < A.V ? b + kHalf : (int64_t)A.V;
-    const uint32_t bytes = e > b ? (uint32_t)((e - b) * (16 / E::kPerVec)) : 0u;
+  __syncthreads();
+  W = sm.W;
+  if (!landed || W != W) return kDrawFailed;
+  if (!(W > 0.0)) return kDrawNoMass;
+  const double target = (double)u * W;
+  if (tid < 32) {
+    double before;
+    bool tl;
+    const int c = pick_chunk(
+        A.nch, target, [&](int cc) { return part[(int64_t)cc * kWarps]; }, before, tl);
+    if (lane == 0) {
+      sm.chunk = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
+      sm.before = before;
+      sm.take_last = tl;
+    }
+  }
+  __syncthreads();
+  const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
+  VW q = vw;
+  q.j1 = chunk_end<E>(j0, A.V);
+  if (!ring.usable) {
+    t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, q, sm.scan);
+    return kDrawOk;
+  }
+  // nobody reads the ring any more (the barrier above): stage the chunk of every row
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)((q.j1 - j0) * (16 / E::kPerVec));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (bytes == 0) {
-      mbar_arrive(&ring.full[st]);
-      return;
-    }
-    mbar_arrive_expect_tx(&ring.full[st], 2 * bytes);
-    bulk_g2s(ring.buf + st * kChunkBytes, static_cast<const char*>(rs.rp) + b * (16 / E::kPerVec),
-             bytes, &ring.full[st]);
-    bulk_g2s(ring.buf + st * kChunkBytes + kHalfBytes,
-             static_cast<const char*>(rs.rq) + b * (16 / E::kPerVec), bytes, &ring.full[st]);
-  };
-  if (tid == 0)
-    for (int h = 0; h < kStages && h < nh; ++h) issue(h);
-  // every thread follows the same barrier phases
-  float acc = 0.0f;
-  bool timed_out = false;
-  for (int h = 0; h < nh; ++h) {
-    const int st = h % kStages;
-    if (!ring_wait(ring, st)) timed_out = true;
-    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
-    const int64_t e = b + kHalf < A.V ? b + kHalf : (int64_t)A.V;
-    const unsigned char* buf = ring.buf + st * kChunkBytes;
-    uint4 vp[kHalfVecPerLane], vq[kHalfVecPerLane];
 #pragma unroll
-    for (int it = 0; it < kHalfVecPerLane; ++it) {
-      const int slot = warp * (kHalfVecPerLane * 32) + it * 32 + lane;
-      const bool in = b + (int64_t)slot * E::kPerVec < e;
-      vp[it] = in ? lds16(buf + slot * 16) : E::pad_vec(E::kNegInfBits);
-      vq[it] = in ? lds16(buf + kHalfBytes + slot * 16) : E::pad_vec(E::kNegInfBits);
-    }
-    __syncwarp();
-    if (lane == 0 && atomic_add_acq_rel_cta(&ring.released[st], 1) == kWarps - 1) {
-      ring.released[st] = 0;
-      if (h + kStages < nh) issue(h + kStages);
-    }
-#pragma unroll
-    for (int it = 0; it < kHalfVecPerLane; ++it) {
-      float w[E::kPerVec];
-      rs.weights(typename ResidScan<E>::Raw{vp[it], vq[it]}, w);
-#pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
-    }
-    if (h & 1) {  // both halves of chunk h/2 are in
-      float hi = acc, lo = 0.0f;
-      warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)(h >> 1) * kWarps + warp] = (double)hi + (double)lo;
-      acc = 0.0f;
+    for (int i = 0; i < VW::kRows; ++i) {
+      mbar_arrive_expect_tx(&ring.full[i], bytes);
+      bulk_g2s(ring.buf + i * kChunkBytes,
+               static_cast<const char*>(vw.row(i)) + j0 * (16 / E::kPerVec), bytes,
+               &ring.full[i]);
     }
   }
-  if (__any_sync(0xffffffffu, timed_out) && lane == 0) {
-    atomicOr(&ring.ctl->error, 1u);
-    for (int c = 0; c < A.nch; ++c) part[(int64_t)c * kWarps + warp] = __longlong_as_double(0x7ff8000000000000ll);
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < VW::kRows; ++i) ok &= ring_wait(ring, i);
+  const StagedScan<E, VW> ss{&q, ring.buf, j0, q.j1};
+  t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) atomicOr(&ring.ctl->error, 1u);
+    return kDrawFailed;
   }
+  return kDrawOk;
 }
 
 template <typename ET>
 __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
                                              Ring& ring) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int R = 2 * A.k + 1;
   const int32_t* x = A.tokens + (int64_t)r * A.k;
   const float* u = A.uniforms + (int64_t)r * (A.k + 1);
@@ -649,123 +753,52 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   }
   __syncthreads();
   const int a = sm.a;
-  if (sm.err) {
+  int t = -1;
+  double W = 0.0;
+  int st = kDrawFailed;
+  if (!sm.err) {
+    const float s = A.s;
+    const float uk = __ldg(u + A.k);
+    double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
+    st = kDrawNoMass;
+    if (a < n) {
+      // ---- residual norm(max(0, p_a - q_a)) ----
+      const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
+      const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
+      ResidScan<E> rs;
+      rs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
+      rs.rq = row_ptr<E>(A.draft, (int64_t)r * A.k + a, A.V);
+      rs.j1 = A.V;
+      rs.aligned = A.aligned;
+      rs.wf.s = s;
+      rs.wf.cp = -tp.K;
+      rs.wf.cq = -dq.K;
+      rs.wf.ip = (float)(1.0 / tp.S);
+      rs.wf.iq = (float)(1.0 / dq.S);
+      st = draw(A, rs, part, uk, sm, ring, t, W);
+    }
+    if (st == kDrawNoMass) {
+      // ---- bonus draw from p (row n after full acceptance; row a if the residual vanished
+      //      through rounding), in units of 2^K of that row ----
+      const RowSoftmax rw = ld_row(A.row + (int64_t)r * R + a);
+      BonusScan<E> bs;
+      bs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
+      bs.j1 = A.V;
+      bs.aligned = A.aligned;
+      bs.s = s;
+      bs.c = -rw.K;
+      double Wb;
+      st = draw(A, bs, part, uk, sm, ring, t, Wb);
+      if (st == kDrawNoMass) st = kDrawFailed;
+    }
+  }
+  if (st != kDrawOk) {  // a data error, or a copy that never landed: the error sentinel
     if (tid <= A.k) A.out_tokens[(int64_t)r * (A.k + 1) + tid] = -1;
     if (tid == 0) {
       A.out_accept_len[r] = -1;
       if (A.out_resid) A.out_resid[r] = __int_as_float(0x7fc00000);
     }
     return;
-  }
-
-  const float s = A.s;
-  int t = -1;
-  double W = 0.0;
-  bool drew = false;
-  if (a < n) {
-    // ---- residual norm(max(0, p_a - q_a)): per-chunk masses, then one chunk ----
-    ResidScan<E> rs;
-    rs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
-    rs.rq = row_ptr<E>(A.draft, (int64_t)r * A.k + a, A.V);
-    rs.aligned = A.aligned;
-    const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
-    const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
-    rs.wf.s = s;
-    rs.wf.cp = -tp.K;
-    rs.wf.cq = -dq.K;
-    rs.wf.ip = (float)(1.0 / tp.S);
-    rs.wf.iq = (float)(1.0 / dq.S);
-    double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
-    residual_masses(A, rs, part, sm, ring);
-    __syncthreads();
-    // chunk masses R_c = sum over warps (fixed order) and W = sum_c R_c (warp 0)
-    if (tid < 32) {
-      double wsum = 0.0;
-      for (int c = lane; c < A.nch; c += 32) {
-        double rc = 0.0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) rc += part[(int64_t)c * kWarps + w];
-        part[(int64_t)c * kWarps] = rc;
-        wsum += rc;
-      }
-      wsum = warp_sum_d(wsum);
-      if (lane == 0) sm.W = wsum;
-    }
-    __syncthreads();
-    W = sm.W;
-    if (W > 0.0) {
-      const double target = (double)__ldg(u + A.k) * W;
-      if (tid < 32) {
-        double before;
-        bool tl;
-        const int c = pick_chunk(
-            A.nch, target, [&](int cc) { return part[(int64_t)cc * kWarps]; }, before, tl);
-        if (lane == 0) {
-          sm.chunk = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
-          sm.before = before;
-          sm.take_last = tl;
-        }
-      }
-      __syncthreads();
-      const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
-      rs.j1 = chunk_end<E>(j0, A.V);
-      if (ring.usable) {
-        // the chosen chunk of both rows into the two stages, then the scan from shared memory
-        __syncthreads();  // nobody still reads the ring
-        const bool ok0 = stage_chunk<E>(ring, 0, rs.rp, j0, rs.j1);
-        const bool ok1 = stage_chunk<E>(ring, 1, rs.rq, j0, rs.j1);
-        ResidScanSmem<E> ss{ring.buf, ring.buf + kChunkBytes, j0, rs.j1, rs.wf};
-        t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
-        if (!__syncthreads_and(ok0 && ok1)) t = -1;
-      } else {
-        t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, rs, sm.scan);
-      }
-      drew = true;
-    }
-  }
-  if (!drew) {
-    // ---- bonus draw from p_row (row n after full acceptance; row a if the residual
-    //      vanished through rounding); everything in units of 2^K of that row ----
-    const int brow = a;
-    const int64_t rid = (int64_t)r * R + brow;
-    const RowSoftmax rsw = ld_row(A.row + rid);
-    const WarpSoftmax* wp = A.part + rid * A.nch * kWarps;
-    const double target = (double)__ldg(u + A.k) * rsw.S;
-    if (tid < 32) {
-      double before;
-      bool tl;
-      const int c = pick_chunk(
-          A.nch, target,
-          [&](int cc) {
-            double mass = 0.0;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) mass += part_mass(ld_part(wp + cc * kWarps + w), rsw.K);
-            return mass;
-          },
-          before, tl);
-      if (lane == 0) {
-        sm.chunk = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
-        sm.before = before;
-        sm.take_last = tl;
-      }
-    }
-    __syncthreads();
-    BonusScan<E> bs;
-    bs.row = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + brow, A.V);
-    bs.aligned = A.aligned;
-    bs.s = s;
-    bs.c = -rsw.K;
-    const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
-    bs.j1 = chunk_end<E>(j0, A.V);
-    if (ring.usable) {
-      __syncthreads();  // nobody still reads the ring
-      const bool ok = stage_chunk<E>(ring, 0, bs.row, j0, bs.j1);
-      BonusScanSmem<E> ss{ring.buf, j0, bs.j1, s, bs.c};
-      t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
-      if (!__syncthreads_and(ok)) t = -1;
-    } else {
-      t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, bs, sm.scan);
-    }
   }
 
   // ---- emit ----
@@ -792,7 +825,7 @@ struct GreedyArgs {
   bool aligned;
   int32_t* out_tokens;
   int32_t* out_accept_len;
-  WarpArgmax* part;  // [B * (k+1)][nch][kWarps]
+  WarpArgmax* part;  // [B * (k+1)][nseg][kWarps]
   int* row;
   unsigned int* row_cnt;
   unsigned int* req_cnt;
@@ -845,18 +878,33 @@ struct GreedyOp {
     g.rid = (int64_t)r * R + i;
     g.r = r;
     g.slot = i;
+    g.seg = seg;
+    g.keep = false;
     g.c0 = seg * kSegChunks;
     g.c1 = min(g.c0 + kSegChunks, A.nch);
     g.nseg = A.nseg;
     return true;
   }
 
-  __device__ static void warp_chunk(const Args& A, const Seg& g, int c,
-                                    const uint4 (&v)[kVecPerThread], bool poison) {
+  // One lane's running argmax over the segment, in increasing logit index.
+  struct Acc {
+    float best;
+    int bidx;
+    bool poison;
+  };
+
+  __device__ static __forceinline__ void seg_begin(Acc& a) {
+    a.best = -INFINITY;
+    a.bidx = kNoIndex;
+    a.poison = false;
+  }
+
+  __device__ static __forceinline__ void warp_chunk(const Args&, const Seg&, int c,
+                                                    const uint4 (&v)[kVecPerThread],
+                                                    bool poison, Acc& acc) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t j0 = (int64_t)c * E::kChunk;
-    float best = -INFINITY;
-    int bidx = kNoIndex;
+    acc.poison |= poison;
 #pragma unroll
     for (int it = 0; it < kVecPerThread; ++it) {
       const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
@@ -864,16 +912,22 @@ struct GreedyOp {
       for (int l = 0; l < E::kPerVec; ++l) {
         const float z = E::get(v[it], l);
         // in increasing j: the first comparable logit, then only strictly larger ones
-        if (z > best || (bidx == kNoIndex && z == z)) {
-          best = z;
-          bidx = jb + l;
+        if (z > acc.best || (acc.bidx == kNoIndex && z == z)) {
+          acc.best = z;
+          acc.bidx = jb + l;
         }
       }
     }
-    warp_argmax(best, bidx);
+  }
+
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool poison = __any_sync(0xffffffffu, acc.poison);
+    warp_argmax(acc.best, acc.bidx);
     if (lane == 0) {
-      WarpArgmax* p = A.part + ((g.rid * A.nch + c) * kWarps + w);
-      *reinterpret_cast<float2*>(p) = make_float2(best, __int_as_float(poison ? kPoisoned : bidx));
+      WarpArgmax* p = A.part + ((g.rid * A.nseg + g.seg) * kWarps + w);
+      *reinterpret_cast<float2*>(p) =
+          make_float2(acc.best, __int_as_float(poison ? kPoisoned : acc.bidx));
     }
   }
 
@@ -889,7 +943,7 @@ struct GreedyOp {
     __threadfence();
 
     if (threadIdx.x < 32) {
-      const int np = A.nch * kWarps;
+      const int np = A.nseg * kWarps;
       const WarpArgmax* wp = A.part + g.rid * np;
       float bv = -INFINITY;
       int bi = kNoIndex;
