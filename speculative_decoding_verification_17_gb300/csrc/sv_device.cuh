@@ -21,7 +21,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---- consumer-group barriers ---------------------------------------------------------------
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void cbar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
 
 // Barrier that also returns whether any consumer thread passed pred != 0.
 __device__ __forceinline__ bool cbar_or(bool pred) {
@@ -172,17 +174,6 @@ __device__ __forceinline__ uint4 load_vec(const void* row, int64_t j, int64_t j1
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// The chunk [j0, j1) of a row in the consumer layout, straight from global memory.
-template <typename E>
-__device__ __forceinline__ void load_chunk(const void* row, int64_t j0, int64_t j1,
-                                           bool aligned, uint32_t pad,
-                                           uint4 (&v)[kVecPerThread]) {
-#pragma unroll
-  for (int it = 0; it < kVecPerThread; ++it)
-    v[it] = load_vec<E>(row, j0 + (int64_t)(it * kThreads + threadIdx.x) * E::kPerVec, j1,
-                        aligned, pad);
 }
 
 // ---- arithmetic ----------------------------------------------------------------------------

@@ -74,8 +74,10 @@ template <typename ET>
 struct GateOp {
   using Args = GateArgs;
   using E = ET;
+  using T = SV_TILE(4, 2, 4);  // a light scan: half-chunk stages, 4 CTAs per SM
   static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is skipped
   struct Smem {
+    float4 wpart[kWarps];  // the warp partials of this segment
     int row_last;
   };
 
@@ -105,16 +107,15 @@ struct GateOp {
     a.poison = false;
   }
 
-  __device__ static __forceinline__ void warp_chunk(const Args&, const Seg&, int c,
-                                                    const uint4 (&v)[kVecPerThread],
+  __device__ static __forceinline__ void warp_slice(const Args&, const Seg&, int64_t j0,
+                                                    const uint4 (&v)[T::kStageVec],
                                                     bool poison, Acc& acc) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t j0 = (int64_t)c * E::kChunk;
     acc.poison |= poison;
     Top2& t = acc.t;
 #pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
+    for (int it = 0; it < T::kStageVec; ++it) {
+      const int jb = (int)(j0 + (int64_t)warp_vec_slot<T::kStageVec>(w, it, lane) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
         const float z = E::get(v[it], l);
@@ -133,31 +134,39 @@ struct GateOp {
     }
   }
 
-  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+  __device__ static __forceinline__ void prologue(const Args&, const Seg&, Smem&) {}
+
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc,
+                                                 Smem& sm) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const bool poison = __any_sync(0xffffffffu, acc.poison);
     const Top2 t = warp_top2(acc.t);
     if (lane == 0) {
-      WarpTop2* p = A.part + ((g.rid * A.nseg + g.seg) * kWarps + w);
-      *reinterpret_cast<float4*>(p) =
+      const float4 out =
           make_float4(t.m1, __int_as_float(poison ? kPoisonedTop2 : t.i1), t.m2, 0.0f);
+      sm.wpart[w] = out;
+      if (g.nseg > 1)
+        *reinterpret_cast<float4*>(A.part + ((g.rid * A.nseg + g.seg) * kWarps + w)) = out;
     }
   }
 
   __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring&) {
     const int row = g.r;
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + row, (unsigned)g.nseg);
+    // a row of one segment is complete here: no counter, and its partials are this CTA's
+    if (threadIdx.x == 0)
+      sm.row_last = g.nseg == 1 || arrive_last(A.row_cnt + row, (unsigned)g.nseg);
     __syncthreads();
     if (!sm.row_last) return;
-    __threadfence();
+    if (g.nseg > 1) __threadfence();
     if (threadIdx.x < 32) {
       const int np = A.nseg * kWarps;
       const WarpTop2* wp = A.part + (int64_t)row * np;
       Top2 b{-INFINITY, -INFINITY, kNoIndex};
       bool poison = false;
       for (int q = lane; q < np; q += 32) {
-        const float4 pv = __ldcg(reinterpret_cast<const float4*>(wp + q));
+        const float4 pv =
+            g.nseg > 1 ? __ldcg(reinterpret_cast<const float4*>(wp + q)) : sm.wpart[q];
         const int pi = __float_as_int(pv.y);
         poison |= pi == kPoisonedTop2;
         if (pi != kPoisonedTop2) b = top2_merge(b, Top2{pv.x, pv.z, pi});

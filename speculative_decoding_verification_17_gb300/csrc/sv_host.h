@@ -132,7 +132,8 @@ inline GateLayout gate_layout(int N, int V, sv_dtype d) {
   const size_t nseg = static_cast<size_t>(num_segments(num_chunks(V, d)));
   GateLayout L{};
   size_t o = 0;
-  L.part = o;    o = round_up(o + static_cast<size_t>(N) * nseg * kWarpsPerChunk * sizeof(WarpTop2), 256);
+  L.part = o;
+  o = round_up(o + static_cast<size_t>(N) * nseg * kWarpsPerChunk * sizeof(WarpTop2), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + static_cast<size_t>(N) * sizeof(unsigned int), 256);
   L.total = o;

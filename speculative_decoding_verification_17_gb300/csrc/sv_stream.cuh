@@ -1,36 +1,41 @@
 // sv_stream.cuh — the driver that feeds logit chunks to a row operation.
 //
 // A row of V logits is cut into chunks of kChunkBytes (32 KiB). The unit of work of one
-// CTA (kThreads threads, kCtasPerSm CTAs per SM) is a row segment of up to kSegChunks
-// consecutive chunks. Warp w always owns the contiguous 4 KiB slice w of a chunk. Each lane
-// folds its share of every chunk of the segment into a running accumulator of its own, and
-// the warp reduces the lanes once, at the end of the segment, into one partial per (row,
-// segment, warp); pass 1 has no CTA-wide barrier at all.
+// CTA (kThreads threads; the operation's Tile sets the CTAs per SM) is a row segment of up
+// to kSegChunks consecutive chunks. Warp w always owns the contiguous eighth w of a ring
+// stage. Each lane folds its share of every stage of the segment into a running accumulator
+// of its own, and the warp reduces the lanes once, at the end of the segment, into one
+// partial per (row, segment, warp); pass 1 has no CTA-wide barrier at all.
 //
-// For a row that starts on a 16-byte boundary the segment's chunks stream through a
-// kStages-deep shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each
-// completing on that stage's mbarrier; the last warp to finish reading a stage (a shared
-// counter) starts the copy of the chunk kStages ahead into it, so the next chunks land while
-// the current one is reduced. For rows that are not 16-byte aligned the CTA stages each
-// chunk into the ring with plain loads, logit by logit. Every mbarrier wait is bounded: a
-// copy that never lands poisons its row (the request gets the error sentinel) and sets a bit
-// in the call's control word.
+// For a row that starts on a 16-byte boundary the segment streams through a kStages-deep
+// shared-memory ring: thread 0 starts one cp.async.bulk (TMA) per stage, each completing on
+// that stage's mbarrier; the last warp to finish reading a stage (a shared counter) starts
+// the copy kStages stages ahead into it, so the next stages land while the current one is
+// reduced. For rows that are not 16-byte aligned the CTA stages each piece into the ring with
+// plain loads, logit by logit. Every mbarrier wait is bounded: a copy that never lands
+// poisons its row (the request gets the error sentinel) and sets a bit in the call's control
+// word.
 //
-// After the segment, thread 0 publishes the segment (one acquire-release atomic on the row's
-// counter, after a CTA barrier); the CTA that completes a row merges its partials, and the
-// one that completes a request finishes the request. No CTA ever waits for another one.
+// After the segment, thread 0 publishes it (one acquire-release atomic on the row's counter,
+// after a CTA barrier; a row of one segment needs none); the CTA that completes a row merges
+// its partials, and the one that completes a request finishes the request. No CTA ever
+// waits for another one.
 //
 // An operation Op provides:
 //   using E; static constexpr uint32_t kPad; struct Smem; struct Args (with bool aligned);
 //   struct Acc (one lane's running state over the segment);
 //   static bool unit(const Args&, int64_t u, Seg& g);       false: unit not needed
 //   static void seg_begin(Acc&);
-//   static void warp_chunk(const Args&, const Seg&, int c, const uint4 (&v)[8], bool poison,
-//                          Acc&);
-//       one warp, chunk c of the row, the warp's 8 vectors v (lane l holds vector
-//       w*256 + it*32 + l of the chunk in v[it], logits past the row's end set to kPad);
-//       folds them into the lane's accumulator
-//   static void seg_end(const Args&, const Seg&, Acc&);  one warp: reduce and store its partial
+//   static void prologue(const Args&, const Seg&, Smem&);  all threads, while the first
+//       stages are in flight (a place to start loads the finish will need)
+//   using T = Tile<...> (the ring's shape);
+//   static void warp_slice(const Args&, const Seg&, int64_t j0,
+//                          const uint4 (&v)[T::kStageVec], bool poison, Acc&);
+//       one warp, the ring stage that starts at logit j0 of the row, the warp's vectors v
+//       (lane l holds vector warp_vec_slot<T::kStageVec>(w, it, l) of the stage in v[it],
+//       logits past the row's end set to kPad); folds them into the lane's accumulator
+//   static void seg_end(const Args&, const Seg&, Acc&, Smem&);  one warp: reduce and store
+//       its partial (in shared memory as well, where a row of one segment merges it)
 //   static void finish(const Args&, const Seg&, Smem&, Ring&);  all threads, after the segment
 #pragma once
 
@@ -41,24 +46,37 @@
 
 namespace sv {
 
-// Tuning constants (a build may override them to try other values): ring depth, and CTAs
-// resident per SM (shared memory: kCtasPerSm * kStages * 32 KiB <= 227 KiB). The chunks per
-// segment, kSegChunks, are set in sv_host.h, since the workspace layouts depend on them.
-#ifndef SV_STAGES
-#define SV_STAGES 2
+// The shape of an operation's ring: 16-byte vectors per thread in one stage (a stage holds
+// kThreads * Vec * 16 bytes: 32 KiB at 8, a whole chunk), ring depth, and CTAs resident per
+// SM (shared memory: Ctas * kRingBytes <= 227 KiB; registers: 65536 / (Ctas * kThreads) per
+// thread). Each operation picks its own: exp-heavy passes want long stages, light scans more
+// warps per SM. A build may force one shape on every operation (SV_STAGE_VEC, SV_STAGES and
+// SV_CTAS_PER_SM together) to compare shapes. The chunks per segment, kSegChunks, are set in
+// sv_host.h, since the workspace layouts depend on them.
+template <int Vec, int Stages, int Ctas>
+struct Tile {
+  static constexpr int kStageVec = Vec;
+  static constexpr int kStages = Stages;
+  static constexpr int kCtasPerSm = Ctas;
+  static constexpr int kStageBytes = kThreads * Vec * 16;
+  static constexpr int kRingBytes = Stages * kStageBytes;
+  static_assert(kChunkBytes % kStageBytes == 0, "a chunk is a whole number of stages");
+  static_assert(Stages >= 2 && Stages <= 8, "ring depth");
+  static_assert(kRingBytes >= kChunkBytes, "the finishing passes need a chunk of ring");
+  static_assert(Ctas * (kRingBytes + 2048) <= 232448, "shared memory of Ctas CTAs");
+};
+#if defined(SV_STAGE_VEC) && defined(SV_STAGES) && defined(SV_CTAS_PER_SM)
+#define SV_TILE(vec, stages, ctas) Tile<SV_STAGE_VEC, SV_STAGES, SV_CTAS_PER_SM>
+#else
+#define SV_TILE(vec, stages, ctas) Tile<vec, stages, ctas>
 #endif
-#ifndef SV_CTAS_PER_SM
-#define SV_CTAS_PER_SM 3
-#endif
+
 // L2 priority of the pass-1 copies: with SV_L2_KEEP_POS = p > 0 the rows an operation marks
 // as likely to be read again (Seg::keep) are copied with evict_last and all others with
 // evict_first; with 0 every copy keeps its default priority.
 #ifndef SV_L2_KEEP_POS
-#define SV_L2_KEEP_POS 0
+#define SV_L2_KEEP_POS 2
 #endif
-constexpr int kStages = SV_STAGES;
-constexpr int kCtasPerSm = SV_CTAS_PER_SM;
-constexpr int kRingBytes = kStages * kChunkBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far past any legitimate wait
 
 // A row segment: the row (its first logit), its slot, and its chunks [c0, c1).
@@ -93,16 +111,17 @@ __device__ __forceinline__ bool ring_wait(Ring& R, int s) {
   return ok;
 }
 
-// Index of the 16-byte vector lane `lane` of warp `w` holds in slot `it` of a chunk.
+// Index, within a ring stage of Vec vectors per thread, of the 16-byte vector lane `lane`
+// of warp `w` holds in slot `it`: warp w reads the w-th contiguous eighth of the stage.
+template <int Vec>
 __device__ __forceinline__ int warp_vec_slot(int w, int it, int lane) {
-  return w * (kVecPerThread * 32) + it * 32 + lane;
+  return w * (Vec * 32) + it * 32 + lane;
 }
 
+// Copy logits [j0, j1) of a row into a ring stage, completing on its barrier.
 template <typename E>
-__device__ __forceinline__ void issue_chunk(const Seg& g, int c, int V, unsigned char* dst,
-                                            uint64_t* bar) {
-  const int64_t j0 = (int64_t)c * E::kChunk;
-  const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
+__device__ __forceinline__ void issue_stage(const Seg& g, int64_t j0, int64_t j1,
+                                            unsigned char* dst, uint64_t* bar) {
   const uint32_t bytes = (uint32_t)((j1 - j0) * (16 / E::kPerVec));
   // the warps' shared-memory reads of this stage come before the async copy that overwrites it
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -115,9 +134,13 @@ __device__ __forceinline__ void issue_chunk(const Seg& g, int c, int V, unsigned
 }
 
 template <class Op>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, Op::T::kCtasPerSm)
     segment_kernel(const typename Op::Args A, CallCtl* ctl) {
   using E = typename Op::E;
+  constexpr int kStageVec = Op::T::kStageVec;
+  constexpr int kStages = Op::T::kStages;
+  constexpr int kStageBytes = Op::T::kStageBytes;
+  constexpr int64_t kStageElems = (int64_t)kStageBytes / 16 * E::kPerVec;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ int released[kStages];
@@ -125,9 +148,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   Seg g;
   if (!Op::unit(A, (int64_t)blockIdx.x, g)) return;
-  const int nc = g.c1 - g.c0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int V = A.V;
+  const int64_t jb = (int64_t)g.c0 * E::kChunk;
+  const int64_t je = (int64_t)g.c1 * E::kChunk < A.V ? (int64_t)g.c1 * E::kChunk : (int64_t)A.V;
+  const int ns = (int)((je - jb + kStageElems - 1) / kStageElems);  // stages of the segment
 
   typename Op::Acc acc;
   Op::seg_begin(acc);
@@ -138,64 +162,70 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         released[s] = 0;
       }
       fence_barrier_init();
-      for (int q = 0; q < kStages && q < nc; ++q)
-        issue_chunk<E>(g, g.c0 + q, V, ring + q * kChunkBytes, &full[q]);
+      for (int q = 0; q < kStages && q < ns; ++q) {
+        const int64_t j0 = jb + q * kStageElems;
+        issue_stage<E>(g, j0, j0 + kStageElems < je ? j0 + kStageElems : je,
+                       ring + q * kStageBytes, &full[q]);
+      }
     }
     __syncthreads();
-    for (int ci = 0; ci < nc; ++ci) {
-      const int s = ci % kStages;
-      const bool ok = mbar_wait(&full[s], (uint32_t)((ci / kStages) & 1), kWaitLimitNs);
+    Op::prologue(A, g, sm);
+    for (int si = 0; si < ns; ++si) {
+      const int s = si % kStages;
+      const bool ok = mbar_wait(&full[s], (uint32_t)((si / kStages) & 1), kWaitLimitNs);
       const bool poison = __any_sync(0xffffffffu, !ok);
       if (poison && lane == 0) atomicOr(&ctl->error, 1u);
-      const int c = g.c0 + ci;
-      const int64_t j0 = (int64_t)c * E::kChunk;
-      const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
-      const unsigned char* buf = ring + s * kChunkBytes;
-      uint4 v[kVecPerThread];
-      if (j1 - j0 == E::kChunk) {  // a whole chunk (CTA-uniform): no per-vector bound
+      const int64_t j0 = jb + si * kStageElems;
+      const int64_t j1 = j0 + kStageElems < je ? j0 + kStageElems : je;
+      const unsigned char* buf = ring + s * kStageBytes;
+      uint4 v[kStageVec];
+      if (j1 - j0 == kStageElems) {  // a whole stage (CTA-uniform): no per-vector bound
 #pragma unroll
-        for (int it = 0; it < kVecPerThread; ++it)
-          v[it] = lds16(buf + warp_vec_slot(warp, it, lane) * 16);
+        for (int it = 0; it < kStageVec; ++it)
+          v[it] = lds16(buf + warp_vec_slot<kStageVec>(warp, it, lane) * 16);
       } else {
 #pragma unroll
-        for (int it = 0; it < kVecPerThread; ++it) {
-          const int slot = warp_vec_slot(warp, it, lane);
+        for (int it = 0; it < kStageVec; ++it) {
+          const int slot = warp_vec_slot<kStageVec>(warp, it, lane);
           v[it] = (j0 + (int64_t)slot * E::kPerVec < j1) ? lds16(buf + slot * 16)
                                                           : E::pad_vec(Op::kPad);
         }
       }
       __syncwarp();
-      if (lane == 0) {  // the last warp out of a stage refills it with the chunk kStages ahead
+      if (lane == 0) {  // the last warp out of a stage refills it kStages stages ahead
         if (atomic_add_acq_rel_cta(&released[s], 1) == kWarps - 1) {
           released[s] = 0;
-          if (ci + kStages < nc)
-            issue_chunk<E>(g, g.c0 + ci + kStages, V, ring + s * kChunkBytes, &full[s]);
+          if (si + kStages < ns) {
+            const int64_t n0 = j0 + kStages * kStageElems;
+            issue_stage<E>(g, n0, n0 + kStageElems < je ? n0 + kStageElems : je,
+                           ring + s * kStageBytes, &full[s]);
+          }
         }
       }
-      Op::warp_chunk(A, g, c, v, poison, acc);
+      Op::warp_slice(A, g, j0, v, poison, acc);
     }
   } else {
-    // rows off the 16-byte grid: the CTA stages each chunk into the ring with plain loads
+    // rows off the 16-byte grid: the CTA stages each piece into the ring with plain loads
     // (logit by logit, coalesced), then every warp reads its vectors as above
-    for (int ci = 0; ci < nc; ++ci) {
-      const int c = g.c0 + ci;
-      const int64_t j0 = (int64_t)c * E::kChunk;
-      const int64_t j1 = j0 + E::kChunk < V ? j0 + E::kChunk : (int64_t)V;
-      __syncthreads();  // the previous chunk has been read
+    Op::prologue(A, g, sm);
+    for (int si = 0; si < ns; ++si) {
+      const int64_t j0 = jb + si * kStageElems;
+      const int64_t j1 = j0 + kStageElems < je ? j0 + kStageElems : je;
+      __syncthreads();  // the previous piece has been read
 #pragma unroll 1
-      for (int i = threadIdx.x; i < kChunkBytes / 16; i += kThreads) {
+      for (int i = threadIdx.x; i < kStageBytes / 16; i += kThreads) {
         const uint4 w = load_vec<E>(g.row, j0 + (int64_t)i * E::kPerVec, j1, false, Op::kPad);
         *reinterpret_cast<uint4*>(ring + i * 16) = w;
       }
       __syncthreads();
-      uint4 v[kVecPerThread];
+      uint4 v[kStageVec];
 #pragma unroll
-      for (int it = 0; it < kVecPerThread; ++it)
-        v[it] = lds16(ring + warp_vec_slot(warp, it, lane) * 16);
-      Op::warp_chunk(A, g, c, v, false, acc);
+      for (int it = 0; it < kStageVec; ++it)
+        v[it] = lds16(ring + warp_vec_slot<kStageVec>(warp, it, lane) * 16);
+      Op::warp_slice(A, g, j0, v, false, acc);
     }
   }
-  Op::seg_end(A, g, acc);
+  Op::seg_end(A, g, acc, sm);
   __syncthreads();  // every warp partial of the segment is stored
   Ring ring_state;
   ring_state.buf = ring;
@@ -203,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   ring_state.released = released;
   ring_state.phase = 0;
   if (A.aligned)
-    for (int q = 0; q < kStages; ++q) ring_state.phase |= (uint32_t)(((nc - q + kStages - 1) / kStages) & 1) << q;
+    for (int q = 0; q < kStages; ++q)
+      ring_state.phase |= (uint32_t)(((ns - q + kStages - 1) / kStages) & 1) << q;
   ring_state.ctl = ctl;
   ring_state.usable = A.aligned;
   Op::finish(A, g, sm, ring_state);
@@ -215,7 +246,8 @@ sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* 
                           cudaStream_t st) {
   if (units <= 0) return SV_OK;
   // host-side function attributes (no stream work), set on every call so they hold in any
-  // context: the ring's dynamic shared memory, and the carveout that fits kCtasPerSm CTAs
+  // context: the ring's dynamic shared memory, and the carveout that fits the op's CTAs
+  constexpr int kRingBytes = Op::T::kRingBytes;
   cudaError_t e = cudaFuncSetAttribute(segment_kernel<Op>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -314,13 +314,31 @@ struct StagedScan {
   }
 };
 
+constexpr int pow2_floor(int x) { return x >= 2 ? 2 * pow2_floor(x / 2) : 1; }
+
+// The finishing passes see the ring (RingBytes) as two stages (its halves, on stage barriers
+// 0 and 1). A draw over VW streams pieces of kPieceBytes of every row per stage, and it scans
+// the chosen chunk from the ring when a whole chunk of every row fits (else from global
+// memory).
+template <class VW, int RingBytes>
+struct DrawRing {
+  static constexpr int kRingBytes = RingBytes;
+  static constexpr int kHalf = kRingBytes / 2;
+  static constexpr int kPieceBytes =
+      pow2_floor(kHalf / VW::kRows < kChunkBytes ? kHalf / VW::kRows : kChunkBytes);
+  static constexpr int kPiecesPerChunk = kChunkBytes / kPieceBytes;
+  static constexpr int kVecPerLane = kPieceBytes / 16 / kThreads;
+  static constexpr bool kStagedScan = VW::kRows * kChunkBytes <= kRingBytes;
+  static_assert(kVecPerLane >= 1, "a piece gives every thread at least one vector");
+};
+
 // Per-warp masses of every chunk of the rows of VW, into part[c][warp]; false if a copy
 // never landed (the masses are then NaN). With the TMA ring (aligned rows) the rows stream
-// through the two stages half a chunk at a time: a stage holds the same 16 KiB of every row,
-// one bulk copy each, completing on the stage barrier, and the last warp out of a stage
-// starts the copy of the half kStages ahead. Without it, every thread loads its vectors from
-// global memory. Every thread calls this.
-template <typename E, class VW>
+// through the two halves of the ring a piece at a time: a half holds the same piece of every
+// row, one bulk copy each, completing on its barrier, and the last warp out of a half starts
+// the copy of the piece two ahead. Without it, every thread loads its vectors from global
+// memory. Every thread calls this.
+template <typename E, int RingBytes, class VW>
 __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!ring.usable || !SV_RESID_RING) {
@@ -349,14 +367,19 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& r
     }
     return true;
   }
-  constexpr int kHalf = E::kChunk / 2;         // logits per half chunk
-  constexpr int kHalfBytes = kChunkBytes / 2;  // 16 KiB
-  constexpr int kHalfVecPerLane = kVecPerThread / 2;
-  const int nh = 2 * nch;
+  using DR = DrawRing<VW, RingBytes>;
+  constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
+  constexpr int kPer = DR::kPiecesPerChunk;
+  constexpr int kVec = DR::kVecPerLane;
+  const int np = nch * kPer;
+  auto piece = [&](int h, int64_t& b, int64_t& e) {
+    b = (int64_t)(h / kPer) * E::kChunk + (int64_t)(h % kPer) * kPieceElems;
+    e = b + kPieceElems < V ? b + kPieceElems : (int64_t)V;
+  };
   auto issue = [&](int h) {
-    const int st = h % kStages;
-    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
-    const int64_t e = b + kHalf < V ? b + kHalf : (int64_t)V;
+    const int st = h & 1;
+    int64_t b, e;
+    piece(h, b, e);
     const uint32_t bytes = e > b ? (uint32_t)((e - b) * (16 / E::kPerVec)) : 0u;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (bytes == 0) {
@@ -366,50 +389,50 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& r
     mbar_arrive_expect_tx(&ring.full[st], VW::kRows * bytes);
 #pragma unroll
     for (int i = 0; i < VW::kRows; ++i) {
-      void* dst = ring.buf + st * kChunkBytes + i * kHalfBytes;
+      void* dst = ring.buf + st * DR::kHalf + i * DR::kPieceBytes;
       const void* src = static_cast<const char*>(vw.row(i)) + b * (16 / E::kPerVec);
-      if (SV_L2_KEEP_POS > 0)
+      if (SV_L2_KEEP_POS > 0 && DR::kStagedScan)
         bulk_g2s(dst, src, bytes, &ring.full[st], l2_policy(false));  // the rows' last read
       else
         bulk_g2s(dst, src, bytes, &ring.full[st]);
     }
   };
   if (tid == 0)
-    for (int h = 0; h < kStages && h < nh; ++h) issue(h);
+    for (int h = 0; h < 2 && h < np; ++h) issue(h);
   // every thread follows the same barrier phases
   float acc = 0.0f;
   bool timed_out = false;
-  for (int h = 0; h < nh; ++h) {
-    const int st = h % kStages;
+  for (int h = 0; h < np; ++h) {
+    const int st = h & 1;
     if (!ring_wait(ring, st)) timed_out = true;
-    const int64_t b = (int64_t)(h >> 1) * E::kChunk + (int64_t)(h & 1) * kHalf;
-    const int64_t e = b + kHalf < V ? b + kHalf : (int64_t)V;
-    const unsigned char* buf = ring.buf + st * kChunkBytes;
-    typename VW::Raw raw[kHalfVecPerLane];
+    int64_t b, e;
+    piece(h, b, e);
+    const unsigned char* buf = ring.buf + st * DR::kHalf;
+    typename VW::Raw raw[kVec];
 #pragma unroll
-    for (int it = 0; it < kHalfVecPerLane; ++it) {
-      const int slot = warp * (kHalfVecPerLane * 32) + it * 32 + lane;
+    for (int it = 0; it < kVec; ++it) {
+      const int slot = warp * (kVec * 32) + it * 32 + lane;
       if (b + (int64_t)slot * E::kPerVec < e)
-        raw[it] = vw.lds(buf, kHalfBytes, slot);
+        raw[it] = vw.lds(buf, DR::kPieceBytes, slot);
       else
         raw[it] = vw.pad();
     }
     __syncwarp();
     if (lane == 0 && atomic_add_acq_rel_cta(&ring.released[st], 1) == kWarps - 1) {
       ring.released[st] = 0;
-      if (h + kStages < nh) issue(h + kStages);
+      if (h + 2 < np) issue(h + 2);
     }
 #pragma unroll
-    for (int it = 0; it < kHalfVecPerLane; ++it) {
+    for (int it = 0; it < kVec; ++it) {
       float w[E::kPerVec];
       vw.weights(raw[it], w);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
     }
-    if (h & 1) {  // both halves of chunk h/2 are in
+    if (h % kPer == kPer - 1) {  // every piece of chunk h / kPer is in
       float hi = acc, lo = 0.0f;
       warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)(h >> 1) * kWarps + warp] = (double)hi + (double)lo;
+      if (lane == 0) part[(int64_t)(h / kPer) * kWarps + warp] = (double)hi + (double)lo;
       acc = 0.0f;
     }
   }
@@ -450,8 +473,11 @@ template <typename ET>
 struct SampleOp {
   using Args = SampleArgs;
   using E = ET;
+  using T = SV_TILE(8, 2, 3);  // exp-heavy: whole-chunk stages, 3 CTAs of 80 registers
   static constexpr uint32_t kPad = E::kNegInfBits;
   struct Smem {
+    float4 wpart[kWarps];  // the warp partials of this segment
+    float zx;              // the logit of the row's draft token, when prefetched
     int row_last, req_last;
     int a, err, chunk, take_last;
     double W, before;
@@ -502,22 +528,40 @@ struct SampleOp {
     a.bad = false;
   }
 
-  // Pass 1, one chunk: the lane's maximum m over its 8 vectors, the integer reference
+  // Slot of a row in its request: draft position i (target rows 0..k, draft rows k+1..2k).
+  __device__ static __forceinline__ int position(const Args& A, const Seg& g) {
+    return g.slot <= A.k ? g.slot : g.slot - A.k - 1;
+  }
+
+  // A row of one segment is merged by this CTA: fetch its draft token's logit while the
+  // first stages are in flight.
+  __device__ static __forceinline__ void prologue(const Args& A, const Seg& g, Smem& sm) {
+    if (threadIdx.x != 0 || g.nseg != 1) return;
+    bool ok;
+    const int n = n_of(A, g.r, ok);
+    const int i = position(A, g);
+    if (i >= n) return;
+    const int32_t xi = __ldg(A.tokens + (int64_t)g.r * A.k + i);
+    if (xi >= 0 && xi < A.V) sm.zx = E::load1(g.row, xi);
+  }
+
+  // Pass 1, one ring stage: the lane's maximum m over its vectors, the integer reference
   // K = ceil(m*s), the sum of 2^(z*s - K) (logits two at a time: packed fp32x2 FMA and adds,
   // two SFU exp2 per pair, a pairwise tree), then folded into the lane's running pair after
   // rescaling the side with the smaller reference by an exact power of two.
-  __device__ static __forceinline__ void warp_chunk(const Args& A, const Seg&, int,
-                                                    const uint4 (&v)[kVecPerThread],
+  __device__ static __forceinline__ void warp_slice(const Args& A, const Seg&, int64_t,
+                                                    const uint4 (&v)[T::kStageVec],
                                                     bool poison, Acc& acc) {
+    constexpr int kStageVec = T::kStageVec;
     const float m = E::max_lane(v);
     acc.bad |= poison;
     if (m > -INFINITY && m < INFINITY) {
       const float s = A.s;
       const float K = ceilf(m * s);
       const float2 s2 = make_float2(s, s), c2 = make_float2(-K, -K);
-      float2 part[kVecPerThread];
+      float2 part[kStageVec];
 #pragma unroll
-      for (int it = 0; it < kVecPerThread; ++it) {
+      for (int it = 0; it < kStageVec; ++it) {
         float2 e[E::kPerVec / 2];
 #pragma unroll
         for (int p = 0; p < E::kPerVec / 2; ++p) {
@@ -531,7 +575,7 @@ struct SampleOp {
         part[it] = e[0];
       }
 #pragma unroll
-      for (int q = kVecPerThread / 2; q >= 1; q >>= 1)
+      for (int q = kStageVec / 2; q >= 1; q >>= 1)
 #pragma unroll
         for (int l = 0; l < q; ++l) part[l] = __fadd2_rn(part[l], part[l + q]);
       const float Kn = fmaxf(K, acc.K);
@@ -546,7 +590,7 @@ struct SampleOp {
       // no finite logit here: masked entries carry no mass, a NaN poisons the row
       bool nan = false;
 #pragma unroll
-      for (int it = 0; it < kVecPerThread; ++it) nan |= E::has_nan(v[it]);
+      for (int it = 0; it < kStageVec; ++it) nan |= E::has_nan(v[it]);
       acc.bad |= nan;
     } else {
       acc.bad = true;  // +inf, or nothing but NaN
@@ -555,7 +599,8 @@ struct SampleOp {
 
   // End of the segment: the warp's reference K = the largest lane reference, every lane's
   // pair scaled to it (exact), and the compensated warp sum; lane 0 stores the partial.
-  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc,
+                                                 Smem& sm) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const bool bad = __any_sync(0xffffffffu, acc.bad);
     const float K = warp_max_f(acc.K);
@@ -571,8 +616,11 @@ struct SampleOp {
       warp_sum_compensated(hi, lo);
       out = make_float4(K, hi, lo, 0.0f);
     }
-    if (lane == 0)
-      *reinterpret_cast<float4*>(A.part + ((g.rid * A.nseg + g.seg) * kWarps + w)) = out;
+    if (lane == 0) {
+      sm.wpart[w] = out;
+      if (g.nseg > 1)
+        *reinterpret_cast<float4*>(A.part + ((g.rid * A.nseg + g.seg) * kWarps + w)) = out;
+    }
   }
 
   __device__ static void finish(const Args& A, const Seg& g, Smem& sm, Ring& ring);
@@ -588,22 +636,30 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   const int r = g.r;
   bool n_ok;
   const int n = n_of(A, r, n_ok);
-  const int i = g.slot <= A.k ? g.slot : g.slot - A.k - 1;
+  const int i = position(A, g);
   const float s = A.s;
-  if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
+  // a row of one segment is complete here: no counter, and its partials are this CTA's
+  if (threadIdx.x == 0)
+    sm.row_last = g.nseg == 1 || arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
   __syncthreads();
   if (!sm.row_last) return;
-  __threadfence();
+  if (g.nseg > 1) __threadfence();
 
-  // ---- row finish: merge the warp partials of the row (warp 0) ----
+  // ---- row finish: merge the warp partials of the row (warp 0; from shared memory when
+  //      the row is this one segment) ----
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int np = A.nseg * kWarps;
     const WarpSoftmax* wp = A.part + g.rid * np;
+    auto part_q = [&](int q) {
+      if (g.nseg > 1) return ld_part(wp + q);
+      const float4 v = sm.wpart[q];
+      return WarpSoftmax{v.x, v.y, v.z, v.w};
+    };
     float K = -INFINITY;
     bool poison = false;
     for (int q = lane; q < np; q += 32) {
-      const WarpSoftmax w = ld_part(wp + q);
+      const WarpSoftmax w = part_q(q);
       poison |= (w.K != w.K) || (w.hi != w.hi);
       if (w.K > K) K = w.K;
     }
@@ -611,7 +667,7 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
     K = warp_max_f(K);
     double S = 0.0;
     if (K > -INFINITY)
-      for (int q = lane; q < np; q += 32) S += part_mass(ld_part(wp + q), K);
+      for (int q = lane; q < np; q += 32) S += part_mass(part_q(q), K);
     S = warp_sum_d(S);
     if (lane == 0) {
       int status = (!poison && K > -INFINITY && isfinite(S) && S > 0.0) ? 0 : 1;
@@ -621,7 +677,7 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
         if (xi < 0 || xi >= A.V) {
           status = status ? status : 2;
         } else if (status == 0) {
-          const float zx = E::load1(g.row, xi);
+          const float zx = g.nseg == 1 ? sm.zx : E::load1(g.row, xi);
           px = exp2((double)zx * (double)s - (double)K) / S;
         }
       }
@@ -648,7 +704,7 @@ template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, double* part, float u, Smem& sm,
                                   Ring& ring, int& t, double& W) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const bool landed = chunk_masses<E>(A.nch, A.V, vw, part, ring);
+  const bool landed = chunk_masses<E, T::kRingBytes>(A.nch, A.V, vw, part, ring);
   __syncthreads();
   // chunk masses M_c = sum over warps (fixed order), and W = sum_c M_c (warp 0)
   if (tid < 32) {
@@ -683,7 +739,7 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, double* part, flo
   const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
   VW q = vw;
   q.j1 = chunk_end<E>(j0, A.V);
-  if (!ring.usable) {
+  if (!ring.usable || !DrawRing<VW, T::kRingBytes>::kStagedScan) {
     t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, q, sm.scan);
     return kDrawOk;
   }
@@ -854,8 +910,10 @@ template <typename ET>
 struct GreedyOp {
   using Args = GreedyArgs;
   using E = ET;
+  using T = SV_TILE(4, 2, 4);  // a light scan: half-chunk stages, 4 CTAs per SM
   static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is never chosen
   struct Smem {
+    float2 wpart[kWarps];  // the warp partials of this segment
     int row_last, req_last;
     int g[SV_MAX_K + 1];
   };
@@ -899,15 +957,14 @@ struct GreedyOp {
     a.poison = false;
   }
 
-  __device__ static __forceinline__ void warp_chunk(const Args&, const Seg&, int c,
-                                                    const uint4 (&v)[kVecPerThread],
+  __device__ static __forceinline__ void warp_slice(const Args&, const Seg&, int64_t j0,
+                                                    const uint4 (&v)[T::kStageVec],
                                                     bool poison, Acc& acc) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t j0 = (int64_t)c * E::kChunk;
     acc.poison |= poison;
 #pragma unroll
-    for (int it = 0; it < kVecPerThread; ++it) {
-      const int jb = (int)(j0 + (int64_t)warp_vec_slot(w, it, lane) * E::kPerVec);
+    for (int it = 0; it < T::kStageVec; ++it) {
+      const int jb = (int)(j0 + (int64_t)warp_vec_slot<T::kStageVec>(w, it, lane) * E::kPerVec);
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
         const float z = E::get(v[it], l);
@@ -920,14 +977,18 @@ struct GreedyOp {
     }
   }
 
-  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc) {
+  __device__ static __forceinline__ void prologue(const Args&, const Seg&, Smem&) {}
+
+  __device__ static __forceinline__ void seg_end(const Args& A, const Seg& g, Acc& acc,
+                                                 Smem& sm) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const bool poison = __any_sync(0xffffffffu, acc.poison);
     warp_argmax(acc.best, acc.bidx);
     if (lane == 0) {
-      WarpArgmax* p = A.part + ((g.rid * A.nseg + g.seg) * kWarps + w);
-      *reinterpret_cast<float2*>(p) =
-          make_float2(acc.best, __int_as_float(poison ? kPoisoned : acc.bidx));
+      const float2 out = make_float2(acc.best, __int_as_float(poison ? kPoisoned : acc.bidx));
+      sm.wpart[w] = out;
+      if (g.nseg > 1)
+        *reinterpret_cast<float2*>(A.part + ((g.rid * A.nseg + g.seg) * kWarps + w)) = out;
     }
   }
 
@@ -937,10 +998,12 @@ struct GreedyOp {
     const int n = n_of(A, r, n_ok);
     const int R = A.k + 1;
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) sm.row_last = arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
+    // a row of one segment is complete here: no counter, and its partials are this CTA's
+    if (threadIdx.x == 0)
+      sm.row_last = g.nseg == 1 || arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
     __syncthreads();
     if (!sm.row_last) return;
-    __threadfence();
+    if (g.nseg > 1) __threadfence();
 
     if (threadIdx.x < 32) {
       const int np = A.nseg * kWarps;
@@ -949,7 +1012,8 @@ struct GreedyOp {
       int bi = kNoIndex;
       bool poison = false;
       for (int q = lane; q < np; q += 32) {
-        const float2 pv = __ldcg(reinterpret_cast<const float2*>(wp + q));
+        const float2 pv =
+            g.nseg > 1 ? __ldcg(reinterpret_cast<const float2*>(wp + q)) : sm.wpart[q];
         const int pi = __float_as_int(pv.y);
         poison |= pi == kPoisoned;
         argmax_merge(bv, bi, pv.x, pi == kPoisoned ? kNoIndex : pi);
