@@ -45,6 +45,8 @@ SMALL = [
     (64, 4, 24577, "f32", 0.9, True, 4.0, 2.0, 0.5),       # 4 chunks (fp32), ragged tail
     (7, 8, 50001, "bf16", 1e-2, False, 2.0, 1.0, 1.0),     # very low temperature
     (5, 3, 777, "bf16", 50.0, True, 2.0, 1.0, 1.0),        # very high temperature
+    (6, 3, 151936, "bf16", 0.8, True, 2.0, 1.0, 1.0),      # 10 chunks: two segments per row
+    (4, 2, 200003, "bf16", 1.0, False, 2.0, 0.7, 1.0),     # two segments, rows not aligned
 ]
 
 
@@ -58,8 +60,9 @@ def test_sample_small(case):
     assert stats["flagged"] <= max(2, B // 4), stats
 
 
-def test_sample_draft_equals_target_accepts_all():
-    B, k, V = 32, 6, 20000
+@pytest.mark.parametrize("B,k,V", [(32, 6, 20000), (6, 3, 151936)])
+def test_sample_draft_equals_target_accepts_all(B, k, V):
+    # every draft accepted: the bonus draw from row k (one and two segments per row)
     d = synth.sample_inputs(B, k, V, "bf16", 0.9, device=DEV, seed=3)
     d["draft"] = d["target"][:, :k].contiguous()
     g = torch.Generator(device=DEV).manual_seed(4)
@@ -138,7 +141,9 @@ def test_sample_workload3_full_sampled_requests():
 
 # ------------------------------------------------------------------------------ greedy
 @pytest.mark.parametrize("B,k,V,dt,ties", [(64, 5, 32000, "bf16", False), (30, 4, 8191, "f32", True),
-                                          (10, 16, 40000, "bf16", True), (3, 1, 2, "f32", True)])
+                                          (10, 16, 40000, "bf16", True), (3, 1, 2, "f32", True),
+                                          (8, 4, 151936, "bf16", False),   # two segments per row
+                                          (5, 2, 300001, "f32", True)])    # five, not aligned
 def test_greedy_small(B, k, V, dt, ties):
     g = torch.Generator(device=DEV).manual_seed(V)
     if ties:
@@ -205,7 +210,7 @@ def test_sampled_on_one_hot_rows_equals_greedy():
 
 # ------------------------------------------------------------------------------ gate
 @pytest.mark.parametrize("N,V,dt", [(40, 151936, "f32"), (33, 50001, "bf16"), (17, 8191, "f32"),
-                                    (5, 2, "bf16")])
+                                    (5, 2, "bf16"), (9, 262145, "bf16")])
 def test_gate_small(N, V, dt):
     g = torch.Generator(device=DEV).manual_seed(N)
     z = torch.randn((N, V), generator=g, device=DEV) * 3
