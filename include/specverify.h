@@ -107,8 +107,10 @@ int sv_last_cuda_error(void);
  *   draft_tokens    [B, k] int32; entries past n_r are ignored (e.g. -1 padding).
  *   num_draft       [B] int32 per-request draft count n_r in [0, k], or NULL for all k.
  *   uniforms        [B, k+1] fp32 in [0, 1).
- *   B, k, V         B >= 0 (B = 0 is a no-op), 1 <= k <= SV_MAX_K, V >= 2,
- *                   B*(2k+1)*ceil(V/chunk) < 2^31.
+ *   B, k, V         B >= 0 (B = 0 is a no-op), 1 <= k <= SV_MAX_K, V >= 2, and
+ *                   B*(2k+1)*ceil(V/S) < 2^31 with S = 65536 logits for SV_F32 and
+ *                   131072 for SV_BF16 (one CTA per row piece of S logits); beyond that,
+ *                   SV_ERR_UNSUPPORTED.
  *   temperature     T, finite, 1e-4 <= T <= 1e4 (the fp32 exponent scale log2(e)/T must
  *                   stay in range); greedy decoding is spec_verify_greedy, not T -> 0.
  *   out_tokens      [B, k+1] int32: x_0..x_{a-1}, t, then -1 padding.
@@ -141,9 +143,9 @@ sv_status spec_verify_sample(const void* target_logits, const void* draft_logits
  *   g_i = argmax_j target[r, i, j] (lowest j among equal maxima; NaN entries are skipped)
  *   a   = the first i < n with x_i != g_i, else n
  *   emitted tokens: x_0 .. x_{a-1}, g_a;  accept length a.
- * Temperature does not enter. Arguments as for spec_verify_sample; a request with a data
- * error (bad n_r, a token outside [0, V), a needed row that is all NaN) gets
- * out_accept_len = -1 and an all -1 out_tokens row.
+ * Temperature does not enter. Arguments as for spec_verify_sample (with B*(k+1)*ceil(V/S)
+ * < 2^31); a request with a data error (bad n_r, a token outside [0, V), a needed row that
+ * is all NaN) gets out_accept_len = -1 and an all -1 out_tokens row.
  * ---------------------------------------------------------------------------------------- */
 size_t spec_verify_greedy_workspace(int B, int k, int V, sv_dtype dtype);
 sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
@@ -190,7 +192,8 @@ sv_status spec_verify_greedy_noalloc(const void* target_logits, sv_dtype dtype,
  *        gamma = 0); NaN entries are skipped;
  *   gamma = l1 - l2 (evaluated in double), fire = gamma > tau && a_hat in A.
  * Arguments
- *   logits      [N, V] dtype.  N >= 0 (N = 0 is a no-op), V >= 2.
+ *   logits      [N, V] dtype.  N >= 0 (N = 0 is a no-op), V >= 2, N*ceil(V/S) < 2^31
+ *               (S as for spec_verify_sample; beyond that, SV_ERR_UNSUPPORTED).
  *   tau         threshold (any float; compared in double).
  *   answer_set  [n_answer] int32, sorted ascending (duplicates allowed); may be NULL when
  *               n_answer == 0 (then nothing fires). An unsorted set gives unspecified
