@@ -174,12 +174,17 @@ def time_launches(fn, steps, warmup, stream, flush=None):
 
 
 def make_flush(device):
+    """L2 flush before a timed launch: write a buffer twice the size of L2, then read another
+    one, so the written lines are back in HBM (their write-back is not charged to the timed
+    launch) and L2 holds only clean lines of no use to it."""
     import torch
 
     buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device)
+    clean = torch.zeros(2 * L2_BYTES // 8, dtype=torch.int64, device=device)
 
     def flush():
         buf.fill_(1)
+        clean.max()
 
     return flush
 
@@ -331,7 +336,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
     value = whole_job_rate(world, n_total, args.steps, total_ms)
     rows = {}
     if rank == 0 and not args.no_rows:
-        rows = secondary_rows(args, dev, stream, peak)
+        rows = secondary_rows(args, dev, stream, peak, head=d)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -391,8 +396,9 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
         dist.destroy_process_group()
 
 
-def secondary_rows(args, dev, stream, peak):
-    """Event-timed launches of the other calls of the path on their own workloads."""
+def secondary_rows(args, dev, stream, peak, head=None):
+    """Event-timed launches of the other calls of the path on their own workloads (and the
+    greedy verify on the headline batch's target rows, `head`)."""
     import torch
 
     import speculative_decoding_verification_17_gb300 as sv
@@ -429,6 +435,21 @@ def secondary_rows(args, dev, stream, peak):
     rows["gate_n1280_v151936_f32"] = dict(ms=ms, rows_per_s=rows_t.shape[0] / (ms * 1e-3),
                                           gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak, bytes=nb)
     del d, rows_t, ws, gws
+
+    # greedy verify on the headline batch's target rows (B=512, k=8, V=128256 bf16, 1.18 GB)
+    if head is not None:
+        B, k, V = head["B"], head["k"], head["V"]
+        gws = torch.zeros(sv.spec_verify_greedy_workspace(B, k, V, sv.SV_BF16),
+                          dtype=torch.uint8, device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: sv.spec_verify_greedy(head["target"], head["draft_tokens"], None,
+                                          workspace=gws, stream=stream),
+            steps, 3, stream))
+        nb = B * (k + 1) * V * 2
+        rows[f"greedy_b{B}_k{k}_v{V}_bf16"] = dict(
+            ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms),
+            frac=gbs(nb, ms) / peak, bytes=nb)
+        del gws
 
     # bf16 Zipf workload: sampled + greedy (fits in L2: flushed before every launch)
     w = synth.WORKLOADS[1]
