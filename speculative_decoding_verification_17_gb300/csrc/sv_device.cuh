@@ -206,6 +206,51 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// A float-float number: an unevaluated sum hi + lo with |lo| <= ulp(hi)/2, about 48 bits.
+// Its arithmetic runs on the FP32 pipes; this GPU's FP64 pipe is far slower, and the draw's
+// scans are latency chains of such additions.
+struct DF {
+  float hi, lo;
+};
+
+// a + b, renormalised. Commutative to the bit (TwoSum's error term is exact), so a butterfly
+// of these leaves the same sum in every lane.
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  const float h = __fadd_rn(s, e);
+  return {h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ DF df_from_double(double d) {
+  const float h = __double2float_rn(d);
+  return {h, __double2float_rn(d - (double)h)};
+}
+
+__device__ __forceinline__ DF df_shfl_xor(DF a, int o) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+
+__device__ __forceinline__ DF df_shfl_up(DF a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+
+// Inclusive warp scan of float-float values (Hillis-Steele).
+__device__ __forceinline__ DF df_warp_scan(DF x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y = df_shfl_up(x, o);
+    if (lane >= o) x = df_add(y, x);
+  }
+  return x;
+}
+
 // Warp sum of floats carried as an unevaluated (hi, lo) pair: every level adds exactly.
 __device__ __forceinline__ void warp_sum_compensated(float& hi, float& lo) {
 #pragma unroll

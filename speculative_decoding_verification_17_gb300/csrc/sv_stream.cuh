@@ -39,6 +39,8 @@
 //   static void finish(const Args&, const Seg&, Smem&, Ring&);  all threads, after the segment
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "sv_device.cuh"
@@ -245,17 +247,40 @@ template <class Op>
 sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* ctl,
                           cudaStream_t st) {
   if (units <= 0) return SV_OK;
-  // host-side function attributes (no stream work), set on every call so they hold in any
-  // context: the ring's dynamic shared memory, and the carveout that fits the op's CTAs
   constexpr int kRingBytes = Op::T::kRingBytes;
-  cudaError_t e = cudaFuncSetAttribute(segment_kernel<Op>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+  // Host-side function attributes (no stream work): the ring's dynamic shared memory and the
+  // carveout that fits the op's CTAs. They are set once per device (bit d of `ready`); if a
+  // launch is refused anyway (the context was reset since), they are set again and the
+  // launch is retried once.
+  static std::atomic<unsigned long long> ready{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(segment_kernel<Op>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  auto set_attributes = [&]() -> cudaError_t {
+    cudaError_t r = cudaFuncSetAttribute(
+        segment_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(segment_kernel<Op>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (r == cudaSuccess && bit) ready.fetch_or(bit);
+    return r;
+  };
+  if (!(ready.load() & bit)) {
+    e = set_attributes();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
-  return launch_status();
+  e = cudaGetLastError();
+  if (e != cudaSuccess && bit) {  // attributes lost with a reset context: set them, retry
+    ready.fetch_and(~bit);
+    if (set_attributes() == cudaSuccess) {
+      segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
+      e = cudaGetLastError();
+    }
+  }
+  return e == cudaSuccess ? SV_OK : cuda_fail(e);
 }
 
 }  // namespace sv

@@ -59,24 +59,31 @@ __device__ __forceinline__ int64_t chunk_end(int64_t j0, int V) {
 // ============================================================================================
 // In-order draw inside one chunk
 // ============================================================================================
+constexpr int kScanRounds = 8;  // rounds of 32 vectors in one warp's share of a chunk
+
 struct ScanSmem {
-  double seg_tot[kWarps];
+  DF rt[kWarps * kScanRounds];  // round totals, in vocabulary order
   int seg_last[kWarps];
-  double owner_excl;
-  int owner;
+  int round;  // the round that holds the crossing, or -1
+  DF excl;    // the weight before it
   int result;
 };
 
 // Inverse-CDF draw inside the chunk that starts at j0: the first logit j, in vocabulary
 // order, whose running weight exceeds `target` (chunk units); when rounding leaves the
-// target at or past the chunk's total, the last logit with positive weight. Warp w owns the
-// contiguous segment [j0 + w*kSeg, j0 + (w+1)*kSeg) and reads it in rounds of 32*kPerVec
-// logits (one coalesced 16-byte vector per lane per round, two rounds loaded at once).
-// Lane sums are sequential fp32, round totals come from an inclusive warp scan in double,
-// segment totals are sequential sums of round totals. The owning warp replays exactly the
-// same loads and arithmetic, so the crossing is found there.
+// target at or past the chunk's total, the last logit with positive weight. Every consumer
+// thread must call this. Warp w owns the contiguous segment [j0 + w*kSeg, j0 + (w+1)*kSeg),
+// read in kScanRounds rounds of 32 coalesced 16-byte vectors; a lane sums its vector's
+// weights in order in fp32. The crossing is then found top down, in float-float sums:
+//  1. every warp reduces each of its rounds (a butterfly, the same total in every lane);
+//  2. one warp scans the kWarps*kScanRounds round totals for the crossing round;
+//  3. one warp scans that round's lane sums for the crossing lane, whose lane walks its
+//     vector.
+// Steps 2 and 3 add in other orders than step 1; where that moves the answer, the target
+// lies within rounding of a boundary, and the walk falls back to the round's (or chunk's)
+// last positive weight.
 // VW provides: using Raw; Raw load(int64_t j) const; void weights(const Raw&, float (&)[]),
-// with zero weight past the end of the row. Every consumer thread must call this.
+// with zero weight past the end of the row.
 template <typename E, typename VW>
 __device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& vw,
                           ScanSmem& sm) {
@@ -84,13 +91,14 @@ __device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& v
   constexpr int kRound = 32 * E::kPerVec;
   constexpr int kRounds = kSeg / kRound;
   constexpr int kBatch = 2;  // rounds loaded at once
-  static_assert(kRounds * kRound == kSeg && kRounds % kBatch == 0, "whole rounds and batches");
+  static_assert(kRounds == kScanRounds && kRounds % kBatch == 0, "whole rounds and batches");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t seg0 = j0 + (int64_t)warp * kSeg;
 
-  double seg = 0.0;
+  // ---- 1. lane sums and round totals (every warp) ----
+  float ls[kRounds];
   int lastpos = -1;
-#pragma unroll 1
+#pragma unroll
   for (int b = 0; b < kRounds; b += kBatch) {
     typename VW::Raw raw[kBatch];
 #pragma unroll
@@ -100,68 +108,79 @@ __device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& v
     for (int q = 0; q < kBatch; ++q) {
       float w[E::kPerVec];
       vw.weights(raw[q], w);
-      float ls = 0.0f;
+      float acc = 0.0f;
 #pragma unroll
       for (int l = 0; l < E::kPerVec; ++l) {
-        ls += w[l];
+        acc += w[l];
         if (w[l] > 0.0f) lastpos = (int)(seg0 + (b + q) * kRound + lane * E::kPerVec + l);
       }
-      const double incl = warp_scan_d((double)ls);
-      seg += __shfl_sync(0xffffffffu, incl, 31);
+      ls[b + q] = acc;
     }
   }
+  DF t[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) t[r] = DF{ls[r], 0.0f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) t[r] = df_add(t[r], df_shfl_xor(t[r], o));
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r)
+    if (lane == r) sm.rt[warp * kRounds + r] = t[r];
   lastpos = __reduce_max_sync(0xffffffffu, lastpos);
-  if (lane == 0) {
-    sm.seg_tot[warp] = seg;
-    sm.seg_last[warp] = lastpos;
-  }
+  if (lane == 0) sm.seg_last[warp] = lastpos;
   cbar();
-  if (threadIdx.x == 0) {
-    double run = 0.0;
-    int owner = -1, last = -1;
-    for (int w = 0; w < kWarps; ++w) {
-      if (owner < 0 && !take_last && sm.seg_tot[w] > 0.0 && run + sm.seg_tot[w] > target) {
-        owner = w;
-        sm.owner_excl = run;
-      }
-      if (owner < 0) run += sm.seg_tot[w];
-      last = max(last, sm.seg_last[w]);
-    }
-    sm.owner = owner;
-    sm.result = owner < 0 ? last : sm.seg_last[owner];
-  }
-  cbar();
-  if (warp == sm.owner) {
-    // replay: the same loads (identical bits) and the same arithmetic, round by round
-    double run = sm.owner_excl;
-#pragma unroll 1
-    for (int ro = 0; ro < kRounds; ++ro) {
-      const typename VW::Raw raw = vw.load(seg0 + ro * kRound + lane * E::kPerVec);
-      float w[E::kPerVec];
-      vw.weights(raw, w);
-      float ls = 0.0f;
+
+  if (warp == 0) {
+    const DF tgt = df_from_double(target);
+    // ---- 2. the crossing round (lane l holds round totals 2l and 2l+1) ----
+    const DF e0 = sm.rt[2 * lane], e1 = sm.rt[2 * lane + 1];
+    const DF incl = df_warp_scan(df_add(e0, e1));
+    DF ex = df_shfl_up(incl, 1);
+    if (lane == 0) ex = DF{0.0f, 0.0f};
+    const DF p0 = df_add(ex, e0), p1 = df_add(p0, e1);
+    const unsigned b0 = __ballot_sync(0xffffffffu, !take_last && e0.hi > 0.0f && df_gt(p0, tgt));
+    const unsigned b1 = __ballot_sync(0xffffffffu, !take_last && e1.hi > 0.0f && df_gt(p1, tgt));
+    int first = 0x7fffffff;
+    if (b0) first = 2 * (__ffs(b0) - 1);
+    if (b1) first = min(first, 2 * (__ffs(b1) - 1) + 1);
+    int last = sm.seg_last[lane < kWarps ? lane : 0];
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (first == 0x7fffffff) {
+      if (lane == 0) sm.result = last;
+    } else {
+      const float before = __shfl_sync(0xffffffffu, (first & 1) ? p0.hi : ex.hi, first >> 1);
+      const float before_lo = __shfl_sync(0xffffffffu, (first & 1) ? p0.lo : ex.lo, first >> 1);
+      // ---- 3. the crossing lane of that round, then the logit in its vector ----
+      const int w = first / kRounds, r = first - w * kRounds;
+      const int64_t base = j0 + (int64_t)w * kSeg + (int64_t)r * kRound;
+      const typename VW::Raw raw = vw.load(base + lane * E::kPerVec);
+      float wt[E::kPerVec];
+      vw.weights(raw, wt);
+      float acc = 0.0f;
 #pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) ls += w[l];
-      const double incl = warp_scan_d((double)ls);
-      const double tot = __shfl_sync(0xffffffffu, incl, 31);
-      if (run + tot > target) {
-        const unsigned bal = __ballot_sync(0xffffffffu, ls > 0.0f && run + incl > target);
-        const int L = bal ? __ffs(bal) - 1 : 31;
-        const double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == L) {
-          double r2 = run + (lane ? excl : 0.0);
-          int t = -1, lp = -1;
+      for (int l = 0; l < E::kPerVec; ++l) acc += wt[l];
+      const DF li = df_warp_scan(DF{acc, 0.0f});
+      DF lex = df_shfl_up(li, 1);
+      if (lane == 0) lex = DF{0.0f, 0.0f};
+      const DF start = df_add(DF{before, before_lo}, lex);
+      const DF through = df_add(start, DF{acc, 0.0f});
+      const unsigned bl = __ballot_sync(0xffffffffu, acc > 0.0f && df_gt(through, tgt));
+      const unsigned pos = __ballot_sync(0xffffffffu, acc > 0.0f);
+      const int L = bl ? __ffs(bl) - 1 : (pos ? 31 - __clz(pos) : 0);
+      if (lane == L) {
+        DF run = start;
+        int tk = -1, lp = -1;
 #pragma unroll
-          for (int l = 0; l < E::kPerVec; ++l) {
-            if (w[l] > 0.0f) lp = (int)(seg0 + ro * kRound + lane * E::kPerVec + l);
-            r2 += (double)w[l];
-            if (t < 0 && r2 > target && w[l] > 0.0f) t = lp;
+        for (int l = 0; l < E::kPerVec; ++l) {
+          run = df_add(run, DF{wt[l], 0.0f});
+          if (wt[l] > 0.0f) {
+            lp = (int)(base + lane * E::kPerVec + l);
+            if (tk < 0 && df_gt(run, tgt)) tk = lp;
           }
-          if (t >= 0 || lp >= 0) sm.result = t >= 0 ? t : lp;
         }
-        break;  // warp-uniform
+        sm.result = tk >= 0 ? tk : (lp >= 0 ? lp : last);
       }
-      run += tot;
     }
   }
   cbar();
@@ -169,34 +188,40 @@ __device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& v
 }
 
 // Chunk choice for an inverse-CDF draw over per-chunk masses mass(c), c in [0, nch): the
-// first chunk whose running total exceeds target. Run by one full warp. Returns the chunk
-// (or, when rounding leaves none, the last chunk with positive mass and take_last = true)
-// and the running total before it.
+// first chunk whose running total exceeds target. Run by one full warp, in float-float sums.
+// Returns the chunk (or, when rounding leaves none, the last chunk with positive mass and
+// take_last = true) and the running total before it.
 template <typename MF>
-__device__ int pick_chunk(int nch, double target, MF mass, double& before, bool& take_last) {
+__device__ int pick_chunk(int nch, DF target, MF mass, DF& before, bool& take_last) {
   const int lane = threadIdx.x & 31;
-  double run = 0.0;
+  DF run{0.0f, 0.0f};
   int last_pos = -1;
-  double last_before = 0.0;
+  DF last_before{0.0f, 0.0f};
   for (int c0 = 0; c0 < nch; c0 += 32) {
     const int c = c0 + lane;
-    const double m = c < nch ? mass(c) : 0.0;
-    const double incl = warp_scan_d(m);
-    const bool cross = c < nch && m > 0.0 && run + incl > target;
-    const unsigned bal = __ballot_sync(0xffffffffu, cross);
+    const DF m = c < nch ? mass(c) : DF{0.0f, 0.0f};
+    const DF incl = df_warp_scan(m);
+    DF ex = df_shfl_up(incl, 1);
+    if (lane == 0) ex = DF{0.0f, 0.0f};
+    const DF through = df_add(run, df_add(ex, m));
+    const unsigned bal = __ballot_sync(0xffffffffu, c < nch && m.hi > 0.0f &&
+                                                        df_gt(through, target));
     if (bal) {
       const int fl = __ffs(bal) - 1;
-      before = run + __shfl_sync(0xffffffffu, incl - m, fl);
+      before = df_add(run, DF{__shfl_sync(0xffffffffu, ex.hi, fl),
+                              __shfl_sync(0xffffffffu, ex.lo, fl)});
       take_last = false;
       return c0 + fl;
     }
-    const unsigned pos = __ballot_sync(0xffffffffu, c < nch && m > 0.0);
+    const unsigned pos = __ballot_sync(0xffffffffu, c < nch && m.hi > 0.0f);
     if (pos) {
       const int ll = 31 - __clz(pos);
       last_pos = c0 + ll;
-      last_before = run + __shfl_sync(0xffffffffu, incl - m, ll);
+      last_before = df_add(run, DF{__shfl_sync(0xffffffffu, ex.hi, ll),
+                                   __shfl_sync(0xffffffffu, ex.lo, ll)});
     }
-    run += __shfl_sync(0xffffffffu, incl, 31);
+    run = df_add(run, DF{__shfl_sync(0xffffffffu, incl.hi, 31),
+                         __shfl_sync(0xffffffffu, incl.lo, 31)});
   }
   before = last_before;
   take_last = true;
@@ -222,7 +247,7 @@ struct SampleArgs {
   float* out_resid;
   WarpSoftmax* part;  // [B * (2k+1)][nseg][kWarps]
   RowSoftmax* row;
-  double* resid;      // [B][nch][kWarps] per-warp chunk masses of the request's draw
+  DF* resid;          // [B][nch][kWarps] per-warp chunk masses of the request's draw
   unsigned int* row_cnt;
   unsigned int* req_cnt;
 };
@@ -239,6 +264,17 @@ struct ResidW {
     const float ep = ex2(fmaf(zp, s, cp));
     const float eq = ex2(fmaf(zq, s, cq));
     return fmaxf(0.0f, fmaf(ep, ip, -(eq * iq)));
+  }
+  // The same for two logit pairs at once, with packed fp32x2 arithmetic (each lane of a
+  // packed FMA or multiply rounds exactly like the scalar one, so the weights are identical).
+  __device__ __forceinline__ float2 pair(float2 zp, float2 zq) const {
+    const float2 xp = __ffma2_rn(zp, make_float2(s, s), make_float2(cp, cp));
+    const float2 xq = __ffma2_rn(zq, make_float2(s, s), make_float2(cq, cq));
+    const float2 ep = make_float2(ex2(xp.x), ex2(xp.y));
+    const float2 eq = make_float2(ex2(xq.x), ex2(xq.y));
+    const float2 nq = __fmul2_rn(eq, make_float2(-iq, -iq));
+    const float2 d = __ffma2_rn(ep, make_float2(ip, ip), nq);
+    return make_float2(fmaxf(0.0f, d.x), fmaxf(0.0f, d.y));
   }
 };
 
@@ -271,7 +307,11 @@ struct ResidScan {
   }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
 #pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) w[l] = wf(E::get(r.p, l), E::get(r.q, l));
+    for (int p = 0; p < E::kPerVec / 2; ++p) {
+      const float2 v = wf.pair(E::get2(r.p, p), E::get2(r.q, p));
+      w[2 * p] = v.x;
+      w[2 * p + 1] = v.y;
+    }
   }
 };
 
@@ -293,7 +333,11 @@ struct BonusScan {
   __device__ __forceinline__ Raw pad() const { return E::pad_vec(E::kNegInfBits); }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
 #pragma unroll
-    for (int l = 0; l < E::kPerVec; ++l) w[l] = ex2(fmaf(E::get(r, l), s, c));
+    for (int p = 0; p < E::kPerVec / 2; ++p) {
+      const float2 x = __ffma2_rn(E::get2(r, p), make_float2(s, s), make_float2(c, c));
+      w[2 * p] = ex2(x.x);
+      w[2 * p + 1] = ex2(x.y);
+    }
   }
 };
 
@@ -339,7 +383,7 @@ struct DrawRing {
 // the copy of the piece two ahead. Without it, every thread loads its vectors from global
 // memory. Every thread calls this.
 template <typename E, int RingBytes, class VW>
-__device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& ring) {
+__device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!ring.usable || !SV_RESID_RING) {
     for (int c = 0; c < nch; ++c) {
@@ -363,7 +407,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& r
       }
       float hi = acc, lo = 0.0f;
       warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)c * kWarps + warp] = (double)hi + (double)lo;
+      if (lane == 0) part[(int64_t)c * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
     }
     return true;
   }
@@ -432,7 +476,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& r
     if (h % kPer == kPer - 1) {  // every piece of chunk h / kPer is in
       float hi = acc, lo = 0.0f;
       warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)(h / kPer) * kWarps + warp] = (double)hi + (double)lo;
+      if (lane == 0) part[(int64_t)(h / kPer) * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
       acc = 0.0f;
     }
   }
@@ -440,7 +484,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, double* part, Ring& r
     if (lane == 0) {
       atomicOr(&ring.ctl->error, 1u);
       for (int c = 0; c < nch; ++c)
-        part[(int64_t)c * kWarps + warp] = __longlong_as_double(0x7ff8000000000000ll);
+        part[(int64_t)c * kWarps + warp] = DF{__int_as_float(0x7fc00000), 0.0f};
     }
     return false;
   }
@@ -475,6 +519,8 @@ struct SampleOp {
   using E = ET;
   using T = SV_TILE(8, 2, 3);  // exp-heavy: whole-chunk stages, 3 CTAs of 80 registers
   static constexpr uint32_t kPad = E::kNegInfBits;
+  static constexpr int kSmemChunks = 32;  // rows of up to this many chunks keep the
+                                          // draw's chunk masses in shared memory
   struct Smem {
     float4 wpart[kWarps];  // the warp partials of this segment
     float zx;              // the logit of the row's draft token, when prefetched
@@ -482,6 +528,7 @@ struct SampleOp {
     int a, err, chunk, take_last;
     double W, before;
     ScanSmem scan;
+    DF cm[kSmemChunks * kWarps];  // per-warp chunk masses of the draw
   };
   // One lane's running softmax sum over the segment: hi + lo (an unevaluated pair) in units
   // of 2^K, K an integer with K >= s * (the largest logit seen), and whether it saw a NaN,
@@ -627,7 +674,7 @@ struct SampleOp {
   __device__ static void finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
                                         Ring& ring);
   template <class VW>
-  __device__ static int draw(const Args& A, const VW& vw, double* part, float u, Smem& sm,
+  __device__ static int draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                              Ring& ring, int& t, double& W);
 };
 
@@ -701,23 +748,25 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
 // one bulk copy each). Every thread calls this. Returns a DrawStatus; t is the drawn token.
 template <typename ET>
 template <class VW>
-__device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, double* part, float u, Smem& sm,
+__device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                                   Ring& ring, int& t, double& W) {
   const int tid = threadIdx.x, lane = tid & 31;
   const bool landed = chunk_masses<E, T::kRingBytes>(A.nch, A.V, vw, part, ring);
   __syncthreads();
-  // chunk masses M_c = sum over warps (fixed order), and W = sum_c M_c (warp 0)
+  // chunk masses M_c = sum over warps (fixed order), and W = sum_c M_c (warp 0), all in
+  // float-float sums
   if (tid < 32) {
-    double wsum = 0.0;
+    DF wsum{0.0f, 0.0f};
     for (int c = lane; c < A.nch; c += 32) {
-      double mc = 0.0;
+      DF mc{0.0f, 0.0f};
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) mc += part[(int64_t)c * kWarps + w];
+      for (int w = 0; w < kWarps; ++w) mc = df_add(mc, part[(int64_t)c * kWarps + w]);
       part[(int64_t)c * kWarps] = mc;
-      wsum += mc;
+      wsum = df_add(wsum, mc);
     }
-    wsum = warp_sum_d(wsum);
-    if (lane == 0) sm.W = wsum;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum = df_add(wsum, df_shfl_xor(wsum, o));
+    if (lane == 0) sm.W = (double)wsum.hi + (double)wsum.lo;
   }
   __syncthreads();
   W = sm.W;
@@ -725,13 +774,14 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, double* part, flo
   if (!(W > 0.0)) return kDrawNoMass;
   const double target = (double)u * W;
   if (tid < 32) {
-    double before;
+    DF before;
     bool tl;
     const int c = pick_chunk(
-        A.nch, target, [&](int cc) { return part[(int64_t)cc * kWarps]; }, before, tl);
+        A.nch, df_from_double(target), [&](int cc) { return part[(int64_t)cc * kWarps]; },
+        before, tl);
     if (lane == 0) {
       sm.chunk = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
-      sm.before = before;
+      sm.before = (double)before.hi + (double)before.lo;
       sm.take_last = tl;
     }
   }
@@ -815,7 +865,9 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   if (!sm.err) {
     const float s = A.s;
     const float uk = __ldg(u + A.k);
-    double* part = A.resid + (int64_t)r * A.nch * kWarps;  // [nch][kWarps]
+    DF* part = A.nch <= kSmemChunks  // [nch][kWarps]
+                       ? sm.cm
+                       : A.resid + (int64_t)r * A.nch * kWarps;
     st = kDrawNoMass;
     if (a < n) {
       // ---- residual norm(max(0, p_a - q_a)) ----
@@ -1133,7 +1185,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   char* ws = static_cast<char*>(workspace);
   A.part = reinterpret_cast<WarpSoftmax*>(ws + L.part);
   A.row = reinterpret_cast<RowSoftmax*>(ws + L.row);
-  A.resid = reinterpret_cast<double*>(ws + L.resid);
+  A.resid = reinterpret_cast<DF*>(ws + L.resid);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
