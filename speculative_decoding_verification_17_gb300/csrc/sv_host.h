@@ -66,14 +66,15 @@ struct WarpSoftmax {
   float pad;
 };
 
-// Merged softmax statistics of one row: S = sum of 2^(z*s - K) over the row in double,
-// K = the largest slice reference (an integer), px = probability of the row's draft token.
+// Merged softmax statistics of one row: S = sum of 2^(z*s - K) over the row, K = the
+// largest reference of its partials (an integer), and zx = the logit of the row's draft
+// token; its probability is 2^(zx*s - K) / S.
 struct RowSoftmax {
   double S;
-  double px;
+  float zx;
   float K;
   int status;  // 0 ok, 1 not a distribution, 2 draft token out of range
-  double pad;
+  int pad[3];
 };
 
 struct WarpArgmax {

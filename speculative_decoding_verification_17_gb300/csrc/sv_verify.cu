@@ -22,13 +22,14 @@
 //                           compensated pair; per segment one warp reduction to a partial
 //                           (K, hi, lo); in the greedy verify the running argmax.
 //  row finish (the CTA that completes the row)  K_row = max K; S = sum of partial sums times
-//                           2^(K - K_row), exact powers of two, in double; p(x) =
-//                           2^(z_x*s - K_row) / S in double.
-//  request finish (the CTA that completes the request)  ratios p_i(x_i)/q_i(x_i) in double
-//                           against the uniforms, the accepted prefix a, then one draw: the
-//                           residual max(0, p_a - q_a) or the bonus p_n, each as one pass
-//                           over its row (pair) for per-chunk masses, then one chunk scanned
-//                           in vocabulary order.
+//                           2^(K - K_row), exact powers of two, in float-float; the row
+//                           publishes S, K_row and its draft token's logit z_x.
+//  request finish (the CTA that completes the request)  the accept tests u_i < p_i/q_i, as
+//                           u*S_p < 2^(y_p - y_q)*S_q with y = z_x*s - K exact in double,
+//                           the accepted prefix a, then one draw: the residual
+//                           max(0, p_a - q_a) or the bonus p_n, each as one pass over its
+//                           row (pair) for per-chunk masses, then one chunk scanned in
+//                           vocabulary order (float-float sums throughout).
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -251,11 +252,6 @@ struct SampleArgs {
   unsigned int* row_cnt;
   unsigned int* req_cnt;
 };
-
-// 2^d for an integer d <= 0, exactly (0 below the double range).
-__device__ __forceinline__ double pow2i(int d) {
-  return d < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + d) << 52);
-}
 
 // Residual weight max(0, p_j - q_j) with both normalisers folded in (row units).
 struct ResidW {
@@ -499,16 +495,10 @@ __device__ __forceinline__ WarpSoftmax ld_part(const WarpSoftmax* p) {
 __device__ __forceinline__ RowSoftmax ld_row(const RowSoftmax* p) {
   RowSoftmax r;
   r.S = __ldcg(&p->S);
-  r.px = __ldcg(&p->px);
+  r.zx = __ldcg(&p->zx);
   r.K = __ldcg(&p->K);
   r.status = __ldcg(&p->status);
   return r;
-}
-
-// Mass of a warp partial in units of 2^K (K the row reference): exact power-of-two scaling.
-__device__ __forceinline__ double part_mass(const WarpSoftmax& w, float K) {
-  if (!(w.K > -INFINITY)) return w.K == -INFINITY ? 0.0 : w.hi;  // empty, or NaN (poisoned)
-  return ((double)w.hi + (double)w.lo) * pow2i((int)(w.K - K));
 }
 
 enum DrawStatus { kDrawOk = 0, kDrawNoMass = 1, kDrawFailed = 2 };
@@ -684,7 +674,6 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   bool n_ok;
   const int n = n_of(A, r, n_ok);
   const int i = position(A, g);
-  const float s = A.s;
   // a row of one segment is complete here: no counter, and its partials are this CTA's
   if (threadIdx.x == 0)
     sm.row_last = g.nseg == 1 || arrive_last(A.row_cnt + g.rid, (unsigned)g.nseg);
@@ -712,25 +701,30 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
     }
     poison = __any_sync(0xffffffffu, poison);
     K = warp_max_f(K);
-    double S = 0.0;
+    // S = sum of the partials in units of 2^K (exact power-of-two scaling), in float-float
+    DF Sd{0.0f, 0.0f};
     if (K > -INFINITY)
-      for (int q = lane; q < np; q += 32) S += part_mass(part_q(q), K);
-    S = warp_sum_d(S);
+      for (int q = lane; q < np; q += 32) {
+        const WarpSoftmax w = part_q(q);
+        if (w.K > -INFINITY) {
+          const float sc = pow2_nonpos(w.K - K);
+          Sd = df_add(Sd, df_add(DF{w.hi * sc, 0.0f}, DF{w.lo * sc, 0.0f}));
+        }
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Sd = df_add(Sd, df_shfl_xor(Sd, o));
+    const double S = (double)Sd.hi + (double)Sd.lo;
     if (lane == 0) {
       int status = (!poison && K > -INFINITY && isfinite(S) && S > 0.0) ? 0 : 1;
-      double px = 0.0;
+      float zx = 0.0f;
       if (i < n) {
         const int32_t xi = __ldg(A.tokens + (int64_t)r * A.k + i);
-        if (xi < 0 || xi >= A.V) {
-          status = status ? status : 2;
-        } else if (status == 0) {
-          const float zx = g.nseg == 1 ? sm.zx : E::load1(g.row, xi);
-          px = exp2((double)zx * (double)s - (double)K) / S;
-        }
+        if (xi < 0 || xi >= A.V) status = status ? status : 2;
+        else if (status == 0) zx = g.nseg == 1 ? sm.zx : E::load1(g.row, xi);
       }
       RowSoftmax* rs = A.row + g.rid;
       rs->S = S;
-      rs->px = px;
+      rs->zx = zx;
       rs->K = K;
       rs->status = status;
       sm.req_last = arrive_last(A.req_cnt + r, (unsigned)(2 * n + 1));
@@ -829,15 +823,22 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   if (tid < 32) {
     bool bad = !n_ok;
     bool reject = false;
-    double pt = 0.0, pq = 0.0;
+    float pt = 0.0f, pq = 0.0f;
     if (n_ok && lane < n) {
       const RowSoftmax t = ld_row(A.row + (int64_t)r * R + lane);
       const RowSoftmax q = ld_row(A.row + (int64_t)r * R + A.k + 1 + lane);
       const float ui = __ldg(u + lane);
       bad = t.status != 0 || q.status != 0 || !(ui >= 0.0f && ui < 1.0f);
-      pt = t.px;
-      pq = q.px;
-      reject = !((double)ui < pt / pq);
+      // p = 2^(yp)/Sp and q = 2^(yq)/Sq with y = zx*s - K, exact in double. The test
+      // u < p/q, as u*Sp < 2^(yp - yq)*Sq: one exp2 and no division (q(x) = 0 accepts,
+      // p(x) = q(x) = 0 rejects, as the quotient would).
+      const double sd = (double)A.s;
+      const double yp = (double)t.zx * sd - (double)t.K;
+      const double yq = (double)q.zx * sd - (double)q.K;
+      reject = !((double)ui * t.S < exp2(yp - yq) * q.S);
+      // the optional p and q outputs, in fp32
+      pt = ex2(fmaf(t.zx, A.s, -t.K)) / (float)t.S;
+      pq = ex2(fmaf(q.zx, A.s, -q.K)) / (float)q.S;
     }
     if (n_ok && lane == 0) {
       const RowSoftmax t = ld_row(A.row + (int64_t)r * R + n);
@@ -849,8 +850,8 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     const int a = rej ? __ffs(rej) - 1 : n;
     if (lane < A.k) {
       const float nan = __int_as_float(0x7fc00000);
-      if (A.out_p) A.out_p[(int64_t)r * A.k + lane] = err ? nan : (lane < n ? (float)pt : 0.0f);
-      if (A.out_q) A.out_q[(int64_t)r * A.k + lane] = err ? nan : (lane < n ? (float)pq : 0.0f);
+      if (A.out_p) A.out_p[(int64_t)r * A.k + lane] = err ? nan : (lane < n ? pt : 0.0f);
+      if (A.out_q) A.out_q[(int64_t)r * A.k + lane] = err ? nan : (lane < n ? pq : 0.0f);
     }
     if (lane == 0) {
       sm.a = a;
