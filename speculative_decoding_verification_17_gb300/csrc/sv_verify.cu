@@ -440,7 +440,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
   if (tid == 0)
     for (int h = 0; h < 2 && h < np; ++h) issue(h);
   // every thread follows the same barrier phases
-  float acc = 0.0f;
+  float2 acc2 = make_float2(0.0f, 0.0f);
   bool timed_out = false;
   for (int h = 0; h < np; ++h) {
     const int st = h & 1;
@@ -462,18 +462,27 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
       ring.released[st] = 0;
       if (h + 2 < np) issue(h + 2);
     }
+    // each vector's weights in a pairwise tree of packed fp32x2 adds, then into the
+    // lane's running pair (the chunk masses only choose the chunk; the scan recomputes)
 #pragma unroll
     for (int it = 0; it < kVec; ++it) {
       float w[E::kPerVec];
       vw.weights(raw[it], w);
+      float2 t[E::kPerVec / 2];
 #pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
+      for (int p = 0; p < E::kPerVec / 2; ++p) t[p] = make_float2(w[2 * p], w[2 * p + 1]);
+#pragma unroll
+      for (int q = E::kPerVec / 4; q >= 1; q >>= 1)
+#pragma unroll
+        for (int p = 0; p < q; ++p) t[p] = __fadd2_rn(t[p], t[p + q]);
+      acc2 = __fadd2_rn(acc2, t[0]);
     }
     if (h % kPer == kPer - 1) {  // every piece of chunk h / kPer is in
-      float hi = acc, lo = 0.0f;
+      float hi = acc2.x + acc2.y, lo = 0.0f;
       warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)(h / kPer) * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
-      acc = 0.0f;
+      if (lane == 0)
+        part[(int64_t)(h / kPer) * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
+      acc2 = make_float2(0.0f, 0.0f);
     }
   }
   if (__any_sync(0xffffffffu, timed_out)) {
