@@ -58,9 +58,10 @@ def _bind(lib):
     lib.oracle_spec_verify_greedy.argtypes = [P, I, P, P, I, I, I, P, P, I, I]
     lib.oracle_logit_gap_gate.argtypes = [P, I, I, I, D, P, I, P, P, P, P, I, I]
     lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, I, I]
+    lib.oracle_draft_confidence.argtypes = [P, I, P, I, I, I, D, I, D, P, P, P, I, I]
     for f in (lib.oracle_row_softmax, lib.oracle_spec_verify_sample,
               lib.oracle_spec_verify_greedy, lib.oracle_logit_gap_gate,
-              lib.oracle_ngram_propose):
+              lib.oracle_ngram_propose, lib.oracle_draft_confidence):
         f.restype = ctypes.c_int
     return lib
 
@@ -287,6 +288,31 @@ def logit_gap_gate(logits, tau: float, answer_set, rows=None, threads: int = 1) 
                                          _ptr(out["flag"]), a, b)
 
     _run(fn, _ranges(idx, threads), threads)
+    return out
+
+
+CONF_TOP_PROB = 0
+CONF_INV_ENTROPY = 1
+
+
+def draft_confidence(draft, num_draft, T: float, mode: int, floor: float, requests=None,
+                     threads: int = 1) -> dict:
+    """Draft-side confidence c[B, k] and the variable-length stop num_draft[B] (see
+    oracle.h); flag[B] is the first near-tie position up to the stop, or -1."""
+    z, code = as_logits(draft)
+    B, k, V = z.shape
+    nd = _i32(num_draft)
+    out = dict(num_draft=np.full(B, -2, np.int32), conf=np.full((B, k), np.nan),
+               flag=np.full(B, -2, np.int32))
+    lib = _load()
+    reqs = sorted(range(B) if requests is None else {int(r) for r in requests})
+
+    def fn(a, b):
+        return lib.oracle_draft_confidence(_ptr(z), code, _ptr(nd), B, k, V, float(T),
+                                           int(mode), float(floor), _ptr(out["num_draft"]),
+                                           _ptr(out["conf"]), _ptr(out["flag"]), a, b)
+
+    _run(fn, _ranges(reqs, threads), threads)
     return out
 
 

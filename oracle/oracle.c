@@ -21,6 +21,9 @@
  *    mismatch take the target's token).
  *  - Gate: "Speculative Pre-Positioning", section 2.4, Eq. (11) and Eq. (12), and section 3.4,
  *    Algorithm 2 (Top2, gap, argmax, fire or fall through).
+ *  - Draft-confidence stop: the "speculative-decoding-plan.md" design note, the
+ *    variable-length drafting paragraph (keep drafting while the draft's top probability, or
+ *    the inverse of its entropy, stays above a floor).
  *  - N-gram proposer: "The Inference Wall, Part 7", section "What S is in this experiment,
  *    and what 'ngram' actually means" (four-word phrase first, then three, then two; copy
  *    what followed the phrase; nothing earlier means no proposal).
@@ -307,6 +310,73 @@ int oracle_spec_verify_greedy(const void* target, int dtype, const int32_t* draf
 static int in_answer_set(const int32_t* set, int n, int32_t v) {
   for (int i = 0; i < n; ++i)
     if (set[i] == v) return 1;
+  return 0;
+}
+
+/* ---- draft-side confidence stop ---- */
+
+/* c of one draft row: its top probability (mode 0) or the inverse of its entropy in nats
+ * (mode 1), from q = softmax(row / T) written out term by term in ascending token order.
+ * Returns -1 when the row is not a distribution. */
+static int row_confidence(const void* base, int dtype, size_t off, int V, double T, int mode,
+                          double* c) {
+  double m, S;
+  if (softmax_stats(base, dtype, off, V, T, &m, &S) != 0) return -1;
+  if (mode == 0) {
+    double top = 0.0;
+    for (int j = 0; j < V; ++j) {
+      const double q = prob_at(base, dtype, off, m, S, T, j);
+      if (q > top) top = q;
+    }
+    *c = top;
+    return 0;
+  }
+  double H = 0.0;
+  for (int j = 0; j < V; ++j) {
+    const double q = prob_at(base, dtype, off, m, S, T, j);
+    if (q > 0.0) H -= q * log(q);
+  }
+  *c = H > 0.0 ? 1.0 / H : INFINITY;
+  return 0;
+}
+
+int oracle_draft_confidence(const void* draft, int dtype, const int32_t* num_draft, int B,
+                            int k, int V, double T, int mode, double floor_val,
+                            int32_t* out_num_draft, double* out_conf, int32_t* out_flag,
+                            int r0, int r1) {
+  if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  if (!(T > 0.0) || !isfinite(T) || (mode != 0 && mode != 1) || isnan(floor_val)) return -1;
+  if (r0 < 0 || r1 > B || r0 > r1) return -1;
+  if (r0 == r1) return 0;
+  if (!draft || !out_num_draft) return -1;
+  for (int r = r0; r < r1; ++r) {
+    const int n_in = num_draft ? num_draft[r] : k;
+    double c[ORACLE_MAX_K];
+    int bad = n_in < 0 || n_in > k;
+    for (int i = 0; !bad && i < n_in; ++i) {
+      const size_t off = ((size_t)r * (size_t)k + (size_t)i) * (size_t)V;
+      if (row_confidence(draft, dtype, off, V, T, mode, &c[i]) != 0) bad = 1;
+    }
+    if (bad) {
+      out_num_draft[r] = -1;
+      if (out_conf)
+        for (int i = 0; i < k; ++i) out_conf[(size_t)r * k + i] = NAN;
+      if (out_flag) out_flag[r] = -1;
+      continue;
+    }
+    int n = n_in, flag = -1;
+    for (int i = 0; i < n_in; ++i) {
+      if (flag < 0 && fabs(c[i] - floor_val) <= ORACLE_CONF_MARGIN * fabs(floor_val)) flag = i;
+      if (c[i] < floor_val) {
+        n = i;
+        break;
+      }
+    }
+    out_num_draft[r] = n;
+    if (out_conf)
+      for (int i = 0; i < k; ++i) out_conf[(size_t)r * k + i] = i < n_in ? c[i] : 0.0;
+    if (out_flag) out_flag[r] = flag;
+  }
   return 0;
 }
 

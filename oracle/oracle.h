@@ -59,6 +59,29 @@ int oracle_logit_gap_gate(const void* logits, int dtype, int N, int V, double ta
                           double* out_gap, uint8_t* out_fire, uint8_t* out_flag, int i0,
                           int i1);
 
+/* Relative near-tie threshold of the draft-confidence stop: |c - floor| <= this * floor. */
+#define ORACLE_CONF_MARGIN 1e-5
+
+/* Draft-side confidence and the variable-length stop ("speculative-decoding-plan.md", the
+ * variable-length drafting paragraph after "The acceptance math": the draft keeps proposing
+ * while its own confidence stays above a floor, by top probability or an inverse-entropy
+ * gate, and stops when it gets unsure). For request r in [r0, r1), with n_in = num_draft[r]
+ * (all k when num_draft is NULL) and q_i = softmax(draft[r, i] / T) for i < n_in:
+ *   mode 0: c_i = max_j q_i(j)                                  (top probability)
+ *   mode 1: c_i = 1 / H_i, H_i = -sum_j q_i(j) ln q_i(j) nats   (+inf when H_i = 0)
+ *   out_num_draft[r] = the first i < n_in with c_i < floor, else n_in;
+ *   out_conf[r, i]   = c_i for i < n_in, 0 beyond (may be NULL);
+ *   out_flag[r]      = the first i up to the stop with |c_i - floor| <= ORACLE_CONF_MARGIN
+ *                      * floor, else -1 (may be NULL).
+ * A request with a data error (n_in outside [0, k], or a row it reads that is not a
+ * distribution) gets out_num_draft -1, out_conf NaN and flag -1. H is the definition
+ * evaluated in double: accurate to about 1e-17 nats absolute, so 1/H is accurate wherever
+ * H is well above that (a floor on 1/H below 1e12, say). */
+int oracle_draft_confidence(const void* draft, int dtype, const int32_t* num_draft, int B,
+                            int k, int V, double T, int mode, double floor_val,
+                            int32_t* out_num_draft, double* out_conf, int32_t* out_flag,
+                            int r0, int r1);
+
 /* Prompt-lookup n-gram proposer; outputs as the library's ngram_propose. */
 int oracle_ngram_propose(const int32_t* history, const int32_t* hist_len, int B, int L_max,
                          int n_max, int n_min, int k, int32_t* out_draft,

@@ -11,6 +11,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_confidence as C
 import test_oracle_rules as R
 import test_oracle_sample as S
 
@@ -61,6 +62,15 @@ MUTANTS = [
      [lambda: R.test_ngram_brute_force(3)]),
     ("n-gram takes the latest occurrence", "for (int s = 0; s + n <= L - 1; ++s) {",
      "for (int s = L - 1 - n; s >= 0; --s) {", [lambda: R.test_ngram_brute_force(2)]),
+    ("entropy in bits", "if (q > 0.0) H -= q * log(q);", "if (q > 0.0) H -= q * log2(q);",
+     [C.test_uniform_rows_have_closed_forms, C.test_inverse_entropy_stop_uses_the_entropy_in_nats]),
+    ("confidence stop at c == floor", "if (c[i] < floor_val) {", "if (c[i] <= floor_val) {",
+     [C.test_near_tie_is_flagged]),
+    ("top probability of the first token", "if (q > top) top = q;", "if (j == 0) top = q;",
+     [C.test_stop_is_the_first_position_below_the_floor,
+      lambda: C.test_random_rows_match_scipy(1.0)]),
+    ("draft count ignored", "const int n_in = num_draft ? num_draft[r] : k;",
+     "const int n_in = k;", [C.test_stop_respects_the_input_draft_count]),
 ]
 
 
