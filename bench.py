@@ -450,6 +450,23 @@ def secondary_rows(args, dev, stream, peak, head=None):
             ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms),
             frac=gbs(nb, ms) / peak, bytes=nb)
         del gws
+        # draft-side confidence stop on the same batch's draft rows (k rows per request)
+        nb = B * k * V * 2
+        cws = torch.zeros(sv.draft_confidence_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                          device=dev)
+        cnd = torch.empty((B,), dtype=torch.int32, device=dev)
+        cc = torch.empty((B, k), dtype=torch.float32, device=dev)
+        for mode, name, floor in ((sv.SV_CONF_TOP_PROB, "top", 0.05),
+                                  (sv.SV_CONF_INV_ENTROPY, "inv_entropy", 0.2)):
+            ms = statistics.mean(time_launches(
+                lambda: sv.draft_confidence_stop(head["draft"], head["T"], mode, floor,
+                                                 out_num_draft=cnd, out_conf=cc,
+                                                 workspace=cws, stream=stream),
+                steps, 3, stream))
+            rows[f"confidence_{name}_b{B}_k{k}_v{V}_bf16"] = dict(
+                ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms),
+                frac=gbs(nb, ms) / peak, bytes=nb)
+        del cws, cnd, cc
 
     # bf16 Zipf workload: sampled + greedy (fits in L2: flushed before every launch)
     w = synth.WORKLOADS[1]

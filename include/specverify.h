@@ -1,7 +1,7 @@
 /*
  * specverify.h — C ABI of the speculative-decoding verify step on GB300 (sm_103a).
  *
- * Four device operations sit behind this boundary:
+ * Five device operations sit behind this boundary:
  *
  *   spec_verify_sample  the lossless modified-rejection verify: temperature softmax of the
  *                       target logits at k+1 positions and of the draft logits at k positions,
@@ -12,6 +12,8 @@
  *   spec_verify_greedy  the temperature-0 variant: accept while the draft token equals the
  *                       target argmax, then emit the target argmax.
  *   logit_gap_gate      top-1/top-2 logit-gap confidence gate over cached distributions.
+ *   draft_confidence_stop  variable-length drafting: the first draft position whose
+ *                       top probability (or inverse entropy) falls below a floor.
  *   ngram_propose       prompt-lookup n-gram draft proposer.
  *
  * General conventions (all entry points)
@@ -208,6 +210,48 @@ sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, int V, float
                          const int32_t* answer_set, int n_answer, int32_t* out_token,
                          float* out_gap, uint8_t* out_fire, void* workspace,
                          size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Draft-side confidence stop (variable-length drafting).
+ *
+ * Defined by: the "speculative-decoding-plan.md" design note, the variable-length drafting
+ * paragraph after "The acceptance math (standard speculative sampling)" (the draft keeps
+ * proposing while its own confidence stays above a floor, by top probability or an
+ * inverse-entropy gate, and stops early when it gets unsure; the accept loop is unchanged).
+ * The result feeds the num_draft argument of the verify calls.
+ *
+ * For request r, with n_in = num_draft[r] (k when num_draft is NULL) and
+ * q_i = softmax(draft[r, i, :] / T) for i < n_in:
+ *   SV_CONF_TOP_PROB:     c_i = max_j q_i(j)
+ *   SV_CONF_INV_ENTROPY:  c_i = 1 / H_i, H_i = -sum_j q_i(j) ln q_i(j) in nats (+inf if 0)
+ *   n_r = the first i < n_in with c_i < floor, else n_in.
+ * Rows at or past n_in are not read. Accuracy: the top probability to a few 1e-7 relative;
+ * H to a few 1e-7 nats absolute (the relative error of the fp32 exponentials), so 1/H to
+ * 1e-5 relative while H is above ~0.05 nats. A near-certain row gets a large 1/H, or +inf
+ * when the computed H is not positive.
+ * Arguments
+ *   draft_logits   [B, k, V] dtype.
+ *   num_draft      [B] int32 in [0, k], or NULL for k.
+ *   B, k, V        B >= 0 (0 is a no-op), 1 <= k <= SV_MAX_K, V >= 2, and
+ *                  B*k*ceil(V/S) < 2^31 (S as for spec_verify_sample).
+ *   temperature    T as for spec_verify_sample (the draft's own sampling temperature).
+ *   mode           SV_CONF_TOP_PROB or SV_CONF_INV_ENTROPY.
+ *   floor_val      the confidence floor (compared in double; any finite value).
+ *   out_num_draft  [B] int32: n_r, or -1 for a request with a data error (n_in outside
+ *                  [0, k], or a row it reads that holds NaN or +inf or is all -inf).
+ *   out_conf       [B, k] fp32 or NULL: c_i for i < n_in, 0 beyond, NaN on a data error.
+ *   workspace      >= draft_confidence_workspace(B, k, V, dtype) bytes (see the conventions).
+ * The pages' drafting loop stops generating at the first unsure position; here the draft
+ * logits of all k positions already exist, and one batched call finds that position.
+ * ---------------------------------------------------------------------------------------- */
+typedef enum { SV_CONF_TOP_PROB = 0, SV_CONF_INV_ENTROPY = 1 } sv_conf_mode;
+
+size_t draft_confidence_workspace(int B, int k, int V, sv_dtype dtype);
+sv_status draft_confidence_stop(const void* draft_logits, sv_dtype dtype,
+                                const int32_t* num_draft, int B, int k, int V,
+                                float temperature, sv_conf_mode mode, float floor_val,
+                                int32_t* out_num_draft, float* out_conf, void* workspace,
+                                size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Prompt-lookup n-gram proposer.

@@ -12,6 +12,8 @@ Calls (same names as the C ABI):
 - :func:`spec_verify_greedy` — greedy (temperature-0) verify.
 - :func:`spec_verify_greedy_noalloc` — the same without a workspace (fixed library scratch).
 - :func:`logit_gap_gate`     — top-1/top-2 logit-gap confidence gate.
+- :func:`draft_confidence_stop` — variable-length drafting: the first draft position whose
+  top probability (or inverse entropy) is below a floor.
 - :func:`ngram_propose`      — prompt-lookup n-gram draft proposer.
 
 Workspaces: pass ``workspace=`` (a uint8 CUDA tensor of at least the size the matching
@@ -33,11 +35,15 @@ __all__ = [
     "spec_verify_sample_workspace", "spec_verify_sample",
     "spec_verify_greedy_workspace", "spec_verify_greedy", "spec_verify_greedy_noalloc",
     "logit_gap_gate_workspace", "logit_gap_gate", "ngram_propose",
+    "SV_CONF_TOP_PROB", "SV_CONF_INV_ENTROPY", "draft_confidence_workspace",
+    "draft_confidence_stop",
 ]
 
 SV_F32 = 0
 SV_BF16 = 1
 SV_MAX_K = 16
+SV_CONF_TOP_PROB = 0
+SV_CONF_INV_ENTROPY = 1
 
 _STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
            4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT"}
@@ -253,6 +259,37 @@ def logit_gap_gate(logits, tau: float, answer_set=None, *, out_token=None, out_g
         _ptr(logits), code, N, V, float(tau), _ptr(answer_set), n_answer, _ptr(out_token),
         _ptr(out_gap), _ptr(out_fire), _ptr(ws), ws.numel(), h), "logit_gap_gate")
     return out_token, out_gap, out_fire
+
+
+# ------------------------------------------------------------------------------ confidence
+def draft_confidence_workspace(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().draft_confidence_workspace(B, k, V, dtype))
+
+
+def draft_confidence_stop(draft_logits, temperature: float, mode: int, floor: float,
+                          num_draft=None, *, out_num_draft=None, out_conf=None,
+                          want_conf: bool = True, workspace=None, stream=None):
+    """Variable-length drafting over draft logits [B, k, V]. Returns (num_draft [B] int32,
+    conf [B, k] fp32 or None)."""
+    B, k, V = draft_logits.shape
+    dev = draft_logits.device
+    code = _dtype_code(draft_logits)
+    _check_cuda("draft_logits", draft_logits)
+    _check_cuda("num_draft", num_draft, torch.int32, (B,), dev)
+    if out_num_draft is None:
+        out_num_draft = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_conf is None and want_conf:
+        out_conf = torch.empty((B, k), dtype=torch.float32, device=dev)
+    _check_cuda("out_num_draft", out_num_draft, torch.int32, (B,), dev)
+    _check_cuda("out_conf", out_conf, torch.float32, (B, k), dev)
+    h, st = _stream_handle(stream)
+    need = draft_confidence_workspace(B, k, V, code)
+    ws = workspace if workspace is not None else _workspace("conf", need, dev, st)
+    _ok(library().draft_confidence_stop(
+        _ptr(draft_logits), code, _ptr(num_draft), B, k, V, float(temperature), int(mode),
+        float(floor), _ptr(out_num_draft), _ptr(out_conf), _ptr(ws), ws.numel(), h),
+        "draft_confidence_stop")
+    return out_num_draft, out_conf
 
 
 # ------------------------------------------------------------------------------ n-gram

@@ -121,3 +121,7 @@ def _declare(L):
     L.logit_gap_gate.argtypes = [P, I, I, I, F, P, I, P, P, P, P, Z, P]
     L.ngram_propose.restype = I
     L.ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P]
+    L.draft_confidence_workspace.restype = Z
+    L.draft_confidence_workspace.argtypes = [I, I, I, I]
+    L.draft_confidence_stop.restype = I
+    L.draft_confidence_stop.argtypes = [P, I, P, I, I, I, F, I, F, P, P, P, Z, P]

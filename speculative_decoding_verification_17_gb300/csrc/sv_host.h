@@ -77,6 +77,26 @@ struct RowSoftmax {
   int pad[3];
 };
 
+// Confidence partial of one warp's share of a draft-row segment: S = hi + lo = sum of
+// 2^(z*s - K) and B = bhi + blo = sum of 2^(z*s - K) * (z*s - K) (the entropy's moment; 0
+// in the top-probability variant), with the integer reference K, and the largest logit m.
+// K = -inf: no finite logit; K = NaN: poisoned.
+struct ConfPartial {
+  float K, m;
+  float hi, lo;
+  float bhi, blo;
+  float pad[2];
+};
+
+// Merged statistics of one draft row for the confidence stop (in units of 2^K).
+struct ConfRow {
+  double S;
+  double Bm;   // the entropy's moment
+  float K, m;  // the row's reference and largest logit
+  int status;  // 0 ok, 1 not a distribution
+  int pad;
+};
+
 struct WarpArgmax {
   float v;  // largest logit of the warp's share
   int idx;  // its lowest index; kNoIndex when the share holds no comparable logit, -2 poisoned
@@ -119,6 +139,23 @@ inline GreedyLayout greedy_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpArgmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(int), 256);
+  L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
+  L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
+  L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);
+  L.total = o;
+  return L;
+}
+
+struct ConfLayout {
+  size_t part, row, ctl, row_cnt, req_cnt, total;
+};
+inline ConfLayout conf_layout(int B, int k, int V, sv_dtype d) {
+  const size_t R = static_cast<size_t>(k);
+  const size_t nseg = static_cast<size_t>(num_segments(num_chunks(V, d)));
+  ConfLayout L{};
+  size_t o = 0;
+  L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(ConfPartial), 256);
+  L.row = o;     o = round_up(o + B * R * sizeof(ConfRow), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);

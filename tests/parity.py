@@ -73,3 +73,51 @@ def compare_gate(token, gap, fire, orc) -> int:
     keep = orc["flag"] == 0
     assert np.array_equal(fire[keep], orc["fire"][keep]), "gate decisions differ"
     return int((~keep).sum())
+
+
+def compare_confidence(nd, conf, nin, orc, floor: float, mode: int, requests,
+                       rel: float = 1e-5, h_abs: float = 5e-7) -> dict:
+    """Draft-confidence stop. nd [B] and conf [B, k] from the CUDA path, nin [B] the input
+    draft counts. Top probabilities agree within ``rel``; for the inverse entropy, H = 1/c
+    agrees within rel * H + h_abs nats (the CUDA path's H carries an absolute error of a few
+    1e-7 nats from its fp32 exponentials, see the library header). The stop agrees exactly
+    unless a position up to the oracle's stop is a near tie (the oracle's flag, or a
+    confidence within this tolerance of the floor) at f; then the CUDA stop is at least f
+    and is the first position whose own confidence is below the floor."""
+    stats = dict(requests=0, flagged=0, errors=0, max_rel=0.0)
+
+    def inv(c):
+        return 0.0 if c == np.inf else 1.0 / c
+
+    for r in requests:
+        stats["requests"] += 1
+        on = int(orc["num_draft"][r])
+        if on == -1:
+            stats["errors"] += 1
+            assert nd[r] == -1, (r, nd[r])
+            assert np.isnan(conf[r]).all(), r
+            continue
+        n = int(nin[r])
+        assert (conf[r, n:] == 0).all(), r
+        f = int(orc["flag"][r])
+        for i in range(n):
+            g, o = float(conf[r, i]), float(orc["conf"][r, i])
+            if mode == 0:
+                err = abs(g - o) / o
+                assert err <= rel, (r, i, g, o)
+                tie = abs(o - floor) <= rel * max(o, floor)
+            else:
+                hg, ho = inv(g), inv(o)
+                err = abs(hg - ho) / ho if ho > 0 else 0.0
+                assert abs(hg - ho) <= rel * ho + h_abs, (r, i, g, o)
+                tie = abs(ho - inv(floor)) <= rel * ho + h_abs
+            stats["max_rel"] = max(stats["max_rel"], err)
+            if tie and i <= on and (f == -1 or i < f):
+                f = i
+        if f == -1:
+            assert nd[r] == on, (r, nd[r], on)
+        else:
+            stats["flagged"] += 1
+            below = [i for i in range(n) if conf[r, i] < floor]
+            assert nd[r] >= f and nd[r] == (below[0] if below else n), (r, nd[r], f)
+    return stats

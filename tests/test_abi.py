@@ -101,6 +101,23 @@ def test_greedy_gate_ngram_validation():
     assert ng(B=0, h=None) == OK
 
 
+def test_confidence_stop_validation():
+    L = sv.library()
+    ws = ctypes.c_void_p(0x100000)
+    dc = lambda **kw: L.draft_confidence_stop(
+        kw.get("z", FAKE), kw.get("dtype", 1), None, kw.get("B", 4), kw.get("k", 5),
+        kw.get("V", 1000), kw.get("T", 1.0), kw.get("mode", 0), kw.get("floor", 0.5),
+        kw.get("out", FAKE), None, kw.get("ws", ws), kw.get("wsb", 1 << 30), None)
+    assert dc(B=-1) == INVALID and dc(k=0) == INVALID and dc(V=1) == INVALID
+    assert dc(dtype=7) == INVALID and dc(T=0.0) == INVALID and dc(mode=2) == INVALID
+    assert dc(floor=float("nan")) == INVALID and dc(floor=float("inf")) == INVALID
+    assert dc(k=17) == UNSUPPORTED and dc(z=None) == INVALID and dc(out=None) == INVALID
+    assert dc(wsb=8) == WORKSPACE and dc(ws=None) == WORKSPACE
+    assert dc(B=0, z=None) == OK
+    assert L.draft_confidence_workspace(4, 5, 1000, 1) > 0
+    assert L.draft_confidence_workspace(4, 17, 1000, 1) == 0
+
+
 def test_binding_raises_on_bad_input():
     import torch
 
