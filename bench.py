@@ -47,12 +47,30 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest() -> str:
+def source_digest(unit: str = "sv_verify.cu") -> str:
+    """sha256 prefix of what the profiled kernel is built from: its translation unit, every
+    header it includes from the package or `include/` (recursively), and the build script
+    that holds the compiler flags."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_17_gb300")
+    dirs = [os.path.join(pkg, "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = [], [unit]
+    while todo:
+        name = todo.pop(0)
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs
+                     if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            continue
+        seen.append(name)
+        todo += re.findall(r'^#include "([^"]+)"', open(path).read(), re.M)
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_decoding_verification_17_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for name in sorted(seen):
+        path = next(os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name)))
+        with open(path, "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(pkg, "_native.py"), "rb") as f:
+        h.update(b"_native.py\0" + f.read())
     return h.hexdigest()[:16]
 
 

@@ -16,7 +16,7 @@
 // 0..k-1) and k+1 in the greedy verify. Units of rows a request does not need (past its n_r)
 // exit at once.
 //
-//  pass 1 (each lane, over its share of the segment)  per chunk the lane maximum m, the
+//  pass 1 (each lane, over its share of the segment)  per ring stage the lane maximum m, the
 //                           integer-valued reference K = ceil(m*s) with s = log2(e)/T in
 //                           fp32 and the sum of 2^(z*s - K) in fp32, folded into a running
 //                           compensated pair; per segment one warp reduction to a partial
