@@ -59,9 +59,17 @@ def _bind(lib):
     lib.oracle_logit_gap_gate.argtypes = [P, I, I, I, D, P, I, P, P, P, P, I, I]
     lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, I, I]
     lib.oracle_draft_confidence.argtypes = [P, I, P, I, I, I, D, I, D, P, P, P, I, I]
+    lib.oracle_wilson.argtypes = [ctypes.c_int64, ctypes.c_int64, D, P, P]
+    lib.oracle_wilson.restype = None
+    lib.oracle_risk_coverage.argtypes = [P, P, P, I, P, I, P, I, D, D, P, P, P, P]
+    lib.oracle_conformal_residual.argtypes = [P, P, I, I, I, P, I, I]
+    lib.oracle_conformal_quantile.argtypes = [P, I, D, P]
+    lib.oracle_conformal_admit.argtypes = [P, I, I, I, I, P, P, P, P, P, I, I]
     for f in (lib.oracle_row_softmax, lib.oracle_spec_verify_sample,
               lib.oracle_spec_verify_greedy, lib.oracle_logit_gap_gate,
-              lib.oracle_ngram_propose, lib.oracle_draft_confidence):
+              lib.oracle_ngram_propose, lib.oracle_draft_confidence,
+              lib.oracle_risk_coverage, lib.oracle_conformal_residual,
+              lib.oracle_conformal_quantile, lib.oracle_conformal_admit):
         f.restype = ctypes.c_int
     return lib
 
@@ -331,4 +339,85 @@ def ngram_propose(history, hist_len, n_max: int, n_min: int, k: int, requests=No
                                         _ptr(out["draft"]), _ptr(out["num_draft"]), a, b)
 
     _run(fn, _ranges(reqs, threads), threads)
+    return out
+
+
+# ------------------------------------------------------------------------ gate calibration
+def wilson(k: int, n: int, z: float = 1.959963984540054) -> tuple[float, float]:
+    """Wilson score interval of k successes in n trials (see oracle.h)."""
+    lo, hi = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_wilson(int(k), int(n), float(z), ctypes.byref(lo), ctypes.byref(hi))
+    return lo.value, hi.value
+
+
+def risk_coverage(gap, token, full_token, answer_set, taus, z: float = 1.959963984540054,
+                  r_max: float = 0.0) -> dict:
+    """Coverage c(tau) and false-accept risk r(tau) with Wilson intervals over a threshold
+    grid, and the index of the smallest tau with r <= r_max (-1 if none)."""
+    g = _f32(gap).reshape(-1)
+    t = _i32(token).reshape(-1)
+    f = _i32(full_token).reshape(-1)
+    A = _i32(answer_set if answer_set is not None else np.zeros(0, np.int32)).reshape(-1)
+    tau = _f32(taus).reshape(-1)
+    N, T = g.size, tau.size
+    assert t.size == N and f.size == N
+    acc = np.zeros(T, np.int64)
+    bad = np.zeros(T, np.int64)
+    st = np.zeros((T, 6), np.float64)
+    idx = ctypes.c_int32(-3)
+    rc = _load().oracle_risk_coverage(_ptr(g), _ptr(t), _ptr(f), N, _ptr(A), A.size, _ptr(tau),
+                                      T, float(z), float(r_max), _ptr(acc), _ptr(bad), _ptr(st),
+                                      ctypes.byref(idx))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return dict(accepted=acc, wrong=bad, coverage=st[:, 0], cov_lo=st[:, 1], cov_hi=st[:, 2],
+                risk=st[:, 3], risk_lo=st[:, 4], risk_hi=st[:, 5], tau_index=idx.value)
+
+
+def conformal_residual(draft, truth, rows=None, threads: int = 1) -> np.ndarray:
+    """Sup-norm residual of each draft row against the true row, fp32 [N] (see oracle.h)."""
+    a, code = as_logits(draft)
+    b, code_b = as_logits(truth)
+    assert code == code_b and a.shape == b.shape
+    a = a.reshape(-1, a.shape[-1])
+    b = b.reshape(-1, b.shape[-1])
+    N, V = a.shape
+    out = np.full(N, np.nan, np.float32)
+    lib = _load()
+    idx = sorted(range(N) if rows is None else {int(r) for r in rows})
+
+    def fn(i0, i1):
+        return lib.oracle_conformal_residual(_ptr(a), _ptr(b), code, N, V, _ptr(out), i0, i1)
+
+    _run(fn, _ranges(idx, threads), threads)
+    return out
+
+
+def conformal_quantile(r, q: float) -> np.float32:
+    """The ceil((n+1) q)-th smallest residual, +inf past n (see oracle.h)."""
+    x = _f32(r).reshape(-1)
+    out = np.zeros(1, np.float32)
+    rc = _load().oracle_conformal_quantile(_ptr(x), x.size, float(q), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out[0]
+
+
+def conformal_admit(logits, Q, steps=None, threads: int = 1) -> dict:
+    """Earliest layer whose 2 Q[k] <= gamma over logits [N, K, V] (see oracle.h)."""
+    z, code = as_logits(logits)
+    N, K, V = z.shape
+    q = _f32(Q).reshape(-1)
+    assert q.size == K
+    out = dict(layer=np.full(N, -2, np.int32), token=np.full(N, -2, np.int32),
+               gap=np.full((N, K), np.nan), flag=np.full(N, -2, np.int32))
+    lib = _load()
+    idx = sorted(range(N) if steps is None else {int(r) for r in steps})
+
+    def fn(a, b):
+        return lib.oracle_conformal_admit(_ptr(z), code, N, K, V, _ptr(q), _ptr(out["layer"]),
+                                          _ptr(out["token"]), _ptr(out["gap"]),
+                                          _ptr(out["flag"]), a, b)
+
+    _run(fn, _ranges(idx, threads), threads)
     return out

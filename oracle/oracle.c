@@ -24,6 +24,11 @@
  *  - Draft-confidence stop: the "speculative-decoding-plan.md" design note, the
  *    variable-length drafting paragraph (keep drafting while the draft's top probability, or
  *    the inverse of its entropy, stays above a floor).
+ *  - Gate calibration: "Speculative Pre-Positioning", section 2.4, Eq. (13) and Eq. (14)
+ *    (coverage and false-accept risk of the gate as tau sweeps; calibration takes the
+ *    smallest tau whose risk meets a budget) and section 4 (Wilson 95 % intervals); the
+ *    "speculative-decoding-plan.md" conformal gate (sup-norm residual, its conformal
+ *    q-quantile Q, admit iff 2 Q <= gamma, per layer the earliest admitting one).
  *  - N-gram proposer: "The Inference Wall, Part 7", section "What S is in this experiment,
  *    and what 'ngram' actually means" (four-word phrase first, then three, then two; copy
  *    what followed the phrase; nothing earlier means no proposal).
@@ -420,6 +425,150 @@ int oracle_logit_gap_gate(const void* logits, int dtype, int N, int V, double ta
     out_gap[row] = gap;
     out_fire[row] = (uint8_t)((gap > tau) && in_answer_set(answer_set, n_answer, ahat));
     if (out_flag) out_flag[row] = (uint8_t)(fabs(gap - tau) < ORACLE_TIE_MARGIN);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------- gate calibration */
+
+void oracle_wilson(int64_t k, int64_t n, double z, double* lo, double* hi) {
+  if (n <= 0) {
+    *lo = NAN;
+    *hi = NAN;
+    return;
+  }
+  const double nn = (double)n;
+  const double p = (double)k / nn;
+  const double z2 = z * z;
+  const double denom = 1.0 + z2 / nn;
+  const double centre = (p + z2 / (2.0 * nn)) / denom;
+  const double half = z / denom * sqrt(p * (1.0 - p) / nn + z2 / (4.0 * nn * nn));
+  double a = centre - half, b = centre + half;
+  if (a < 0.0) a = 0.0;
+  if (b > 1.0) b = 1.0;
+  *lo = a;
+  *hi = b;
+}
+
+int oracle_risk_coverage(const float* gap, const int32_t* token, const int32_t* full_token,
+                         int N, const int32_t* answer_set, int n_answer, const float* taus,
+                         int T, double z, double r_max, int64_t* accepted, int64_t* wrong,
+                         double* stats, int32_t* tau_index) {
+  if (N < 0 || T < 1 || n_answer < 0 || !taus || !accepted || !wrong || !stats || !tau_index)
+    return -1;
+  if (N > 0 && (!gap || !token || !full_token)) return -1;
+  for (int t = 0; t < T; ++t) {
+    if (isnan(taus[t])) return -1;
+    if (t > 0 && taus[t] < taus[t - 1]) return -1;
+  }
+  *tau_index = -1;
+  /* Eq. (13) and Eq. (14), one threshold at a time, straight from the definitions. */
+  for (int t = 0; t < T; ++t) {
+    const double tau = (double)taus[t];
+    int64_t acc = 0, bad = 0;
+    for (int i = 0; i < N; ++i) {
+      const double g = (double)gap[i];
+      if (!(g > tau)) continue;
+      if (!in_answer_set(answer_set, n_answer, token[i])) continue;
+      ++acc;
+      if (token[i] != full_token[i]) ++bad;
+    }
+    accepted[t] = acc;
+    wrong[t] = bad;
+    double* st = stats + 6 * (size_t)t;
+    st[0] = N > 0 ? (double)acc / (double)N : NAN;
+    oracle_wilson(acc, N, z, &st[1], &st[2]);
+    if (acc > 0) {
+      st[3] = (double)bad / (double)acc;
+      oracle_wilson(bad, acc, z, &st[4], &st[5]);
+    } else {
+      st[3] = st[4] = st[5] = NAN;
+    }
+    if (*tau_index < 0 && acc > 0 && st[3] <= r_max) *tau_index = t;
+  }
+  return 0;
+}
+
+int oracle_conformal_residual(const void* draft, const void* truth, int dtype, int N, int V,
+                              float* out, int i0, int i1) {
+  if (N < 0 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
+  if (i0 < 0 || i1 > N || i0 > i1) return -1;
+  if (i0 == i1) return 0;
+  if (!draft || !truth || !out) return -1;
+  for (int i = i0; i < i1; ++i) {
+    const size_t off = (size_t)i * (size_t)V;
+    double r = 0.0;
+    int nan = 0;
+    for (int j = 0; j < V; ++j) {
+      const double a = logit_at(draft, dtype, off + (size_t)j);
+      const double b = logit_at(truth, dtype, off + (size_t)j);
+      if (isnan(a) || isnan(b)) {
+        nan = 1;
+        break;
+      }
+      const double d = a == b ? 0.0 : fabs(a - b);
+      if (d > r) r = d;
+    }
+    out[i] = nan ? NAN : (float)r;
+  }
+  return 0;
+}
+
+/* Ascending order with every NaN after +inf. */
+static int cmp_nan_last(const void* x, const void* y) {
+  const float a = *(const float*)x, b = *(const float*)y;
+  const int na = isnan(a), nb = isnan(b);
+  if (na || nb) return na - nb;
+  return (a > b) - (a < b);
+}
+
+int oracle_conformal_quantile(const float* r, int n, double q, float* out_q) {
+  if (n < 1 || !r || !out_q || !(q > 0.0) || !(q <= 1.0)) return -1;
+  const double rank = ceil((double)(n + 1) * q);
+  if (rank > (double)n) {
+    *out_q = INFINITY;
+    return 0;
+  }
+  float* s = (float*)malloc(sizeof(float) * (size_t)n);
+  if (!s) return -1;
+  memcpy(s, r, sizeof(float) * (size_t)n);
+  qsort(s, (size_t)n, sizeof(float), cmp_nan_last);
+  *out_q = s[(size_t)rank - 1];
+  free(s);
+  return 0;
+}
+
+int oracle_conformal_admit(const void* logits, int dtype, int N, int K, int V, const float* Q,
+                           int32_t* out_layer, int32_t* out_token, double* out_gap,
+                           int32_t* out_flag, int n0, int n1) {
+  if (N < 0 || K < 1 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  if (n0 < 0 || n1 > N || n0 > n1) return -1;
+  if (n0 == n1) return 0;
+  if (!logits || !Q || !out_layer || !out_token) return -1;
+  for (int n = n0; n < n1; ++n) {
+    int layer = K, tok = -1, flag = -1;
+    for (int k = 0; k < K; ++k) {
+      int32_t ahat;
+      double gamma;
+      uint8_t fire, tie;
+      const int row = n * K + k;
+      /* gamma and a_hat of the row exactly as the gate defines them (no answer set) */
+      if (oracle_logit_gap_gate((const char*)logits + (size_t)row * (size_t)V *
+                                                          (dtype == 0 ? 4u : 2u),
+                                dtype, 1, V, 0.0, NULL, 0, &ahat, &gamma, &fire, &tie, 0, 1))
+        return -1;
+      if (out_gap) out_gap[row] = gamma;
+      const double thr = 2.0 * (double)Q[k];
+      if (layer == K && flag < 0 && !isnan(gamma) && fabs(gamma - thr) < ORACLE_TIE_MARGIN)
+        flag = k;
+      if (layer == K && !isnan(gamma) && thr <= gamma) {
+        layer = k;
+        tok = ahat;
+      }
+    }
+    out_layer[n] = layer;
+    out_token[n] = tok;
+    if (out_flag) out_flag[n] = flag;
   }
   return 0;
 }

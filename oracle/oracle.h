@@ -82,6 +82,56 @@ int oracle_draft_confidence(const void* draft, int dtype, const int32_t* num_dra
                             int32_t* out_num_draft, double* out_conf, int32_t* out_flag,
                             int r0, int r1);
 
+/* ---- Gate calibration ("Speculative Pre-Positioning", section 2.4, Eq. (13) coverage and
+ * Eq. (14) false-accept risk, the calibration "smallest tau with r(tau) <= r_max", and the
+ * Wilson 95 % intervals reported with them in section 4, Figures 6 and 7) ---- */
+
+/* Wilson score interval of k successes in n trials at the normal quantile z:
+ *   centre = (k/n + z^2 / (2n)) / (1 + z^2 / n)
+ *   half   = z / (1 + z^2 / n) * sqrt((k/n)(1 - k/n) / n + z^2 / (4 n^2))
+ * lo = centre - half and hi = centre + half, clamped to [0, 1]; both NaN when n = 0. */
+void oracle_wilson(int64_t k, int64_t n, double z, double* lo, double* hi);
+
+/* Risk-coverage sweep over the thresholds taus[0..T) (non-decreasing, no NaN). For each t:
+ *   accepted[t] = #{i : gap[i] > taus[t] and token[i] in A}   (compared in double; a NaN gap
+ *                 is never accepted; answer_set sorted ascending)
+ *   wrong[t]    = #{accepted i : token[i] != full_token[i]}   (the served token disagrees with
+ *                 the model's own full-path output)
+ *   stats[6t..6t+5] = coverage accepted/N, its Wilson interval, risk wrong/accepted, its
+ *                 Wilson interval (the risk and its interval NaN when accepted = 0).
+ * *tau_index = the smallest t with accepted[t] > 0 and risk <= r_max, else -1.
+ * Returns -1 on bad arguments (taus unsorted or NaN, N < 0, T < 1). */
+int oracle_risk_coverage(const float* gap, const int32_t* token, const int32_t* full_token,
+                         int N, const int32_t* answer_set, int n_answer, const float* taus,
+                         int T, double z, double r_max, int64_t* accepted, int64_t* wrong,
+                         double* stats, int32_t* tau_index);
+
+/* Conformal residual of draft logits against the true ones ("speculative-decoding-plan.md",
+ * the conformal 2 tau <= gamma gate: a draft within tau of the truth in sup-norm cannot flip
+ * an argmax whose runner-up margin is at least 2 tau). Row i of [N, V]:
+ *   r_i = max_j d_j, d_j = 0 where the two logits are equal (a token masked, -inf, in both
+ *         included), |draft_j - truth_j| elsewhere (+inf where only one is masked);
+ *   NaN when either row holds a NaN. Evaluated in double, stored rounded to fp32. */
+int oracle_conformal_residual(const void* draft, const void* truth, int dtype, int N, int V,
+                              float* out, int i0, int i1);
+
+/* Split-conformal quantile of n calibration residuals: Q = the ceil((n + 1) q)-th smallest
+ * (ranks from 1; NaN orders above +inf), +inf when that rank exceeds n; the rank is computed
+ * as ceil((double)(n + 1) * q). q in (0, 1], n >= 1. */
+int oracle_conformal_quantile(const float* r, int n, double q, float* out_q);
+
+/* Conformal admission over K layers: logits [N, K, V] (row n*K + k is step n's early-exit
+ * logits at layer k), Q[K] the calibrated quantile of each layer.
+ *   gamma_{n,k}, a_hat_{n,k} as in oracle_logit_gap_gate (double; NaN for an all-NaN row);
+ *   admit_{n,k} = 2 Q[k] <= gamma_{n,k} (in double; a NaN gamma never admits);
+ *   out_layer[n] = the first admitted k, else K; out_token[n] = a_hat at that layer, else -1;
+ *   out_gap[n*K + k] = gamma_{n,k} (may be NULL);
+ *   out_flag[n] = the first k <= out_layer[n] (k < K) with |gamma - 2 Q[k]| <
+ *                 ORACLE_TIE_MARGIN, else -1 (may be NULL). Steps [n0, n1). */
+int oracle_conformal_admit(const void* logits, int dtype, int N, int K, int V, const float* Q,
+                           int32_t* out_layer, int32_t* out_token, double* out_gap,
+                           int32_t* out_flag, int n0, int n1);
+
 /* Prompt-lookup n-gram proposer; outputs as the library's ngram_propose. */
 int oracle_ngram_propose(const int32_t* history, const int32_t* hist_len, int B, int L_max,
                          int n_max, int n_min, int k, int32_t* out_draft,

@@ -11,6 +11,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_calibration as K
 import test_oracle_confidence as C
 import test_oracle_rules as R
 import test_oracle_sample as S
@@ -71,6 +72,30 @@ MUTANTS = [
       lambda: C.test_random_rows_match_scipy(1.0)]),
     ("draft count ignored", "const int n_in = num_draft ? num_draft[r] : k;",
      "const int n_in = k;", [C.test_stop_respects_the_input_draft_count]),
+    ("Wilson half-width without the z^2/(4n^2) term",
+     "sqrt(p * (1.0 - p) / nn + z2 / (4.0 * nn * nn))", "sqrt(p * (1.0 - p) / nn)",
+     [K.test_wilson_matches_the_pages_printed_intervals,
+      lambda: K.test_wilson_matches_scipy(0, 37)]),
+    ("risk over all decision points", "st[3] = (double)bad / (double)acc;",
+     "st[3] = (double)bad / (double)N;", [K.test_the_pages_operating_point]),
+    ("gate calibration accepts gap == tau", "if (!(g > tau)) continue;",
+     "if (!(g >= tau)) continue;", [K.test_the_pages_operating_point,
+                                     K.test_sweep_matches_sort_and_count]),
+    ("calibration ignores the answer set",
+     "if (!in_answer_set(answer_set, n_answer, token[i])) continue;", "",
+     [K.test_the_pages_operating_point]),
+    ("calibration keeps the last qualifying tau", "if (*tau_index < 0 && acc > 0",
+     "if (acc > 0", [K.test_selection_picks_the_smallest_qualifying_tau_not_a_monotone_one]),
+    ("conformal rank without the +1", "ceil((double)(n + 1) * q)", "ceil((double)n * q)",
+     [K.test_quantile_rank_rule_and_edges,
+      lambda: K.test_quantile_has_the_split_conformal_coverage(19, 0.9)]),
+    ("residual without the absolute value", "a == b ? 0.0 : fabs(a - b)", "a == b ? 0.0 : a - b",
+     [K.test_residual_hand_built_rows,
+      K.test_residual_bounds_the_argmax_no_flip_theorem]),
+    ("conformal admission without the factor 2", "const double thr = 2.0 * (double)Q[k];",
+     "const double thr = (double)Q[k];", [K.test_admit_takes_the_earliest_admitting_layer]),
+    ("conformal admission keeps the last layer", "if (layer == K && !isnan(gamma) && thr <= gamma)",
+     "if (!isnan(gamma) && thr <= gamma)", [K.test_admit_takes_the_earliest_admitting_layer]),
 ]
 
 
