@@ -7,8 +7,10 @@ The metric is verified draft positions per second (sum of n_r per step / step ti
 the logit bandwidth (each needed logit read once) against the measured HBM peak.
 
 Secondary rows time the other calls of the hot path on their own workloads (greedy verify,
-logit-gap gate, n-gram proposal + greedy verify, the fp32 sampled verify) with the same
-event timing; workloads that fit in L2 get an L2 flush before every timed launch.
+logit-gap gate, n-gram proposal + greedy verify, the fp32 sampled verify, the draft
+confidence stop, the gate calibration sweep and the conformal residual, quantile and gate)
+with the same event timing; workloads that fit in L2 get an L2 flush before every timed
+launch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 Under torchrun every rank runs its own replica of the batch (request sharding, no
@@ -485,6 +487,65 @@ def secondary_rows(args, dev, stream, peak, head=None):
                 ms=ms, positions_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms),
                 frac=gbs(nb, ms) / peak, bytes=nb)
         del cws, cnd, cc
+        # conformal residual of the draft rows against the target rows at the same positions
+        tgt = head["target"][:, :k].contiguous()
+        rr = torch.empty((B * k,), dtype=torch.float32, device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: sv.conformal_residual(head["draft"], tgt, out_resid=rr, stream=stream),
+            steps, 3, stream))
+        nb = 2 * B * k * V * 2
+        rows[f"conformal_residual_b{B}_k{k}_v{V}_bf16"] = dict(
+            ms=ms, rows_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+            bytes=nb)
+        del tgt, rr
+        # conformal gate over K = 4 layers of 256 steps (the first 1024 target rows seen as
+        # [256, 4, V])
+        z4 = head["target"].reshape(-1, V)[: 256 * 4].reshape(256, 4, V)
+        Q4 = torch.tensor([3.0, 2.0, 1.5, 1.0], dtype=torch.float32, device=dev)
+        aws = torch.zeros(sv.conformal_admit_workspace(256, 4, V, sv.SV_BF16), dtype=torch.uint8,
+                          device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: sv.conformal_admit(z4, Q4, want_gap=False, workspace=aws, stream=stream),
+            steps, 3, stream))
+        nb = 256 * 4 * V * 2
+        rows[f"conformal_admit_n256_k4_v{V}_bf16"] = dict(
+            ms=ms, steps_per_s=256 / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+            bytes=nb)
+        del z4, aws
+
+    # gate calibration: risk-coverage sweep over 16M decision points and 1024 thresholds
+    # (201 MB of inputs, past L2), and at the pre-positioning page's 128 points
+    g = torch.Generator(device=dev).manual_seed(5)
+    for npts, T, tag in ((1 << 24, 1024, "n16m_t1024"), (128, 64, "n128_t64")):
+        gp = torch.rand((npts,), generator=g, device=dev) * 8
+        tk = torch.randint(0, 64, (npts,), generator=g, device=dev, dtype=torch.int32)
+        fl = torch.where(torch.rand((npts,), generator=g, device=dev) < 0.9, tk, tk + 1)
+        A = torch.arange(0, 64, 2, dtype=torch.int32, device=dev)
+        taus = torch.linspace(0, 8, T, device=dev)
+        sws = torch.zeros(sv.gate_risk_coverage_workspace(npts, T), dtype=torch.uint8,
+                          device=dev)
+        pts = torch.empty((T, 8), dtype=torch.float64, device=dev)
+        ti = torch.empty((1,), dtype=torch.int32, device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: sv.gate_risk_coverage(gp, tk, fl, A, taus, 1.959964, 0.1, out_points=pts,
+                                          out_tau_index=ti, workspace=sws, stream=stream),
+            steps, 3, stream, flush if npts < (1 << 20) else None))
+        nb = npts * 12
+        rows[f"gate_risk_coverage_{tag}"] = dict(
+            ms=ms, points_per_s=npts / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+            bytes=nb)
+        del gp, tk, fl, sws, pts, ti
+    # split-conformal quantile of 16M scores (64 MB, three radix passes) and of 4096
+    for n, tag in ((1 << 24, "n16m"), (4096, "n4096")):
+        rs = torch.rand((n,), generator=g, device=dev)
+        qws = torch.zeros(sv.conformal_quantile_workspace(n), dtype=torch.uint8, device=dev)
+        qo = torch.empty((1,), dtype=torch.float32, device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: sv.conformal_quantile(rs, 0.9, out_q=qo, workspace=qws, stream=stream),
+            steps, 3, stream, flush))
+        rows[f"conformal_quantile_{tag}"] = dict(ms=ms, scores_per_s=n / (ms * 1e-3),
+                                                 gbs=gbs(3 * n * 4, ms), bytes=3 * n * 4)
+        del rs, qws, qo
 
     # bf16 Zipf workload: sampled + greedy (fits in L2: flushed before every launch)
     w = synth.WORKLOADS[1]

@@ -16,6 +16,14 @@ Calls (same names as the C ABI):
   top probability (or inverse entropy) is below a floor.
 - :func:`ngram_propose`      — prompt-lookup n-gram draft proposer.
 
+Gate calibration and the conformal gate (C ABI in ``include/specverify_calib.h``):
+
+- :func:`gate_risk_coverage` — coverage and false-accept risk of the gate over a threshold
+  grid, with Wilson intervals, and the smallest threshold within a risk budget.
+- :func:`conformal_residual` — sup-norm distance of draft rows from the true rows.
+- :func:`conformal_quantile` — the split-conformal quantile of those residuals.
+- :func:`conformal_admit`    — the earliest of K layers whose gap clears 2 Q.
+
 Workspaces: pass ``workspace=`` (a uint8 CUDA tensor of at least the size the matching
 ``*_workspace`` query returns, 256-byte aligned, not shared by calls in flight at the same
 time; it needs no initialisation), or let the binding keep one cached per (device, call)
@@ -36,7 +44,9 @@ __all__ = [
     "spec_verify_greedy_workspace", "spec_verify_greedy", "spec_verify_greedy_noalloc",
     "logit_gap_gate_workspace", "logit_gap_gate", "ngram_propose",
     "SV_CONF_TOP_PROB", "SV_CONF_INV_ENTROPY", "draft_confidence_workspace",
-    "draft_confidence_stop",
+    "draft_confidence_stop", "SV_MAX_TAUS", "CALIB_POINT", "gate_risk_coverage_workspace",
+    "gate_risk_coverage", "conformal_residual", "conformal_quantile_workspace",
+    "conformal_quantile", "conformal_admit_workspace", "conformal_admit", "gate_points_dict",
 ]
 
 SV_F32 = 0
@@ -44,6 +54,11 @@ SV_BF16 = 1
 SV_MAX_K = 16
 SV_CONF_TOP_PROB = 0
 SV_CONF_INV_ENTROPY = 1
+SV_MAX_TAUS = 4096
+# sv_calib_point as a row of 8 float64-sized fields: the two counts are int64, the six rates
+# float64 (view the int64 columns with .view(torch.int64)).
+CALIB_POINT = ("accepted", "wrong", "coverage", "cov_lo", "cov_hi", "risk", "risk_lo",
+               "risk_hi")
 
 _STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
            4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT"}
@@ -259,6 +274,120 @@ def logit_gap_gate(logits, tau: float, answer_set=None, *, out_token=None, out_g
         _ptr(logits), code, N, V, float(tau), _ptr(answer_set), n_answer, _ptr(out_token),
         _ptr(out_gap), _ptr(out_fire), _ptr(ws), ws.numel(), h), "logit_gap_gate")
     return out_token, out_gap, out_fire
+
+
+# ------------------------------------------------------------------------ gate calibration
+def gate_risk_coverage_workspace(N: int, T: int) -> int:
+    return int(library().gate_risk_coverage_workspace(N, T))
+
+
+def gate_risk_coverage(gap, token, full_token, answer_set, taus, z: float = 1.959963984540054,
+                       r_max: float = 0.0, *, out_points=None, out_tau_index=None,
+                       workspace=None, stream=None):
+    """Risk-coverage sweep. Returns (points [T, 8] float64 whose columns are CALIB_POINT, the
+    first two holding int64 bits, tau_index [1] int32). ``gate_points_dict`` unpacks them."""
+    N = gap.numel()
+    T = taus.numel()
+    dev = gap.device
+    _check_cuda("gap", gap, torch.float32, (N,), dev)
+    _check_cuda("token", token, torch.int32, (N,), dev)
+    _check_cuda("full_token", full_token, torch.int32, (N,), dev)
+    _check_cuda("taus", taus, torch.float32, (T,), dev)
+    if answer_set is not None:
+        _check_cuda("answer_set", answer_set, torch.int32, None, dev)
+    n_answer = 0 if answer_set is None else answer_set.numel()
+    if out_points is None:
+        out_points = torch.empty((T, 8), dtype=torch.float64, device=dev)
+    if out_tau_index is None:
+        out_tau_index = torch.empty((1,), dtype=torch.int32, device=dev)
+    _check_cuda("out_points", out_points, torch.float64, (T, 8), dev)
+    _check_cuda("out_tau_index", out_tau_index, torch.int32, (1,), dev)
+    h, st = _stream_handle(stream)
+    need = gate_risk_coverage_workspace(N, T)
+    ws = workspace if workspace is not None else _workspace("sweep", need, dev, st)
+    _ok(library().gate_risk_coverage(
+        _ptr(gap), _ptr(token), _ptr(full_token), N, _ptr(answer_set), n_answer, _ptr(taus), T,
+        float(z), float(r_max), _ptr(out_points), _ptr(out_tau_index), _ptr(ws), ws.numel(), h),
+        "gate_risk_coverage")
+    return out_points, out_tau_index
+
+
+def gate_points_dict(points) -> dict:
+    """Columns of gate_risk_coverage's points as CPU tensors (counts as int64)."""
+    p = points.detach().cpu()
+    out = {}
+    for i, name in enumerate(CALIB_POINT):
+        col = p[:, i].contiguous()
+        out[name] = col.view(torch.int64) if i < 2 else col
+    return out
+
+
+def conformal_residual(draft_logits, true_logits, *, out_resid=None, stream=None):
+    """Sup-norm residual of each draft row [..., V] against the true row. Returns [N] fp32."""
+    V = draft_logits.shape[-1]
+    N = draft_logits.numel() // V if V else 0
+    dev = draft_logits.device
+    code = _dtype_code(draft_logits)
+    _check_cuda("draft_logits", draft_logits)
+    _check_cuda("true_logits", true_logits, draft_logits.dtype, tuple(draft_logits.shape), dev)
+    if out_resid is None:
+        out_resid = torch.empty((N,), dtype=torch.float32, device=dev)
+    _check_cuda("out_resid", out_resid, torch.float32, (N,), dev)
+    h, _ = _stream_handle(stream)
+    _ok(library().conformal_residual(_ptr(draft_logits), _ptr(true_logits), code, N, V,
+                                     _ptr(out_resid), h), "conformal_residual")
+    return out_resid
+
+
+def conformal_quantile_workspace(n: int) -> int:
+    return int(library().conformal_quantile_workspace(n))
+
+
+def conformal_quantile(resid, q: float, *, out_q=None, workspace=None, stream=None):
+    """Split-conformal quantile of the residuals [n]. Returns Q as a [1] fp32 tensor."""
+    n = resid.numel()
+    dev = resid.device
+    _check_cuda("resid", resid, torch.float32, (n,), dev)
+    if out_q is None:
+        out_q = torch.empty((1,), dtype=torch.float32, device=dev)
+    _check_cuda("out_q", out_q, torch.float32, (1,), dev)
+    h, st = _stream_handle(stream)
+    need = conformal_quantile_workspace(n)
+    ws = workspace if workspace is not None else _workspace("select", need, dev, st)
+    _ok(library().conformal_quantile(_ptr(resid), n, float(q), _ptr(out_q), _ptr(ws),
+                                     ws.numel(), h), "conformal_quantile")
+    return out_q
+
+
+def conformal_admit_workspace(N: int, K: int, V: int, dtype: int) -> int:
+    return int(library().conformal_admit_workspace(N, K, V, dtype))
+
+
+def conformal_admit(logits, Q, *, out_layer=None, out_token=None, out_gap=None,
+                    want_gap: bool = True, workspace=None, stream=None):
+    """Conformal gate over logits [N, K, V] and per-layer quantiles Q [K]. Returns (layer [N],
+    token [N], gap [N, K] or None)."""
+    N, K, V = logits.shape
+    dev = logits.device
+    code = _dtype_code(logits)
+    _check_cuda("logits", logits)
+    _check_cuda("Q", Q, torch.float32, (K,), dev)
+    if out_layer is None:
+        out_layer = torch.empty((N,), dtype=torch.int32, device=dev)
+    if out_token is None:
+        out_token = torch.empty((N,), dtype=torch.int32, device=dev)
+    if out_gap is None and want_gap:
+        out_gap = torch.empty((N, K), dtype=torch.float32, device=dev)
+    _check_cuda("out_layer", out_layer, torch.int32, (N,), dev)
+    _check_cuda("out_token", out_token, torch.int32, (N,), dev)
+    _check_cuda("out_gap", out_gap, torch.float32, (N, K), dev)
+    h, st = _stream_handle(stream)
+    need = conformal_admit_workspace(N, K, V, code)
+    ws = workspace if workspace is not None else _workspace("admit", need, dev, st)
+    _ok(library().conformal_admit(_ptr(logits), code, N, K, V, _ptr(Q), _ptr(out_layer),
+                                  _ptr(out_token), _ptr(out_gap), _ptr(ws), ws.numel(), h),
+        "conformal_admit")
+    return out_layer, out_token, out_gap
 
 
 # ------------------------------------------------------------------------------ confidence

@@ -125,3 +125,18 @@ def _declare(L):
     L.draft_confidence_workspace.argtypes = [I, I, I, I]
     L.draft_confidence_stop.restype = I
     L.draft_confidence_stop.argtypes = [P, I, P, I, I, I, F, I, F, P, P, P, Z, P]
+    D = ctypes.c_double
+    L.gate_risk_coverage_workspace.restype = Z
+    L.gate_risk_coverage_workspace.argtypes = [I, I]
+    L.gate_risk_coverage.restype = I
+    L.gate_risk_coverage.argtypes = [P, P, P, I, P, I, P, I, D, D, P, P, P, Z, P]
+    L.conformal_residual.restype = I
+    L.conformal_residual.argtypes = [P, P, I, I, I, P, P]
+    L.conformal_quantile_workspace.restype = Z
+    L.conformal_quantile_workspace.argtypes = [I]
+    L.conformal_quantile.restype = I
+    L.conformal_quantile.argtypes = [P, I, D, P, P, Z, P]
+    L.conformal_admit_workspace.restype = Z
+    L.conformal_admit_workspace.argtypes = [I, I, I, I]
+    L.conformal_admit.restype = I
+    L.conformal_admit.argtypes = [P, I, I, I, I, P, P, P, P, P, Z, P]

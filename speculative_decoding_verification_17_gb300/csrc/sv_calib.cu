@@ -1,0 +1,544 @@
+// sv_calib.cu — calibration of the logit-gap gate and the scores of the conformal gate.
+//
+//  gate_risk_coverage  "Speculative Pre-Positioning", section 2.4, Eq. (13)-(14): coverage and
+//                      false-accept risk of the gate over a threshold grid, with the Wilson
+//                      intervals of section 4, and the smallest threshold that meets a risk
+//                      budget. One launch: every CTA bins its decision points by the number
+//                      of thresholds below their gap (a binary search in shared memory) into
+//                      a shared histogram, folds it into a global one, and the last CTA turns
+//                      the histogram into per-threshold counts with one suffix scan.
+//  conformal_residual  the "speculative-decoding-plan.md" conformal gate's calibration score:
+//                      the sup-norm distance of a draft row from the true row. A streaming
+//                      max over two rows (16-byte loads, four pairs in flight per thread),
+//                      folded into the output with an atomic maximum on the float's bits.
+//  conformal_quantile  the split-conformal quantile of those scores: a radix select over the
+//                      scores' order-preserving keys in three passes (11, 11, 10 bits), one
+//                      launch each; the last CTA of a pass picks the digit.
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "specverify.h"
+#include "specverify_calib.h"
+#include "sv_device.cuh"
+#include "sv_host.h"
+
+namespace sv {
+namespace {
+
+constexpr int kCalThreads = 256;
+
+// SMs of the current device (cached per device).
+int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load();
+    if (c > 0) return c;
+  }
+  int c = 0;
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+    c = 152;
+  if (dev >= 0 && dev < 64) cache[dev].store(c);
+  return c;
+}
+
+__device__ __forceinline__ bool in_sorted_set(const int32_t* a, int n, int v) {
+  int lo = 0, hi = n;  // first index with a[i] >= v
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) < v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo < n && __ldg(a + lo) == v;
+}
+
+// Wilson score interval of k successes in n trials at the normal quantile z, clamped to
+// [0, 1]; NaN for n = 0. Each operation is rounded on its own (the half-width's product is
+// kept out of a fused multiply-add), so the result matches the formula evaluated step by step.
+__device__ void wilson(double k, double n, double z, double& lo, double& hi) {
+  if (!(n > 0.0)) {
+    lo = hi = __longlong_as_double(0x7ff8000000000000LL);
+    return;
+  }
+  const double p = k / n;
+  const double z2 = z * z;
+  const double denom = 1.0 + z2 / n;
+  const double centre = (p + z2 / (2.0 * n)) / denom;
+  const double half = __dmul_rn(z / denom, sqrt(p * (1.0 - p) / n + z2 / (4.0 * n * n)));
+  const double a = centre - half, b = centre + half;
+  lo = a < 0.0 ? 0.0 : a;
+  hi = b > 1.0 ? 1.0 : b;
+}
+
+// In place: a[i] <- a[i] + a[i+1] + ... + a[n-1] (inclusive suffix sums), all threads.
+__device__ void block_suffix_sums(unsigned int* a, int n, unsigned int* warp_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int per = (n + kCalThreads - 1) / kCalThreads;
+  const int b0 = threadIdx.x * per;
+  const int b1 = min(b0 + per, n);
+  unsigned int tot = 0;
+  for (int i = b0; i < b1; ++i) tot += a[i];
+  unsigned int incl = tot;  // this thread and the later lanes of its warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int v = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += v;
+  }
+  if (lane == 0) warp_tot[w] = incl;
+  __syncthreads();
+  unsigned int run = incl - tot;
+  for (int v = w + 1; v < kCalThreads / 32; ++v) run += warp_tot[v];
+  for (int i = b1 - 1; i >= b0; --i) {
+    run += a[i];
+    a[i] = run;
+  }
+  __syncthreads();
+}
+
+// In place: a[i] <- a[0] + ... + a[i-1] (exclusive prefix sums), all threads.
+__device__ void block_prefix_sums(unsigned int* a, int n, unsigned int* warp_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int per = (n + kCalThreads - 1) / kCalThreads;
+  const int b0 = threadIdx.x * per;
+  const int b1 = min(b0 + per, n);
+  unsigned int tot = 0;
+  for (int i = b0; i < b1; ++i) tot += a[i];
+  unsigned int incl = tot;  // this thread and the earlier lanes of its warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  unsigned int run = incl - tot;
+  for (int v = 0; v < w; ++v) run += warp_tot[v];
+  for (int i = b0; i < b1; ++i) {
+    const unsigned int x = a[i];
+    a[i] = run;
+    run += x;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ risk-coverage sweep
+struct SweepArgs {
+  const float* gap;
+  const int32_t* token;
+  const int32_t* full;
+  int N;
+  const int32_t* answer;
+  int n_answer;
+  const float* taus;
+  int T;
+  double z, r_max;
+  sv_calib_point* out;
+  int32_t* out_idx;
+  unsigned int* acc;  // [T + 1]: accepted points by bin b = #{t : taus[t] < gap}
+  unsigned int* bad;  // [T + 1]: the wrong ones among them
+  unsigned int* cnt;  // CTA arrivals
+};
+
+inline size_t sweep_smem(int T) {
+  return (size_t)T * sizeof(float) + 2 * (size_t)(T + 1) * sizeof(unsigned int);
+}
+
+__global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int T = A.T;
+  float* tau = reinterpret_cast<float*>(smem);
+  unsigned int* hacc = reinterpret_cast<unsigned int*>(tau + T);
+  unsigned int* hbad = hacc + T + 1;
+  __shared__ unsigned int warp_tot[kCalThreads / 32];
+  __shared__ int last, best;
+  for (int t = threadIdx.x; t < T; t += kCalThreads) tau[t] = __ldg(A.taus + t);
+  for (int b = threadIdx.x; b <= T; b += kCalThreads) hacc[b] = hbad[b] = 0;
+  __syncthreads();
+
+  const float t0 = tau[0];
+  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
+  for (int64_t i = (int64_t)blockIdx.x * kCalThreads + threadIdx.x; i < A.N; i += stride) {
+    const float g = __ldcs(A.gap + i);
+    if (!(g > t0)) continue;  // below every threshold (or NaN): accepted nowhere
+    const int tok = __ldcs(A.token + i);
+    if (A.n_answer == 0 || !in_sorted_set(A.answer, A.n_answer, tok)) continue;
+    int lo = 1, hi = T;  // bin = #{t : tau[t] < g} >= 1
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (tau[mid] < g) lo = mid + 1;
+      else hi = mid;
+    }
+    atomicAdd(&hacc[lo], 1u);
+    if (tok != __ldcs(A.full + i)) atomicAdd(&hbad[lo], 1u);
+  }
+  __syncthreads();
+  for (int b = 1 + threadIdx.x; b <= T; b += kCalThreads) {
+    if (hacc[b]) atomicAdd(A.acc + b, hacc[b]);
+    if (hbad[b]) atomicAdd(A.bad + b, hbad[b]);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = arrive_last(A.cnt, gridDim.x);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
+  // the grid must be non-decreasing without NaN
+  int broken = 0;
+  for (int t = threadIdx.x; t < T; t += kCalThreads)
+    broken |= (tau[t] != tau[t]) || (t > 0 && tau[t] < tau[t - 1]);
+  broken = __syncthreads_or(broken);
+  const double nan = __longlong_as_double(0x7ff8000000000000LL);
+  if (broken) {
+    for (int t = threadIdx.x; t < T; t += kCalThreads)
+      A.out[t] = sv_calib_point{-1, -1, nan, nan, nan, nan, nan, nan};
+    if (threadIdx.x == 0) *A.out_idx = -2;
+    return;
+  }
+  // accepted(t) = sum of bins b > t
+  for (int b = threadIdx.x; b <= T; b += kCalThreads) {
+    hacc[b] = b ? __ldcg(A.acc + b) : 0u;
+    hbad[b] = b ? __ldcg(A.bad + b) : 0u;
+  }
+  if (threadIdx.x == 0) best = INT_MAX;
+  __syncthreads();
+  block_suffix_sums(hacc, T + 1, warp_tot);
+  block_suffix_sums(hbad, T + 1, warp_tot);
+  const double n = (double)A.N;
+  for (int t = threadIdx.x; t < T; t += kCalThreads) {
+    const unsigned int acc = hacc[t + 1], bad = hbad[t + 1];
+    sv_calib_point p;
+    p.accepted = acc;
+    p.wrong = bad;
+    p.coverage = A.N > 0 ? (double)acc / n : nan;
+    wilson((double)acc, n, A.z, p.cov_lo, p.cov_hi);
+    if (acc > 0) {
+      p.risk = (double)bad / (double)acc;
+      wilson((double)bad, (double)acc, A.z, p.risk_lo, p.risk_hi);
+      if (p.risk <= A.r_max) atomicMin(&best, t);
+    } else {
+      p.risk = p.risk_lo = p.risk_hi = nan;
+    }
+    A.out[t] = p;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *A.out_idx = best == INT_MAX ? -1 : best;
+}
+
+struct SweepLayout {
+  size_t acc, bad, cnt, total;
+};
+SweepLayout sweep_layout(int T) {
+  SweepLayout L{};
+  size_t o = 0;
+  L.acc = o; o = round_up(o + (size_t)(T + 1) * sizeof(unsigned int), 256);
+  L.bad = o; o = round_up(o + (size_t)(T + 1) * sizeof(unsigned int), 256);
+  L.cnt = o; o = round_up(o + sizeof(unsigned int), 256);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ conformal residual
+// One CTA per (row pair, piece of kResidPieceVec vectors); 16-byte loads of both rows.
+constexpr int kResidPieceVec = 4096;  // 64 KiB of each row
+constexpr int kResidUnroll = 4;
+
+struct ResidArgs {
+  const void* a;
+  const void* b;
+  int N, V;
+  int pieces;    // pieces per row
+  float* out;
+};
+
+template <typename E>
+__device__ __forceinline__ void resid_fold(float x, float y, float& m, bool& nan) {
+  const float d = x == y ? 0.0f : fabsf(x - y);
+  nan |= d != d;
+  m = fmaxf(m, d);
+}
+
+template <typename E, bool kVec>
+__global__ void __launch_bounds__(kCalThreads) resid_kernel(const ResidArgs A) {
+  const int64_t u = blockIdx.x;
+  const int row = (int)(u / A.pieces);
+  const int piece = (int)(u - (int64_t)row * A.pieces);
+  float m = 0.0f;
+  bool nan = false;
+  if (kVec) {
+    const int64_t nvec = (int64_t)A.V / E::kPerVec;  // rows hold whole vectors here
+    const uint4* ra = reinterpret_cast<const uint4*>(A.a) + (int64_t)row * nvec;
+    const uint4* rb = reinterpret_cast<const uint4*>(A.b) + (int64_t)row * nvec;
+    const int64_t v0 = (int64_t)piece * kResidPieceVec;
+    const int64_t v1 = min(v0 + kResidPieceVec, nvec);
+    for (int64_t v = v0 + threadIdx.x; v < v1; v += kResidUnroll * kCalThreads) {
+      uint4 xa[kResidUnroll], xb[kResidUnroll];
+#pragma unroll
+      for (int q = 0; q < kResidUnroll; ++q) {
+        const int64_t vq = v + (int64_t)q * kCalThreads;
+        if (vq < v1) {
+          xa[q] = __ldcs(ra + vq);
+          xb[q] = __ldcs(rb + vq);
+        } else {
+          xa[q] = xb[q] = make_uint4(0u, 0u, 0u, 0u);  // equal: contributes 0
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kResidUnroll; ++q)
+#pragma unroll
+        for (int l = 0; l < E::kPerVec; ++l)
+          resid_fold<E>(E::get(xa[q], l), E::get(xb[q], l), m, nan);
+    }
+  } else {
+    // rows off the 16-byte grid: logit by logit (coalesced)
+    const int64_t pe = (int64_t)kResidPieceVec * E::kPerVec;
+    const int64_t j0 = (int64_t)piece * pe;
+    const int64_t j1 = min(j0 + pe, (int64_t)A.V);
+    const int64_t base = (int64_t)row * A.V;
+    for (int64_t j = j0 + threadIdx.x; j < j1; j += kCalThreads)
+      resid_fold<E>(E::load1(A.a, base + j), E::load1(A.b, base + j), m, nan);
+  }
+  // CTA maximum, then one atomic maximum on the non-negative float's bits (NaN above +inf)
+  __shared__ float wm[kCalThreads / 32];
+  __shared__ int wn[kCalThreads / 32];
+  m = warp_max_f(m);
+  nan = __any_sync(0xffffffffu, nan);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) {
+    wm[w] = m;
+    wn[w] = nan;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int v = 1; v < kCalThreads / 32; ++v) {
+      m = fmaxf(m, wm[v]);
+      nan |= wn[v] != 0;
+    }
+    const unsigned int bits = nan ? 0x7fc00000u : __float_as_uint(m);
+    atomicMax(reinterpret_cast<unsigned int*>(A.out) + row, bits);
+  }
+}
+
+// ------------------------------------------------------------------ conformal quantile
+constexpr int kSelBins = 2048;
+
+struct SelectState {
+  unsigned int prefix;     // the key's bits chosen so far
+  unsigned int remaining;  // the rank within the keys that share the prefix
+  unsigned int done;       // set when the result is already written
+  unsigned int pad;
+  unsigned int cnt[4];     // CTA arrivals per pass
+  unsigned int hist[3][kSelBins];
+};
+
+// Order-preserving key of a float (NaN canonicalised, above +inf; -0 below +0).
+__device__ __forceinline__ unsigned int float_key(float x) {
+  unsigned int u = __float_as_uint(x);
+  if (x != x) u = 0x7fc00000u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(unsigned int k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int n, int64_t rank,
+                                                             int pass, SelectState* st,
+                                                             float* out) {
+  __shared__ unsigned int h[kSelBins];
+  __shared__ unsigned int warp_tot[kCalThreads / 32];
+  __shared__ int last;
+  if (__ldcg(&st->done)) return;
+  const int width = pass == 2 ? 10 : 11;
+  const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+  const unsigned int mask = (1u << width) - 1u;
+  const unsigned int prefix = pass == 0 ? 0u : __ldcg(&st->prefix);
+  for (int b = threadIdx.x; b < kSelBins; b += kCalThreads) h[b] = 0;
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
+  for (int64_t i = (int64_t)blockIdx.x * kCalThreads + threadIdx.x; i < n; i += stride) {
+    const unsigned int key = float_key(__ldg(r + i));
+    if (pass == 0 || (key >> (shift + width)) == prefix) atomicAdd(&h[(key >> shift) & mask], 1u);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
+    if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = arrive_last(&st->cnt[pass], gridDim.x);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const unsigned int want = pass == 0 ? (unsigned int)rank : __ldcg(&st->remaining);
+  for (int b = threadIdx.x; b < kSelBins; b += kCalThreads)
+    h[b] = b <= (int)mask ? __ldcg(&st->hist[pass][b]) : 0u;
+  __syncthreads();
+  // the digit d with (keys below it) < want <= (keys below it) + count(d)
+  unsigned int* cnt = h;
+  // counts before the prefix sums, kept per thread for the check below
+  const int per = kSelBins / kCalThreads;
+  unsigned int own[kSelBins / kCalThreads];
+#pragma unroll
+  for (int i = 0; i < per; ++i) own[i] = cnt[threadIdx.x * per + i];
+  __syncthreads();
+  block_prefix_sums(cnt, kSelBins, warp_tot);
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    const int b = threadIdx.x * per + i;
+    const unsigned int before = cnt[b];
+    if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
+      const unsigned int p = (prefix << width) | (unsigned int)b;
+      if (pass == 2) {
+        *out = key_float(p);
+        st->done = 1u;
+      } else {
+        st->prefix = p;
+        st->remaining = want - before;
+      }
+    }
+  }
+}
+
+constexpr int kSelectPasses = 3;
+
+__global__ void store_inf(float* out) { *out = __uint_as_float(0x7f800000u); }
+
+}  // namespace
+}  // namespace sv
+
+// ============================================================================================
+// C ABI
+// ============================================================================================
+using namespace sv;
+
+extern "C" size_t gate_risk_coverage_workspace(int N, int T) {
+  if (N < 0 || T < 1 || T > SV_MAX_TAUS) return 0;
+  return sweep_layout(T).total;
+}
+
+extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
+                                        const int32_t* full_token, int N,
+                                        const int32_t* answer_set, int n_answer,
+                                        const float* taus, int T, double z, double r_max,
+                                        sv_calib_point* out_points, int32_t* out_tau_index,
+                                        void* workspace, size_t workspace_bytes,
+                                        sv_stream_t stream) {
+  if (N < 0 || n_answer < 0 || T < 1) return SV_ERR_INVALID_ARG;
+  if (T > SV_MAX_TAUS) return SV_ERR_UNSUPPORTED;
+  if (!std::isfinite(z) || z < 0.0) return SV_ERR_INVALID_ARG;
+  if (!taus || !out_points || !out_tau_index || (n_answer > 0 && !answer_set))
+    return SV_ERR_INVALID_ARG;
+  if (N > 0 && (!gap || !token || !full_token)) return SV_ERR_INVALID_ARG;
+  if (!aligned_to(taus, 4) || !aligned_to(out_points, 8) || !aligned_to(out_tau_index, 4) ||
+      (gap && !aligned_to(gap, 4)) || (token && !aligned_to(token, 4)) ||
+      (full_token && !aligned_to(full_token, 4)) || (answer_set && !aligned_to(answer_set, 4)))
+    return SV_ERR_INVALID_ARG;
+  const SweepLayout L = sweep_layout(T);
+  if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
+    return SV_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.total, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  SweepArgs A;
+  A.gap = gap;
+  A.token = token;
+  A.full = full_token;
+  A.N = N;
+  A.answer = answer_set;
+  A.n_answer = n_answer;
+  A.taus = taus;
+  A.T = T;
+  A.z = z;
+  A.r_max = r_max;
+  A.out = out_points;
+  A.out_idx = out_tau_index;
+  char* ws = static_cast<char*>(workspace);
+  A.acc = reinterpret_cast<unsigned int*>(ws + L.acc);
+  A.bad = reinterpret_cast<unsigned int*>(ws + L.bad);
+  A.cnt = reinterpret_cast<unsigned int*>(ws + L.cnt);
+  const size_t smem = sweep_smem(T);
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // enough CTAs to keep the loads in flight, at most four per SM
+  const int64_t want = ((int64_t)N + 8 * kCalThreads - 1) / (8 * kCalThreads);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 4LL * device_sms()));
+  sweep_kernel<<<grid, kCalThreads, smem, st>>>(A);
+  return launch_status();
+}
+
+extern "C" sv_status conformal_residual(const void* draft_logits, const void* true_logits,
+                                        sv_dtype dtype, int N, int V, float* out_resid,
+                                        sv_stream_t stream) {
+  if (N < 0 || V < 1) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (N == 0) return SV_OK;
+  if (!draft_logits || !true_logits || !out_resid) return SV_ERR_INVALID_ARG;
+  const int eb = elem_bytes(dtype);
+  if (!aligned_to(draft_logits, eb) || !aligned_to(true_logits, eb) ||
+      !aligned_to(out_resid, 4))
+    return SV_ERR_INVALID_ARG;
+  const bool vec = aligned_to(draft_logits, 16) && aligned_to(true_logits, 16) &&
+                   ((int64_t)V * eb) % 16 == 0;
+  const int per_vec = 16 / eb;
+  const int64_t piece_elems = (int64_t)kResidPieceVec * per_vec;
+  const int pieces = (int)(((int64_t)V + piece_elems - 1) / piece_elems);
+  const int64_t units = (int64_t)N * pieces;
+  if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(out_resid, 0, (size_t)N * sizeof(float), st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ResidArgs A{draft_logits, true_logits, N, V, pieces, out_resid};
+  const unsigned grid = (unsigned)units;
+  if (dtype == SV_F32) {
+    if (vec) resid_kernel<F32, true><<<grid, kCalThreads, 0, st>>>(A);
+    else resid_kernel<F32, false><<<grid, kCalThreads, 0, st>>>(A);
+  } else {
+    if (vec) resid_kernel<BF16, true><<<grid, kCalThreads, 0, st>>>(A);
+    else resid_kernel<BF16, false><<<grid, kCalThreads, 0, st>>>(A);
+  }
+  return launch_status();
+}
+
+extern "C" size_t conformal_quantile_workspace(int n) {
+  if (n < 1) return 0;
+  return round_up(sizeof(SelectState), 256);
+}
+
+extern "C" sv_status conformal_quantile(const float* resid, int n, double q, float* out_q,
+                                        void* workspace, size_t workspace_bytes,
+                                        sv_stream_t stream) {
+  if (n < 1 || !(q > 0.0) || !(q <= 1.0)) return SV_ERR_INVALID_ARG;
+  if (!resid || !out_q || !aligned_to(resid, 4) || !aligned_to(out_q, 4))
+    return SV_ERR_INVALID_ARG;
+  const size_t need = round_up(sizeof(SelectState), 256);
+  if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < need)
+    return SV_ERR_WORKSPACE;
+  const double rk = std::ceil((double)(n + 1) * q);  // 1 <= rk <= n + 1
+  const int64_t rank = (int64_t)rk;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  SelectState* S = static_cast<SelectState*>(workspace);
+  if (rank > (int64_t)n) {
+    store_inf<<<1, 1, 0, st>>>(out_q);  // the rank is past the largest score
+    return launch_status();
+  }
+  const int64_t want = ((int64_t)n + 8 * kCalThreads - 1) / (8 * kCalThreads);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 2LL * device_sms()));
+  for (int p = 0; p < kSelectPasses; ++p) {
+    select_kernel<<<grid, kCalThreads, 0, st>>>(resid, n, rank, p, S, out_q);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return SV_OK;
+}

@@ -118,6 +118,46 @@ def test_confidence_stop_validation():
     assert L.draft_confidence_workspace(4, 17, 1000, 1) == 0
 
 
+def test_calibration_validation():
+    L = sv.library()
+    ws = ctypes.c_void_p(0x100000)
+    rc = lambda **kw: L.gate_risk_coverage(
+        FAKE, FAKE, FAKE, kw.get("N", 10), kw.get("A", FAKE), kw.get("nA", 3),
+        kw.get("taus", FAKE), kw.get("T", 5), kw.get("z", 1.96), 0.1, kw.get("out", FAKE), FAKE,
+        kw.get("ws", ws), kw.get("wsb", 1 << 30), None)
+    assert rc(N=-1) == INVALID and rc(T=0) == INVALID and rc(nA=-1) == INVALID
+    assert rc(T=4097) == UNSUPPORTED and rc(z=float("nan")) == INVALID and rc(z=-1.0) == INVALID
+    assert rc(taus=None) == INVALID and rc(out=None) == INVALID and rc(A=None) == INVALID
+    assert rc(wsb=16) == WORKSPACE and rc(ws=None) == WORKSPACE
+    assert L.gate_risk_coverage_workspace(10, 5) > 0
+    assert L.gate_risk_coverage_workspace(10, 4097) == 0
+
+    cr = lambda **kw: L.conformal_residual(kw.get("a", FAKE), kw.get("b", FAKE),
+                                           kw.get("dtype", 1), kw.get("N", 4), kw.get("V", 100),
+                                           kw.get("out", FAKE), None)
+    assert cr(N=-1) == INVALID and cr(V=0) == INVALID and cr(dtype=3) == INVALID
+    assert cr(a=None) == INVALID and cr(out=None) == INVALID
+    assert cr(N=0, a=None) == OK
+    assert cr(a=ctypes.c_void_p(0x10001)) == INVALID  # misaligned for bf16
+
+    cq = lambda **kw: L.conformal_quantile(kw.get("r", FAKE), kw.get("n", 10), kw.get("q", 0.9),
+                                           kw.get("out", FAKE), kw.get("ws", ws),
+                                           kw.get("wsb", 1 << 30), None)
+    assert cq(n=0) == INVALID and cq(q=0.0) == INVALID and cq(q=1.5) == INVALID
+    assert cq(q=float("nan")) == INVALID and cq(r=None) == INVALID and cq(out=None) == INVALID
+    assert cq(wsb=64) == WORKSPACE
+    assert L.conformal_quantile_workspace(0) == 0 and L.conformal_quantile_workspace(5) > 0
+
+    ca = lambda **kw: L.conformal_admit(kw.get("z", FAKE), kw.get("dtype", 1), kw.get("N", 3),
+                                        kw.get("K", 2), kw.get("V", 50), kw.get("Q", FAKE),
+                                        kw.get("lay", FAKE), FAKE, None, kw.get("ws", ws),
+                                        kw.get("wsb", 1 << 30), None)
+    assert ca(N=-1) == INVALID and ca(K=0) == INVALID and ca(V=1) == INVALID
+    assert ca(Q=None) == INVALID and ca(lay=None) == INVALID and ca(z=None) == INVALID
+    assert ca(wsb=16) == WORKSPACE and ca(N=0, z=None) == OK
+    assert L.conformal_admit_workspace(3, 0, 50, 1) == 0
+
+
 def test_binding_raises_on_bad_input():
     import torch
 

@@ -1,0 +1,274 @@
+"""CUDA gate calibration and conformal gate vs the oracle, through the C ABI (via the binding).
+
+- gate_risk_coverage: exact counts, selected threshold and rates (bit for bit), on the
+  pre-positioning page's operating point, random decision points with NaN gaps and tied
+  thresholds, the largest grid, an empty set, an unsorted grid, and a million points.
+- conformal_residual: bit-exact fp32 residuals on rows with masked tokens, one-sided masks,
+  NaN and infinities, aligned and unaligned rows, both dtypes, and the sampled-verify
+  benchmark batch's draft rows against its target rows (sampled rows).
+- conformal_quantile: the exact order statistic on ties, NaN, infinities and negative
+  scores, at sizes from 1 to four million.
+- conformal_admit: exact layers and tokens outside near ties and the fp32 gaps bit for bit,
+  K from 1 to 8, both dtypes, rows of two segments, all-NaN rows; and the whole calibration
+  pipeline (residuals -> quantile -> admission) on the device against the oracle's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_17_gb300 as sv
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+Z95 = 1.959963984540054
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def run_sweep(gap, token, full, A, taus, z=Z95, r_max=0.15):
+    pts, idx = sv.gate_risk_coverage(_dev(gap), _dev(token), _dev(full),
+                                     None if A is None else _dev(A), _dev(taus), z, r_max)
+    torch.cuda.synchronize()
+    return sv.gate_points_dict(pts), int(idx.item())
+
+
+def check_sweep(gap, token, full, A, taus, z=Z95, r_max=0.15):
+    got, idx = run_sweep(gap, token, full, A, taus, z, r_max)
+    want = oracle.risk_coverage(gap, token, full, A, taus, z, r_max)
+    np.testing.assert_array_equal(got["accepted"].numpy(), want["accepted"])
+    np.testing.assert_array_equal(got["wrong"].numpy(), want["wrong"])
+    for name in ("coverage", "cov_lo", "cov_hi", "risk", "risk_lo", "risk_hi"):
+        # the same operations in the same order, each rounded on its own: bit for bit
+        np.testing.assert_array_equal(got[name].numpy(), want[name], err_msg=name)
+    assert idx == want["tau_index"], (idx, want["tau_index"])
+    return got, idx
+
+
+def _points(N, seed, n_vocab=500, nan_every=0):
+    rng = np.random.default_rng(seed)
+    A = np.sort(rng.choice(n_vocab, n_vocab // 6, replace=False)).astype(np.int32)
+    token = rng.integers(0, n_vocab, N).astype(np.int32)
+    token[: N // 2] = rng.choice(A, N // 2)
+    gap = np.abs(rng.standard_normal(N) * 3).astype(np.float32)
+    if nan_every:
+        gap[::nan_every] = np.nan
+    p_ok = 1 - 0.5 * np.exp(-np.nan_to_num(gap.astype(np.float64)))
+    full = np.where(rng.random(N) < p_ok, token, token + 1).astype(np.int32)
+    return gap, token, full, A
+
+
+def test_sweep_pages_operating_point():
+    import test_oracle_calibration as K
+
+    gap, token, full, A = K._operating_point_fixture()
+    taus = np.linspace(0.0, 6.0, 25).astype(np.float32)
+    got, idx = check_sweep(gap, token, full, A, taus, r_max=0.15)
+    t = int(np.flatnonzero(taus == 2.0)[0])
+    assert int(got["accepted"][t]) == 121 and int(got["wrong"][t]) == 16
+
+
+@pytest.mark.parametrize("N,T,seed", [(1, 1, 0), (37, 5, 1), (10000, 61, 2), (5000, 4096, 3),
+                                      (300, 4095, 4)])
+def test_sweep_random(N, T, seed):
+    gap, token, full, A = _points(N, seed, nan_every=13)
+    rng = np.random.default_rng(seed + 100)
+    taus = np.sort(rng.uniform(-1, 9, T)).astype(np.float32)
+    if T > 3:
+        taus[1] = taus[2]             # a repeated threshold
+        taus[0] = -np.inf
+        taus[-1] = np.inf
+        gap[: min(N, 8)] = taus[T // 2]  # gaps sitting exactly on a threshold
+    check_sweep(gap, token, full, A, taus, r_max=0.2)
+
+
+def test_sweep_edges():
+    gap, token, full, A = _points(200, 9)
+    taus = np.array([0.5, 1.0, 2.0], np.float32)
+    # empty answer set: nothing accepted, no threshold qualifies
+    got, idx = check_sweep(gap, token, full, None, taus)
+    assert (got["accepted"].numpy() == 0).all() and idx == -1
+    # no decision points at all
+    e = np.zeros(0, np.float32)
+    ei = np.zeros(0, np.int32)
+    got, idx = check_sweep(e, ei, ei, A, taus)
+    assert np.isnan(got["coverage"].numpy()).all() and idx == -1
+    # r_max NaN: nothing qualifies
+    got, idx = check_sweep(gap, token, full, A, taus, r_max=float("nan"))
+    assert idx == -1
+    # an unsorted grid is reported, not guessed at
+    got, idx = run_sweep(gap, token, full, A, np.array([1.0, 0.5, 2.0], np.float32))
+    assert idx == -2 and (got["accepted"].numpy() == -1).all()
+    assert np.isnan(got["risk"].numpy()).all()
+    got, idx = run_sweep(gap, token, full, A, np.array([0.5, np.nan], np.float32))
+    assert idx == -2
+
+
+def test_sweep_a_million_points():
+    gap, token, full, A = _points(1 << 20, 21, n_vocab=120, nan_every=1001)
+    taus = np.linspace(0.0, 8.0, 64).astype(np.float32)
+    check_sweep(gap, token, full, A, taus, r_max=0.3)
+
+
+# ------------------------------------------------------------------------------ residual
+def _bits(x):
+    return np.asarray(x, np.float32).view(np.uint32)
+
+
+def _same_f32(a, b):
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    both_nan = np.isnan(a) & np.isnan(b)
+    return bool(((_bits(a) == _bits(b)) | both_nan).all())
+
+
+@pytest.mark.parametrize("N,V,dt", [(5, 1, "f32"), (7, 1000, "f32"), (9, 1001, "bf16"),
+                                    (6, 40000, "bf16"), (4, 8191, "f32"), (3, 151936, "bf16"),
+                                    (2, 200003, "f32")])
+def test_residual_small(N, V, dt):
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(N * V)
+    t = (torch.randn((N, V), generator=g) * 3).to(tdt)
+    d = (t.float() + torch.randn((N, V), generator=g) * 0.2).to(tdt)
+    if N >= 4 and V >= 8:
+        d[0] = t[0]                                   # identical rows: 0
+        t[1, : V // 2] = d[1, : V // 2] = float("-inf")  # masked in both
+        d[2, V - 1] = float("-inf")                   # masked in one: inf
+        t[3, V // 3] = float("nan")                   # NaN: NaN
+    got = sv.conformal_residual(d.to(DEV), t.to(DEV))
+    torch.cuda.synchronize()
+    want = oracle.conformal_residual(d, t)
+    assert _same_f32(got.cpu().numpy(), want), (got.cpu().numpy(), want)
+
+
+def test_residual_unaligned_views_and_inf():
+    V = 3000
+    base_t = torch.randn((5, V + 1)) * 2
+    base_d = base_t + torch.randn((5, V + 1)) * 0.1
+    base_d[1, 7] = float("inf")
+    base_t[1, 7] = float("inf")                      # +inf in both: equal, 0
+    base_d[2, 9] = float("inf")                      # +inf against a finite value: inf
+    # views 4 bytes into device buffers: the rows are off the 16-byte grid
+    bt = base_t.to(DEV).reshape(-1)[1: 1 + 4 * V].reshape(4, V)
+    bd = base_d.to(DEV).reshape(-1)[1: 1 + 4 * V].reshape(4, V)
+    assert bt.data_ptr() % 16 != 0 and bt.is_contiguous()
+    got = sv.conformal_residual(bd, bt)
+    torch.cuda.synchronize()
+    want = oracle.conformal_residual(bd.cpu(), bt.cpu())
+    assert _same_f32(got.cpu().numpy(), want)
+
+
+def test_residual_benchmark_rows_sampled():
+    # the sampled-verify benchmark batch (B=512, k=8, V=128256 bf16): draft rows against the
+    # target rows at the same positions, 4096 row pairs in one launch
+    d = synth.workload_inputs(3, device=DEV)
+    B, k, V = d["B"], d["k"], d["V"]
+    tgt = d["target"][:, :k].contiguous()
+    got = sv.conformal_residual(d["draft"], tgt).cpu().numpy()
+    torch.cuda.synchronize()
+    rows = sorted(np.random.default_rng(5).choice(B * k, 64, replace=False).tolist())
+    want = oracle.conformal_residual(d["draft"].reshape(-1, V).cpu(), tgt.reshape(-1, V).cpu(),
+                                     rows=rows, threads=16)
+    assert _same_f32(got[rows], want[rows])
+    assert (got > 0).all() and np.isfinite(got).all()
+
+
+# ------------------------------------------------------------------------------ quantile
+@pytest.mark.parametrize("n", [1, 2, 5, 19, 4096, 100003, 1 << 22])
+@pytest.mark.parametrize("q", [1e-6, 0.5, 0.9, 0.95, 1.0])
+def test_quantile_random(n, q):
+    rng = np.random.default_rng(n)
+    r = rng.exponential(1.0, n).astype(np.float32)
+    if n >= 19:
+        r[:5] = r[5]                  # ties
+        r[6] = np.inf
+        r[7] = np.nan
+        r[8] = -1.5                   # negative scores order below zero
+    got = sv.conformal_quantile(_dev(r), q)
+    torch.cuda.synchronize()
+    want = oracle.conformal_quantile(r, q)
+    assert _same_f32(got.cpu().numpy(), [want]), (got.item(), want)
+
+
+def test_quantile_reuses_its_workspace():
+    r = np.arange(1000, dtype=np.float32)[::-1].copy()
+    ws = torch.zeros(sv.conformal_quantile_workspace(1000), dtype=torch.uint8, device=DEV)
+    for q in (0.1, 0.5, 0.99, 0.999):
+        got = sv.conformal_quantile(_dev(r), q, workspace=ws).item()
+        assert got == oracle.conformal_quantile(r, q)
+
+
+# ------------------------------------------------------------------------------ admission
+def _layer_logits(N, K, V, dt, seed, peak_hi=8.0):
+    g = torch.Generator().manual_seed(seed)
+    z = torch.randn((N, K, V), generator=g)
+    idx = torch.randint(0, V, (N, K, 1), generator=g)
+    scale = torch.linspace(0.3, 1.0, K) if K > 1 else torch.ones(1)
+    amp = torch.rand((N, K, 1), generator=g) * peak_hi * scale[None, :, None]
+    z.scatter_add_(2, idx, amp)
+    return z.to(torch.float32 if dt == "f32" else torch.bfloat16)
+
+
+def check_admit(z, Q):
+    lay, tok, gap = sv.conformal_admit(z.to(DEV), _dev(Q))
+    torch.cuda.synchronize()
+    o = oracle.conformal_admit(z, Q)
+    lay, tok, gap = lay.cpu().numpy(), tok.cpu().numpy(), gap.cpu().numpy()
+    assert _same_f32(gap, o["gap"].astype(np.float32))
+    keep = o["flag"] == -1
+    np.testing.assert_array_equal(lay[keep], o["layer"][keep])
+    np.testing.assert_array_equal(tok[keep], o["token"][keep])
+    return lay, tok, o
+
+
+@pytest.mark.parametrize("N,K,V,dt", [(64, 1, 1000, "f32"), (40, 2, 32000, "bf16"),
+                                      (25, 4, 8191, "f32"), (16, 8, 3001, "bf16"),
+                                      (6, 3, 151936, "bf16")])
+def test_admit_random(N, K, V, dt):
+    z = _layer_logits(N, K, V, dt, seed=N * K + V)
+    Q = np.linspace(1.2, 0.4, K).astype(np.float32)
+    lay, tok, o = check_admit(z, Q)
+    assert len(set(lay.tolist())) > 1  # several layers actually taken
+
+
+def test_admit_nan_rows_and_edges():
+    N, K, V = 5, 3, 700
+    z = _layer_logits(N, K, V, "f32", seed=3)
+    z[0, :, :] = float("nan")           # never admits
+    z[1, 0, :] = float("nan")           # layer 0 of step 1 cannot admit
+    z[2, :, :] = float("-inf")
+    z[2, :, 11] = 1.0                   # one finite logit: gamma = +inf admits at layer 0
+    Q = np.array([0.5, 0.5, 0.5], np.float32)
+    lay, tok, o = check_admit(z, Q)
+    assert lay[0] == K and tok[0] == -1
+    assert lay[2] == 0 and tok[2] == 11
+    lay, tok, o = check_admit(z, np.full(K, np.inf, np.float32))  # +inf Q admits only +inf gaps
+    assert lay[2] == 0 and (lay[[0, 1, 3, 4]] == K).all()
+    lay, tok, o = check_admit(z, np.full(K, -1.0, np.float32))    # negative Q admits any gap
+    assert (lay[1:] <= 1).all() and lay[1] == 1
+
+
+def test_calibration_pipeline_on_the_device():
+    # calibrate on draft/true row pairs, then admit fresh steps: residuals -> Q -> admission
+    n_cal, V = 512, 32000
+    g = torch.Generator().manual_seed(77)
+    t = torch.randn((n_cal, V), generator=g) * 2
+    d = (t + torch.randn((n_cal, V), generator=g) * torch.rand((n_cal, 1), generator=g) * 0.5)
+    t, d = t.to(torch.bfloat16), d.to(torch.bfloat16)
+    r = sv.conformal_residual(d.to(DEV), t.to(DEV))
+    Q = sv.conformal_quantile(r, 0.9)
+    torch.cuda.synchronize()
+    r_o = oracle.conformal_residual(d, t)
+    assert _same_f32(r.cpu().numpy(), r_o)
+    Q_o = oracle.conformal_quantile(r_o, 0.9)
+    assert Q.item() == Q_o
+    z = _layer_logits(64, 1, V, "bf16", seed=78, peak_hi=12.0)
+    lay, tok, gap = sv.conformal_admit(z.to(DEV), Q)
+    torch.cuda.synchronize()
+    o = oracle.conformal_admit(z, np.array([Q_o], np.float32))
+    keep = o["flag"] == -1
+    np.testing.assert_array_equal(lay.cpu().numpy()[keep], o["layer"][keep])
+    assert 0 < int((o["layer"] == 0).sum()) < 64
