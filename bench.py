@@ -498,18 +498,19 @@ def secondary_rows(args, dev, stream, peak, head=None):
             ms=ms, rows_per_s=B * k / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
             bytes=nb)
         del tgt, rr
-        # conformal gate over K = 4 layers of 256 steps (the first 1024 target rows seen as
-        # [256, 4, V])
-        z4 = head["target"].reshape(-1, V)[: 256 * 4].reshape(256, 4, V)
+        # conformal gate over K = 4 layers: the batch's B*(k+1) target rows seen as
+        # [B*(k+1)/4, 4, V] (1.18 GB)
+        ns = B * (k + 1) // 4
+        z4 = head["target"].reshape(-1, V)[: ns * 4].reshape(ns, 4, V)
         Q4 = torch.tensor([3.0, 2.0, 1.5, 1.0], dtype=torch.float32, device=dev)
-        aws = torch.zeros(sv.conformal_admit_workspace(256, 4, V, sv.SV_BF16), dtype=torch.uint8,
+        aws = torch.zeros(sv.conformal_admit_workspace(ns, 4, V, sv.SV_BF16), dtype=torch.uint8,
                           device=dev)
         ms = statistics.mean(time_launches(
             lambda: sv.conformal_admit(z4, Q4, want_gap=False, workspace=aws, stream=stream),
             steps, 3, stream))
-        nb = 256 * 4 * V * 2
-        rows[f"conformal_admit_n256_k4_v{V}_bf16"] = dict(
-            ms=ms, steps_per_s=256 / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+        nb = ns * 4 * V * 2
+        rows[f"conformal_admit_n{ns}_k4_v{V}_bf16"] = dict(
+            ms=ms, steps_per_s=ns / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
             bytes=nb)
         del z4, aws
 

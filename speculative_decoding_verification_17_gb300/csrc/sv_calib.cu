@@ -3,17 +3,20 @@
 //  gate_risk_coverage  "Speculative Pre-Positioning", section 2.4, Eq. (13)-(14): coverage and
 //                      false-accept risk of the gate over a threshold grid, with the Wilson
 //                      intervals of section 4, and the smallest threshold that meets a risk
-//                      budget. One launch: every CTA bins its decision points by the number
-//                      of thresholds below their gap (a binary search in shared memory) into
-//                      a shared histogram, folds it into a global one, and the last CTA turns
-//                      the histogram into per-threshold counts with one suffix scan.
+//                      budget. One launch: every CTA bins its decision points (four per
+//                      thread and step, 16-byte loads) by the number of thresholds below
+//                      their gap (branch-free binary searches in shared memory, four at a
+//                      time) into a shared histogram,
+//                      folds it into a global one, and the last CTA turns the histogram into
+//                      per-threshold counts with one suffix scan.
 //  conformal_residual  the "speculative-decoding-plan.md" conformal gate's calibration score:
 //                      the sup-norm distance of a draft row from the true row. A streaming
 //                      max over two rows (16-byte loads, four pairs in flight per thread),
 //                      folded into the output with an atomic maximum on the float's bits.
 //  conformal_quantile  the split-conformal quantile of those scores: a radix select over the
-//                      scores' order-preserving keys in three passes (11, 11, 10 bits), one
-//                      launch each; the last CTA of a pass picks the digit.
+//                      scores' order-preserving keys in three passes (11, 11, 10 bits); up to
+//                      8192 scores in one CTA with the keys in shared memory, beyond that one
+//                      launch per pass whose last CTA picks the digit.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -44,16 +47,6 @@ int device_sms() {
     c = 152;
   if (dev >= 0 && dev < 64) cache[dev].store(c);
   return c;
-}
-
-__device__ __forceinline__ bool in_sorted_set(const int32_t* a, int n, int v) {
-  int lo = 0, hi = n;  // first index with a[i] >= v
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) < v) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo < n && __ldg(a + lo) == v;
 }
 
 // Wilson score interval of k successes in n trials at the normal quantile z, clamped to
@@ -141,6 +134,7 @@ struct SweepArgs {
   unsigned int* acc;  // [T + 1]: accepted points by bin b = #{t : taus[t] < gap}
   unsigned int* bad;  // [T + 1]: the wrong ones among them
   unsigned int* cnt;  // CTA arrivals
+  bool vec;           // gap, token and full_token all start on a 16-byte boundary
 };
 
 inline size_t sweep_smem(int T) {
@@ -160,20 +154,66 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   __syncthreads();
 
   const float t0 = tau[0];
-  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
-  for (int64_t i = (int64_t)blockIdx.x * kCalThreads + threadIdx.x; i < A.N; i += stride) {
-    const float g = __ldcs(A.gap + i);
-    if (!(g > t0)) continue;  // below every threshold (or NaN): accepted nowhere
-    const int tok = __ldcs(A.token + i);
-    if (A.n_answer == 0 || !in_sorted_set(A.answer, A.n_answer, tok)) continue;
-    int lo = 1, hi = T;  // bin = #{t : tau[t] < g} >= 1
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (tau[mid] < g) lo = mid + 1;
-      else hi = mid;
+  // Four decision points at a time: each point's bin b = #{t : tau[t] < g} (accepted at
+  // every t < b) and its membership in A, both by branch-free lower bounds of a fixed number
+  // of steps, so the four searches overlap and the lanes stay converged.
+  auto bin4 = [&](const float (&g)[4], const int (&tok)[4], const int (&full)[4]) {
+    bool ok[4];
+    int ia[4], ib[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      ok[p] = g[p] > t0 && A.n_answer > 0;  // below every threshold (or NaN): accepted nowhere
+      ia[p] = 0;
+      ib[p] = 0;
     }
-    atomicAdd(&hacc[lo], 1u);
-    if (tok != __ldcs(A.full + i)) atomicAdd(&hbad[lo], 1u);
+    for (int n = A.n_answer; n > 1;) {
+      const int half = n >> 1;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        if (__ldg(A.answer + ia[p] + half) < tok[p]) ia[p] += half;
+      n -= half;
+    }
+    for (int n = T; n > 1;) {
+      const int half = n >> 1;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        if (tau[ib[p] + half] < g[p]) ib[p] += half;
+      n -= half;
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      if (!ok[p]) continue;
+      const int la = ia[p] + (__ldg(A.answer + ia[p]) < tok[p]);  // first entry >= tok
+      if (la >= A.n_answer || __ldg(A.answer + la) != tok[p]) continue;
+      const int b = ib[p] + (tau[ib[p]] < g[p]);  // >= 1 since tau[0] < g
+      atomicAdd(&hacc[b], 1u);
+      if (tok[p] != full[p]) atomicAdd(&hbad[b], 1u);
+    }
+  };
+  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
+  const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
+  // four points per thread and step, the three 16-byte loads issued together
+  const int64_t n4 = A.vec ? A.N / 4 : 0;
+  for (int64_t q = tid; q < n4; q += stride) {
+    const float4 g = __ldcs(reinterpret_cast<const float4*>(A.gap) + q);
+    const int4 t = __ldcs(reinterpret_cast<const int4*>(A.token) + q);
+    const int4 f = __ldcs(reinterpret_cast<const int4*>(A.full) + q);
+    const float gg[4] = {g.x, g.y, g.z, g.w};
+    const int tt[4] = {t.x, t.y, t.z, t.w}, ff[4] = {f.x, f.y, f.z, f.w};
+    bin4(gg, tt, ff);
+  }
+  // the rest (or everything, for inputs off the 16-byte grid), four points per step
+  for (int64_t i0 = 4 * n4 + 4 * tid; i0 < A.N; i0 += 4 * stride) {
+    float gg[4];
+    int tt[4], ff[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const bool in = i0 + p < A.N;
+      gg[p] = in ? __ldcs(A.gap + i0 + p) : __int_as_float(0x7fc00000);  // NaN: not accepted
+      tt[p] = in ? __ldcs(A.token + i0 + p) : 0;
+      ff[p] = in ? __ldcs(A.full + i0 + p) : 0;
+    }
+    bin4(gg, tt, ff);
   }
   __syncthreads();
   for (int b = 1 + threadIdx.x; b <= T; b += kCalThreads) {
@@ -361,10 +401,21 @@ __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int
   for (int b = threadIdx.x; b < kSelBins; b += kCalThreads) h[b] = 0;
   __syncthreads();
   const int64_t stride = (int64_t)gridDim.x * kCalThreads;
-  for (int64_t i = (int64_t)blockIdx.x * kCalThreads + threadIdx.x; i < n; i += stride) {
-    const unsigned int key = float_key(__ldg(r + i));
+  auto count = [&](float x) {
+    const unsigned int key = float_key(x);
     if (pass == 0 || (key >> (shift + width)) == prefix) atomicAdd(&h[(key >> shift) & mask], 1u);
+  };
+  // four scores per thread and step (one 16-byte load; the passes re-read them from L2)
+  const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
+  const int64_t n4 = (reinterpret_cast<uintptr_t>(r) % 16 == 0) ? n / 4 : 0;
+  for (int64_t q = tid; q < n4; q += stride) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(r) + q);
+    count(x.x);
+    count(x.y);
+    count(x.z);
+    count(x.w);
   }
+  for (int64_t i = 4 * n4 + tid; i < n; i += stride) count(__ldg(r + i));
   __syncthreads();
   for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
     if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
@@ -407,6 +458,52 @@ __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int
 }
 
 constexpr int kSelectPasses = 3;
+
+// The whole select in one CTA for small score sets: the keys stay in shared memory.
+constexpr int kSmallSelect = 8192;
+
+__global__ void __launch_bounds__(kCalThreads) select_small_kernel(const float* r, int n,
+                                                                   int rank, float* out) {
+  __shared__ unsigned int keys[kSmallSelect];
+  __shared__ unsigned int h[kSelBins];
+  __shared__ unsigned int warp_tot[kCalThreads / 32];
+  __shared__ unsigned int s_prefix, s_want;
+  for (int i = threadIdx.x; i < n; i += kCalThreads) keys[i] = float_key(__ldg(r + i));
+  if (threadIdx.x == 0) {
+    s_prefix = 0u;
+    s_want = (unsigned int)rank;
+  }
+  constexpr int per = kSelBins / kCalThreads;
+  for (int pass = 0; pass < kSelectPasses; ++pass) {
+    const int width = pass == 2 ? 10 : 11;
+    const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+    const unsigned int mask = (1u << width) - 1u;
+    for (int b = threadIdx.x; b < kSelBins; b += kCalThreads) h[b] = 0;
+    __syncthreads();
+    const unsigned int prefix = s_prefix, want = s_want;
+    for (int i = threadIdx.x; i < n; i += kCalThreads) {
+      const unsigned int key = keys[i];
+      if (pass == 0 || (key >> (shift + width)) == prefix) atomicAdd(&h[(key >> shift) & mask], 1u);
+    }
+    __syncthreads();
+    unsigned int own[per];
+#pragma unroll
+    for (int i = 0; i < per; ++i) own[i] = h[threadIdx.x * per + i];
+    __syncthreads();
+    block_prefix_sums(h, kSelBins, warp_tot);
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int b = threadIdx.x * per + i;
+      const unsigned int before = h[b];
+      if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
+        s_prefix = (prefix << width) | (unsigned int)b;
+        s_want = want - before;
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = key_float(s_prefix);
+}
 
 __global__ void store_inf(float* out) { *out = __uint_as_float(0x7f800000u); }
 
@@ -463,15 +560,20 @@ extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
   A.acc = reinterpret_cast<unsigned int*>(ws + L.acc);
   A.bad = reinterpret_cast<unsigned int*>(ws + L.bad);
   A.cnt = reinterpret_cast<unsigned int*>(ws + L.cnt);
+  A.vec = aligned_to(gap, 16) && aligned_to(token, 16) && aligned_to(full_token, 16);
   const size_t smem = sweep_smem(T);
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  // enough CTAs to keep the loads in flight, at most four per SM
+  // every resident CTA slot of the GPU, but no more than one CTA per 2048 points
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel, kCalThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
   const int64_t want = ((int64_t)N + 8 * kCalThreads - 1) / (8 * kCalThreads);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 4LL * device_sms()));
+  const int64_t slots = (int64_t)std::max(per_sm, 1) * device_sms();
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
   sweep_kernel<<<grid, kCalThreads, smem, st>>>(A);
   return launch_status();
 }
@@ -526,15 +628,20 @@ extern "C" sv_status conformal_quantile(const float* resid, int n, double q, flo
   const double rk = std::ceil((double)(n + 1) * q);  // 1 <= rk <= n + 1
   const int64_t rank = (int64_t)rk;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
-  if (e != cudaSuccess) return cuda_fail(e);
-  SelectState* S = static_cast<SelectState*>(workspace);
   if (rank > (int64_t)n) {
     store_inf<<<1, 1, 0, st>>>(out_q);  // the rank is past the largest score
     return launch_status();
   }
-  const int64_t want = ((int64_t)n + 8 * kCalThreads - 1) / (8 * kCalThreads);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 2LL * device_sms()));
+  if (n <= kSmallSelect) {
+    select_small_kernel<<<1, kCalThreads, 0, st>>>(resid, n, (int)rank, out_q);
+    return launch_status();
+  }
+  cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  SelectState* S = static_cast<SelectState*>(workspace);
+  // every resident CTA slot (eight per SM), but no more than one CTA per 4096 scores
+  const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 8LL * device_sms()));
   for (int p = 0; p < kSelectPasses; ++p) {
     select_kernel<<<grid, kCalThreads, 0, st>>>(resid, n, rank, p, S, out_q);
     e = cudaGetLastError();

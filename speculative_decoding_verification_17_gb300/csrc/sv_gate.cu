@@ -83,6 +83,76 @@ __device__ __forceinline__ bool in_sorted(const int32_t* a, int n, int v) {
   return lo < n && __ldg(a + lo) == v;
 }
 
+// ---- the top two of a lane's ring stage, as a tournament of (largest, second) pairs ----
+// Two sets with tops (H1, L1) and (H2, L2) have top two H = max(H1, H2) and
+// L = max(min(H1, H2), max(L1, L2)) (a tie keeps both copies: the multiset's second largest).
+// The maxima propagate NaN, so a stage holding a NaN gives Ms = NaN and is rescanned.
+__device__ __forceinline__ uint32_t bmaxn2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float fmaxn(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// bf16: packed pairs, each 16-bit half keeping the top two of its own half of the stage.
+template <int N>
+__device__ __forceinline__ void stage_top2(const uint4 (&v)[N], float& Ms, float& ms) {
+  uint32_t H[2 * N], L[2 * N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    H[2 * i] = bmaxn2(v[i].x, v[i].y);
+    L[2 * i] = bmin2(v[i].x, v[i].y);
+    H[2 * i + 1] = bmaxn2(v[i].z, v[i].w);
+    L[2 * i + 1] = bmin2(v[i].z, v[i].w);
+  }
+#pragma unroll
+  for (int q = N; q >= 1; q >>= 1)
+#pragma unroll
+    for (int i = 0; i < q; ++i) {
+      const uint32_t h = bmaxn2(H[i], H[i + q]);
+      L[i] = bmaxn2(bmin2(H[i], H[i + q]), bmaxn2(L[i], L[i + q]));
+      H[i] = h;
+    }
+  const float ha = __uint_as_float(H[0] << 16), hb = __uint_as_float(H[0] & 0xffff0000u);
+  const float la = __uint_as_float(L[0] << 16), lb = __uint_as_float(L[0] & 0xffff0000u);
+  Ms = fmaxn(ha, hb);
+  ms = fmaxn(fminf(ha, hb), fmaxn(la, lb));
+}
+
+// fp32: the same tournament on the stage's 4N logits.
+template <int N>
+__device__ __forceinline__ void stage_top2_f32(const uint4 (&v)[N], float& Ms, float& ms) {
+  float H[2 * N], L[2 * N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float a = __uint_as_float(v[i].x), b = __uint_as_float(v[i].y);
+    const float c = __uint_as_float(v[i].z), d = __uint_as_float(v[i].w);
+    H[2 * i] = fmaxn(a, b);
+    L[2 * i] = fminf(a, b);
+    H[2 * i + 1] = fmaxn(c, d);
+    L[2 * i + 1] = fminf(c, d);
+  }
+#pragma unroll
+  for (int q = N; q >= 1; q >>= 1)
+#pragma unroll
+    for (int i = 0; i < q; ++i) {
+      const float h = fmaxn(H[i], H[i + q]);
+      L[i] = fmaxn(fminf(H[i], H[i + q]), fmaxn(L[i], L[i + q]));
+      H[i] = h;
+    }
+  Ms = H[0];
+  ms = L[0];
+}
+
 template <typename ET, bool kConformal = false>
 struct GateOp {
   using Args = GateArgs;
@@ -126,6 +196,21 @@ struct GateOp {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     acc.poison |= poison;
     Top2& t = acc.t;
+    // The stage's top two by a tournament (a NaN anywhere makes Ms NaN); folded into the
+    // lane's state, with the stage scanned for the index only when its maximum takes over.
+    float Ms, ms;
+    if constexpr (E::kPerVec == 8) stage_top2(v, Ms, ms);
+    else stage_top2_f32(v, Ms, ms);
+    if (Ms == Ms) {
+      const bool take = Ms > t.m1 || t.i1 == kNoIndex;
+      t.m2 = fmaxf(fminf(t.m1, Ms), fmaxf(t.m2, ms));
+      if (take) {
+        t.m1 = Ms;
+        t.i1 = first_index(v, j0, w, lane, Ms);
+      }
+      return;
+    }
+    // a stage with NaN entries (or the row's NaN-padded end): logit by logit, NaN skipped
 #pragma unroll
     for (int it = 0; it < T::kStageVec; ++it) {
       const int jb = (int)(j0 + (int64_t)warp_vec_slot<T::kStageVec>(w, it, lane) * E::kPerVec);
@@ -145,6 +230,19 @@ struct GateOp {
         }
       }
     }
+  }
+
+  // Lowest index of the lane's stage logits equal to M (one of them is).
+  __device__ static __forceinline__ int first_index(const uint4 (&v)[T::kStageVec], int64_t j0,
+                                                    int w, int lane, float M) {
+#pragma unroll
+    for (int it = 0; it < T::kStageVec; ++it) {
+      const int jb = (int)(j0 + (int64_t)warp_vec_slot<T::kStageVec>(w, it, lane) * E::kPerVec);
+#pragma unroll
+      for (int l = 0; l < E::kPerVec; ++l)
+        if (E::get(v[it], l) == M) return jb + l;
+    }
+    return kNoIndex;
   }
 
   __device__ static __forceinline__ void prologue(const Args&, const Seg&, Smem&) {}
