@@ -51,8 +51,8 @@ def measured_peaks():
 
 def source_digest(unit: str = "sv_verify.cu") -> str:
     """sha256 prefix of what the profiled kernel is built from: its translation unit, every
-    header it includes from the package or `include/` (recursively), and the build script
-    that holds the compiler flags."""
+    header it includes from the package or `include/` (recursively), and the statements of
+    the build script that set the compiler flags (ARCH, NVCC_FLAGS)."""
     pkg = os.path.join(ROOT, "speculative_decoding_verification_17_gb300")
     dirs = [os.path.join(pkg, "csrc"), os.path.join(ROOT, "include")]
     seen, todo = [], [unit]
@@ -71,8 +71,10 @@ def source_digest(unit: str = "sv_verify.cu") -> str:
         path = next(os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name)))
         with open(path, "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(pkg, "_native.py"), "rb") as f:
-        h.update(b"_native.py\0" + f.read())
+    with open(os.path.join(pkg, "_native.py")) as f:
+        build = f.read()
+    flags = re.findall(r"^(?:ARCH|NVCC_FLAGS) = .*?\n(?=\S|\n)", build, re.M | re.S)
+    h.update(b"_native.py\0" + "".join(flags).encode())
     return h.hexdigest()[:16]
 
 
@@ -684,6 +686,48 @@ def reference_arm(args, rank, world):
     print(json.dumps(line))
 
 
+def kernels_once():
+    """Two rounds of one launch of each secondary call, on workloads past L2, and nothing
+    timed: the command line for an ncu capture of those kernels. Round order: logit_gap_gate
+    (1280 fp32 rows of V=151936), spec_verify_greedy, draft_confidence_stop (top probability,
+    then inverse entropy) and conformal_admit (K=4) on the B=256 k=8 V=128256 bf16 batch,
+    conformal_residual (its draft rows against target rows 0..k-1), gate_risk_coverage (16M
+    points, 1024 thresholds) and conformal_quantile (16M scores)."""
+    import torch
+
+    import speculative_decoding_verification_17_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda")
+    d = synth.workload_inputs(HEAD, device=dev, B=256)
+    B, k, V = d["B"], d["k"], d["V"]
+    w2 = synth.workload_inputs(2, device=dev)
+    rows2 = w2["target"].reshape(-1, w2["V"])
+    tgt = d["target"][:, :k].contiguous()
+    ns = B * (k + 1) // 4
+    z4 = d["target"].reshape(-1, V)[: ns * 4].reshape(ns, 4, V)
+    Q4 = torch.tensor([3.0, 2.0, 1.5, 1.0], device=dev)
+    g = torch.Generator(device=dev).manual_seed(5)
+    npts = 1 << 24
+    gp = torch.rand((npts,), generator=g, device=dev) * 8
+    tk = torch.randint(0, 64, (npts,), generator=g, device=dev, dtype=torch.int32)
+    fl = torch.where(torch.rand((npts,), generator=g, device=dev) < 0.9, tk, tk + 1)
+    A = torch.arange(0, 64, 2, dtype=torch.int32, device=dev)
+    taus = torch.linspace(0, 8, 1024, device=dev)
+    rs = torch.rand((npts,), generator=g, device=dev)
+    for _ in range(2):
+        sv.logit_gap_gate(rows2, w2["tau"], w2["answer_set"])
+        sv.spec_verify_greedy(d["target"], d["draft_tokens"])
+        sv.draft_confidence_stop(d["draft"], d["T"], sv.SV_CONF_TOP_PROB, 0.05)
+        sv.draft_confidence_stop(d["draft"], d["T"], sv.SV_CONF_INV_ENTROPY, 0.2)
+        sv.conformal_admit(z4, Q4, want_gap=False)
+        sv.conformal_residual(d["draft"], tgt)
+        sv.gate_risk_coverage(gp, tk, fl, A, taus, 1.959964, 0.1)
+        sv.conformal_quantile(rs, 0.9)
+    torch.cuda.synchronize()
+    print("kernels-once ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -696,7 +740,12 @@ def main():
     ap.add_argument("--requests", type=int, default=None,
                     help="batch size of the headline workload (default: its own, 512)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--kernels-once", action="store_true",
+                    help="one untimed launch of each secondary call (for an ncu capture)")
     args = ap.parse_args()
+    if args.kernels_once:
+        kernels_once()
+        return
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
