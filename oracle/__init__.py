@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the benchma
 CPU-baseline leg are its only callers. The product library never imports, links or runs
 anything here, and the two share no code: the arithmetic lives in ``oracle.c`` (plain C,
 double precision, ascending-order sums), this module only builds it and marshals numpy
-arrays through ``ctypes``.
+arrays through ``ctypes``. ``ready_cache.py`` holds the ready-distribution cache as a plain
+sequential Python state machine over those functions.
 
 Logit arrays are numpy ``float32`` (dtype code 0) or ``uint16`` holding raw bfloat16 bit
 patterns (dtype code 1); :func:`as_logits` converts torch CPU tensors.

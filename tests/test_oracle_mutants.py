@@ -13,6 +13,7 @@ import pytest
 import oracle
 import test_oracle_calibration as K
 import test_oracle_confidence as C
+import test_oracle_ready_cache as RC
 import test_oracle_rules as R
 import test_oracle_sample as S
 
@@ -118,4 +119,50 @@ def test_planted_mistake_is_caught(workdir, name, old, new, pins):
                 pin()
             except (AssertionError, ValueError):
                 failures += 1
+    assert failures >= 1, f"no pin caught the planted mistake: {name}"
+
+
+# The ready-distribution cache oracle is Python: its mutants are edits of that module's source,
+# executed as a fresh module whose ReadyCache class the pins then use.
+PY_MUTANTS = [
+    ("gate fires at gamma == tau", 'if s["gap"] > float(np.float32(tau))',
+     'if s["gap"] >= float(np.float32(tau))',
+     [RC.test_gate_falls_through_on_a_small_gap_or_outside_the_answer_set]),
+    ("eligibility ignores the decision point",
+     'int(start[r]) == s["position"] - L and', "",
+     [RC.test_eligibility_is_an_exact_entry_match]),
+    ("skip keeps the old pre-position", 's["valid"] = s["decoded"] = s["consumed"] = False\n'
+     '                self.stats["skipped"] += 1', 'self.stats["skipped"] += 1',
+     [RC.test_budget_skip_leaves_no_ready_distribution]),
+    ("invalidation keeps the distribution", 's["valid"] = s["decoded"] = s["consumed"] = False\n'
+     '            s["epoch"] += 1', 's["epoch"] += 1',
+     [RC.test_invalidation_returns_to_no_ready_distribution,
+      RC.test_served_tokens_are_never_stale]),
+    ("every eligible request counts as a consumption", 'if not s["consumed"]:\n'
+     '                s["consumed"] = True\n                self.stats["consumed"] += 1',
+     's["consumed"] = True\n            self.stats["consumed"] += 1',
+     [lambda: RC.test_hit_rate_matches_eq8_for_memoryless_sessions(4.0)]),
+    ("decision point without the entry length", 's["position"] = n_s + L', 's["position"] = n_s',
+     [RC.test_record_then_fast_serve, RC.test_served_tokens_are_never_stale]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_mistake_in_the_cache_oracle_is_caught(monkeypatch, name, old, new, pins):
+    import types
+
+    import oracle.ready_cache as mod
+
+    src = open(mod.__file__).read()
+    assert src.count(old) == 1, f"mutation site not unique: {old!r}"
+    m = types.ModuleType("ready_cache_mutant")
+    m.__dict__["__package__"] = "oracle"
+    exec(compile(src.replace(old, new), "ready_cache_mutant", "exec"), m.__dict__)
+    monkeypatch.setattr(RC, "ReadyCache", m.ReadyCache)
+    failures = 0
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError, TypeError):
+            failures += 1
     assert failures >= 1, f"no pin caught the planted mistake: {name}"
