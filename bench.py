@@ -8,7 +8,8 @@ the logit bandwidth (each needed logit read once) against the measured HBM peak.
 
 Secondary rows time the other calls of the hot path on their own workloads (greedy verify,
 logit-gap gate, n-gram proposal + greedy verify, the fp32 sampled verify, the draft
-confidence stop, the gate calibration sweep and the conformal residual, quantile and gate)
+confidence stop, the gate calibration sweep, the conformal residual, quantile and gate, and
+the ready-distribution cache's record and serve)
 with the same event timing; workloads that fit in L2 get an L2 flush before every timed
 launch.
 
@@ -515,6 +516,45 @@ def secondary_rows(args, dev, stream, peak, head=None):
             ms=ms, steps_per_s=ns / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
             bytes=nb)
         del z4, aws
+
+    # ready-distribution cache: record 2048 sessions from the headline's target rows (0.53 GB
+    # scanned; with the full distributions kept, as much again written), then serve 16384
+    # requests against them
+    if head is not None:
+        V = head["V"]
+        S, E = 2048, 16
+        zr = head["target"].reshape(-1, V)[:S]
+        g = torch.Generator(device=dev).manual_seed(6)
+        sid = torch.arange(S, dtype=torch.int32, device=dev)
+        ent = torch.randint(0, 1000, (S, E), generator=g, device=dev, dtype=torch.int32)
+        n_s = torch.randint(0, 4096, (S,), generator=g, device=dev)
+        L = torch.full((S,), E, dtype=torch.int32, device=dev)
+        Bh = torch.full((S,), 64, dtype=torch.int64, device=dev)
+        st_out = torch.empty((S,), dtype=torch.int32, device=dev)
+        rws = torch.zeros(sv.ready_cache_record_workspace(S, V, sv.SV_BF16), dtype=torch.uint8,
+                          device=dev)
+        for keep, tag in ((False, ""), (True, "_keep_dist")):
+            table = sv.ReadyCacheTable(S, E, dev, V=V, dist_dtype=torch.bfloat16,
+                                       keep_dist=keep)
+            ms = statistics.mean(time_launches(
+                lambda: table.record(sid, n_s, ent, L, Bh, zr, out_status=st_out,
+                                     workspace=rws, stream=stream), steps, 3, stream))
+            nb = S * V * 2 * (2 if keep else 1)
+            rows[f"ready_cache_record_s{S}_v{V}_bf16{tag}"] = dict(
+                ms=ms, sessions_per_s=S / (ms * 1e-3), gbs=gbs(nb, ms), frac=gbs(nb, ms) / peak,
+                bytes=nb)
+        R = 16384
+        rs = torch.randint(0, S, (R,), generator=g, device=dev, dtype=torch.int32)
+        rstart, rtok, rlen = n_s[rs.long()], ent[rs.long()], L[rs.long()]
+        A = torch.arange(0, V, 3, dtype=torch.int32, device=dev)
+        otok = torch.empty((R,), dtype=torch.int32, device=dev)
+        orea = torch.empty((R,), dtype=torch.int32, device=dev)
+        ms = statistics.mean(time_launches(
+            lambda: table.serve(rs, rstart, rtok, rlen, 2.0, A, out_token=otok, out_reason=orea,
+                                stream=stream), steps, 3, stream, flush))
+        rows[f"ready_cache_serve_r{R}"] = dict(ms=ms, requests_per_s=R / (ms * 1e-3),
+                                                us=ms * 1e3)
+        del table, rws, zr
 
     # gate calibration: risk-coverage sweep over 16M decision points and 1024 thresholds
     # (201 MB of inputs, past L2), and at the pre-positioning page's 128 points

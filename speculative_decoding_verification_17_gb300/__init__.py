@@ -24,6 +24,13 @@ Gate calibration and the conformal gate (C ABI in ``include/specverify_calib.h``
 - :func:`conformal_quantile` — the split-conformal quantile of those residuals.
 - :func:`conformal_admit`    — the earliest of K layers whose gap clears 2 Q.
 
+Ready-distribution cache (C ABI in ``include/specverify_cache.h``), through
+:class:`ReadyCacheTable`, which owns a device-resident table of session slots:
+
+- :meth:`ReadyCacheTable.record`     — pre-position on idle for a batch of sessions.
+- :meth:`ReadyCacheTable.serve`      — the confidence-gated fast path for a batch of requests.
+- :meth:`ReadyCacheTable.invalidate` — a mutation of the listed sessions' state.
+
 Workspaces: pass ``workspace=`` (a uint8 CUDA tensor of at least the size the matching
 ``*_workspace`` query returns, 256-byte aligned, not shared by calls in flight at the same
 time; it needs no initialisation), or let the binding keep one cached per (device, call)
@@ -47,6 +54,8 @@ __all__ = [
     "draft_confidence_stop", "SV_MAX_TAUS", "CALIB_POINT", "gate_risk_coverage_workspace",
     "gate_risk_coverage", "conformal_residual", "conformal_quantile_workspace",
     "conformal_quantile", "conformal_admit_workspace", "conformal_admit", "gate_points_dict",
+    "ReadyCacheTable", "ready_cache_record_workspace", "SV_CACHE_VALID", "SV_CACHE_DECODED",
+    "SV_CACHE_CONSUMED", "CACHE_STATS",
 ]
 
 SV_F32 = 0
@@ -388,6 +397,110 @@ def conformal_admit(logits, Q, *, out_layer=None, out_token=None, out_gap=None,
                                   _ptr(out_token), _ptr(out_gap), _ptr(ws), ws.numel(), h),
         "conformal_admit")
     return out_layer, out_token, out_gap
+
+
+# ---------------------------------------------------------------- ready-distribution cache
+SV_CACHE_VALID, SV_CACHE_DECODED, SV_CACHE_CONSUMED = 1, 2, 4
+CACHE_STATS = ("pre_positions", "skipped", "consumed", "wasted", "fast", "fall_invalid",
+               "fall_ineligible", "fall_gate", "bad")
+
+
+def ready_cache_record_workspace(M: int, V: int, dtype: int) -> int:
+    return int(library().ready_cache_record_workspace(M, V, dtype))
+
+
+class ReadyCacheTable:
+    """A device-resident table of S session slots (32 bytes each), entries of at most
+    max_entry tokens, and the table's event counters; with ``keep_dist`` also one stored
+    ready row of V logits per session. A new table is empty (zero-filled)."""
+
+    def __init__(self, S: int, max_entry: int, device, *, V: int | None = None,
+                 dist_dtype=None, keep_dist: bool = False):
+        self.S, self.max_entry = S, max_entry
+        self.slots = torch.zeros((S, 4), dtype=torch.int64, device=device)
+        self.device = self.slots.device  # with its index ("cuda" -> "cuda:0")
+        self.entry_store = torch.zeros((S, max_entry), dtype=torch.int32, device=self.device)
+        self.stats = torch.zeros((len(CACHE_STATS),), dtype=torch.int64, device=self.device)
+        self.dist = None
+        if keep_dist:
+            if V is None or dist_dtype is None:
+                raise ValueError("keep_dist needs V and dist_dtype")
+            self.dist = torch.zeros((S, V), dtype=dist_dtype, device=self.device)
+
+    def record(self, session, end_pos, entry_tokens, entry_len, headroom, ready_logits, *,
+               out_status=None, workspace=None, stream=None):
+        """Algorithm 1 for M sessions (distinct ids). Returns out_status [M] int32."""
+        M, V = ready_logits.shape
+        dev = self.device
+        code = _dtype_code(ready_logits)
+        _check_cuda("ready_logits", ready_logits, None, None, dev)
+        _check_cuda("session", session, torch.int32, (M,), dev)
+        _check_cuda("end_pos", end_pos, torch.int64, (M,), dev)
+        _check_cuda("entry_tokens", entry_tokens, torch.int32, (M, self.max_entry), dev)
+        _check_cuda("entry_len", entry_len, torch.int32, (M,), dev)
+        _check_cuda("headroom", headroom, torch.int64, (M,), dev)
+        if self.dist is not None:
+            _check_cuda("dist", self.dist, ready_logits.dtype, (self.S, V), dev)
+        if out_status is None:
+            out_status = torch.empty((M,), dtype=torch.int32, device=dev)
+        _check_cuda("out_status", out_status, torch.int32, (M,), dev)
+        h, st = _stream_handle(stream)
+        need = ready_cache_record_workspace(M, V, code)
+        ws = workspace if workspace is not None else _workspace("record", need, dev, st)
+        _ok(library().ready_cache_record(
+            _ptr(self.slots), _ptr(self.entry_store), self.S, self.max_entry, _ptr(self.stats),
+            _ptr(session), _ptr(end_pos), _ptr(entry_tokens), _ptr(entry_len), _ptr(headroom),
+            M, _ptr(ready_logits), code, V, _ptr(self.dist), _ptr(out_status), _ptr(ws),
+            ws.numel(), h), "ready_cache_record")
+        return out_status
+
+    def serve(self, session, start, req_tokens, req_len, tau: float, answer_set=None, *,
+              exact: bool = True, out_token=None, out_reason=None, stream=None):
+        """Algorithm 2 for R requests. Returns (token [R], reason [R]) int32."""
+        R = session.numel()
+        dev = self.device
+        _check_cuda("session", session, torch.int32, (R,), dev)
+        _check_cuda("start", start, torch.int64, (R,), dev)
+        _check_cuda("req_tokens", req_tokens, torch.int32, (R, self.max_entry), dev)
+        _check_cuda("req_len", req_len, torch.int32, (R,), dev)
+        if answer_set is not None:
+            _check_cuda("answer_set", answer_set, torch.int32, None, dev)
+        n_answer = 0 if answer_set is None else answer_set.numel()
+        if out_token is None:
+            out_token = torch.empty((R,), dtype=torch.int32, device=dev)
+        if out_reason is None:
+            out_reason = torch.empty((R,), dtype=torch.int32, device=dev)
+        _check_cuda("out_token", out_token, torch.int32, (R,), dev)
+        _check_cuda("out_reason", out_reason, torch.int32, (R,), dev)
+        h, _ = _stream_handle(stream)
+        _ok(library().ready_cache_serve(
+            _ptr(self.slots), _ptr(self.entry_store), self.S, self.max_entry, _ptr(self.stats),
+            _ptr(session), _ptr(start), _ptr(req_tokens), _ptr(req_len), R, float(tau),
+            _ptr(answer_set), n_answer, 1 if exact else 0, _ptr(out_token), _ptr(out_reason),
+            h), "ready_cache_serve")
+        return out_token, out_reason
+
+    def invalidate(self, session, *, stream=None):
+        """Section 3.6: the listed sessions' state mutated."""
+        n = session.numel()
+        _check_cuda("session", session, torch.int32, (n,), self.device)
+        h, _ = _stream_handle(stream)
+        _ok(library().ready_cache_invalidate(_ptr(self.slots), self.S, _ptr(self.stats),
+                                             _ptr(session), n, h), "ready_cache_invalidate")
+
+    def state(self) -> dict:
+        """The slots' fields as CPU numpy arrays (a device-to-host copy)."""
+        import numpy as np
+
+        raw = self.slots.detach().cpu().numpy().tobytes()
+        rec = np.frombuffer(raw, dtype=np.dtype([
+            ("position", "<i8"), ("gap", "<f8"), ("token", "<i4"), ("entry_len", "<i4"),
+            ("flags", "<u4"), ("epoch", "<u4")]))
+        return {k: rec[k].copy() for k in rec.dtype.names}
+
+    def counters(self) -> dict:
+        vals = self.stats.detach().cpu().tolist()
+        return dict(zip(CACHE_STATS, vals))
 
 
 # ------------------------------------------------------------------------------ confidence

@@ -140,3 +140,11 @@ def _declare(L):
     L.conformal_admit_workspace.argtypes = [I, I, I, I]
     L.conformal_admit.restype = I
     L.conformal_admit.argtypes = [P, I, I, I, I, P, P, P, P, P, Z, P]
+    L.ready_cache_record_workspace.restype = Z
+    L.ready_cache_record_workspace.argtypes = [I, I, I]
+    L.ready_cache_record.restype = I
+    L.ready_cache_record.argtypes = [P, P, I, I, P, P, P, P, P, P, I, P, I, I, P, P, P, Z, P]
+    L.ready_cache_serve.restype = I
+    L.ready_cache_serve.argtypes = [P, P, I, I, P, P, P, P, P, I, F, P, I, I, P, P, P]
+    L.ready_cache_invalidate.restype = I
+    L.ready_cache_invalidate.argtypes = [P, I, P, P, I, P]

@@ -158,6 +158,32 @@ def test_calibration_validation():
     assert L.conformal_admit_workspace(3, 0, 50, 1) == 0
 
 
+def test_ready_cache_validation():
+    L = sv.library()
+    ws = ctypes.c_void_p(0x100000)
+    SL = ctypes.c_void_p(0x200000)  # 32-byte aligned
+    rec = lambda **kw: L.ready_cache_record(
+        kw.get("slots", SL), kw.get("store", FAKE), kw.get("S", 8), kw.get("E", 4),
+        kw.get("stats", FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("M", 3), kw.get("z", FAKE),
+        kw.get("dtype", 1), kw.get("V", 100), None, None, kw.get("ws", ws),
+        kw.get("wsb", 1 << 30), None)
+    assert rec(M=-1) == INVALID and rec(V=1) == INVALID and rec(dtype=5) == INVALID
+    assert rec(S=0) == INVALID and rec(E=0) == INVALID and rec(E=5000) == INVALID
+    assert rec(slots=None) == INVALID and rec(slots=ctypes.c_void_p(0x200010)) == INVALID
+    assert rec(z=None) == INVALID and rec(wsb=8) == WORKSPACE and rec(M=0, z=None) == OK
+    srv = lambda **kw: L.ready_cache_serve(
+        SL, FAKE, kw.get("S", 8), 4, FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("R", 5), 1.0,
+        kw.get("A", None), kw.get("nA", 0), 1, kw.get("out", FAKE), FAKE, None)
+    assert srv(R=-1) == INVALID and srv(S=0) == INVALID and srv(nA=2) == INVALID
+    assert srv(out=None) == INVALID and srv(R=0, out=None) == OK
+    inv = lambda **kw: L.ready_cache_invalidate(SL, kw.get("S", 8), FAKE, kw.get("sess", FAKE),
+                                                kw.get("n", 2), None)
+    assert inv(n=-1) == INVALID and inv(S=0) == INVALID and inv(sess=None) == INVALID
+    assert inv(n=0, sess=None) == OK
+    assert L.ready_cache_record_workspace(4, 1000, 1) > 0
+    assert L.ready_cache_record_workspace(4, 1, 1) == 0
+
+
 def test_binding_raises_on_bad_input():
     import torch
 
