@@ -18,7 +18,6 @@
 //                      8192 scores in one CTA with the keys in shared memory, beyond that one
 //                      launch per pass whose last CTA picks the digit.
 #include <algorithm>
-#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -29,25 +28,12 @@
 #include "sv_host.h"
 
 namespace sv {
+
+int device_sm_count();  // sv_common.cu
+
 namespace {
 
 constexpr int kCalThreads = 256;
-
-// SMs of the current device (cached per device).
-int device_sms() {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64) {
-    const int c = cache[dev].load();
-    if (c > 0) return c;
-  }
-  int c = 0;
-  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
-    c = 152;
-  if (dev >= 0 && dev < 64) cache[dev].store(c);
-  return c;
-}
 
 // Wilson score interval of k successes in n trials at the normal quantile z, clamped to
 // [0, 1]; NaN for n = 0. Each operation is rounded on its own (the half-width's product is
@@ -572,7 +558,7 @@ extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel, kCalThreads, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const int64_t want = ((int64_t)N + 8 * kCalThreads - 1) / (8 * kCalThreads);
-  const int64_t slots = (int64_t)std::max(per_sm, 1) * device_sms();
+  const int64_t slots = (int64_t)std::max(per_sm, 1) * device_sm_count();
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
   sweep_kernel<<<grid, kCalThreads, smem, st>>>(A);
   return launch_status();
@@ -641,7 +627,7 @@ extern "C" sv_status conformal_quantile(const float* resid, int n, double q, flo
   SelectState* S = static_cast<SelectState*>(workspace);
   // every resident CTA slot (eight per SM), but no more than one CTA per 4096 scores
   const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 8LL * device_sms()));
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 8LL * device_sm_count()));
   for (int p = 0; p < kSelectPasses; ++p) {
     select_kernel<<<grid, kCalThreads, 0, st>>>(resid, n, rank, p, S, out_q);
     e = cudaGetLastError();

@@ -1,4 +1,6 @@
 // sv_common.cu — library-wide C ABI helpers: version, status names, last CUDA error.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "specverify.h"
@@ -12,6 +14,22 @@ namespace sv {
 sv_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return SV_ERR_CUDA;
+}
+
+// SMs of the current device (queried once per device; 152 if the query fails).
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load();
+    if (c > 0) return c;
+  }
+  int c = 0;
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+    c = 152;
+  if (dev >= 0 && dev < 64) cache[dev].store(c);
+  return c;
 }
 }  // namespace sv
 
