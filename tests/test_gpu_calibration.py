@@ -107,6 +107,27 @@ def test_sweep_edges():
     assert idx == -2
 
 
+def test_sweep_inputs_off_the_16_byte_grid():
+    # views one element into their buffers: the four-at-a-time loads give way to single ones
+    gap, token, full, A = _points(5003, 17, nan_every=7)
+    taus = np.linspace(0, 6, 33).astype(np.float32)
+    g = torch.empty(gap.size + 1, dtype=torch.float32, device=DEV)[1:]
+    t = torch.empty(gap.size + 1, dtype=torch.int32, device=DEV)[1:]
+    f = torch.empty(gap.size + 1, dtype=torch.int32, device=DEV)[1:]
+    g.copy_(torch.from_numpy(gap))
+    t.copy_(torch.from_numpy(token))
+    f.copy_(torch.from_numpy(full))
+    assert g.data_ptr() % 16 != 0
+    pts, idx = sv.gate_risk_coverage(g, t, f, _dev(A), _dev(taus), Z95, 0.2)
+    torch.cuda.synchronize()
+    got = sv.gate_points_dict(pts)
+    want = oracle.risk_coverage(gap, token, full, A, taus, Z95, 0.2)
+    np.testing.assert_array_equal(got["accepted"].numpy(), want["accepted"])
+    np.testing.assert_array_equal(got["wrong"].numpy(), want["wrong"])
+    np.testing.assert_array_equal(got["risk"].numpy(), want["risk"])
+    assert int(idx.item()) == want["tau_index"]
+
+
 def test_sweep_a_million_points():
     gap, token, full, A = _points(1 << 20, 21, n_vocab=120, nan_every=1001)
     taus = np.linspace(0.0, 8.0, 64).astype(np.float32)
@@ -191,6 +212,19 @@ def test_quantile_random(n, q):
     torch.cuda.synchronize()
     want = oracle.conformal_quantile(r, q)
     assert _same_f32(got.cpu().numpy(), [want]), (got.item(), want)
+
+
+def test_quantile_of_scores_off_the_16_byte_grid():
+    rng = np.random.default_rng(4)
+    r = rng.exponential(1.0, 100003).astype(np.float32)
+    buf = torch.empty(r.size + 3, dtype=torch.float32, device=DEV)
+    v = buf[3:]
+    v.copy_(torch.from_numpy(r))
+    assert v.data_ptr() % 16 != 0
+    for q in (0.5, 0.9, 0.999):
+        got = sv.conformal_quantile(v, q)
+        torch.cuda.synchronize()
+        assert _same_f32(got.cpu().numpy(), [oracle.conformal_quantile(r, q)])
 
 
 def test_quantile_reuses_its_workspace():
