@@ -121,7 +121,7 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
-  L.resid = o;   o = round_up(o + B * nch * kWarpsPerChunk * sizeof(double), 256);
+  L.resid = o;   o = round_up(o + B * nch * (2 * kWarpsPerChunk + 1) * sizeof(double), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);
   L.req_cnt = o; o = round_up(o + B * sizeof(unsigned int), 256);

@@ -58,131 +58,69 @@ __device__ __forceinline__ int64_t chunk_end(int64_t j0, int V) {
 }
 
 // ============================================================================================
-// In-order draw inside one chunk
+// In-order draw inside one sub-range of a chunk
 // ============================================================================================
-constexpr int kScanRounds = 8;  // rounds of 32 vectors in one warp's share of a chunk
-
 struct ScanSmem {
-  DF rt[kWarps * kScanRounds];  // round totals, in vocabulary order
-  int seg_last[kWarps];
-  int round;  // the round that holds the crossing, or -1
-  DF excl;    // the weight before it
   int result;
 };
 
-// Inverse-CDF draw inside the chunk that starts at j0: the first logit j, in vocabulary
-// order, whose running weight exceeds `target` (chunk units); when rounding leaves the
-// target at or past the chunk's total, the last logit with positive weight. Every consumer
-// thread must call this. Warp w owns the contiguous segment [j0 + w*kSeg, j0 + (w+1)*kSeg),
-// read in kScanRounds rounds of 32 coalesced 16-byte vectors; a lane sums its vector's
-// weights in order in fp32. The crossing is then found top down, in float-float sums:
-//  1. every warp reduces each of its rounds (a butterfly, the same total in every lane);
-//  2. one warp scans the kWarps*kScanRounds round totals for the crossing round;
-//  3. one warp scans that round's lane sums for the crossing lane, whose lane walks its
-//     vector.
-// Steps 2 and 3 add in other orders than step 1; where that moves the answer, the target
-// lies within rounding of a boundary, and the walk falls back to the round's (or chunk's)
-// last positive weight.
-// VW provides: using Raw; Raw load(int64_t j) const; void weights(const Raw&, float (&)[]),
-// with zero weight past the end of the row.
-template <typename E, typename VW>
-__device__ int scan_chunk(int64_t j0, double target, bool take_last, const VW& vw,
-                          ScanSmem& sm) {
-  constexpr int kSeg = E::kChunk / kWarps;
+// Inverse-CDF draw inside the sub-range that starts at s0 (kRounds rounds of 32 16-byte
+// vectors; the weights are zero past its end): the first logit j, in vocabulary order, whose
+// running weight exceeds `target` (in the sub-range's units); when rounding leaves the target
+// at or past the sub-range's total, or take_last is set, the last logit with positive weight.
+// One warp walks the rounds in order: a lane sums its vector's weights in order in fp32, a
+// float-float warp scan of the lane sums places the crossing lane, and that lane walks its
+// vector. The scan adds in another order than the masses that chose the sub-range; where
+// that moves the answer, the target lies within rounding of a boundary, and the walk falls
+// back to the last positive weight. Every consumer thread calls this; warp 0 works.
+// VW provides: using Raw; Raw load(int64_t j) const; void weights(const Raw&, float (&)[]).
+template <typename E, int kRounds, typename VW>
+__device__ int scan_sub(int64_t s0, double target, bool take_last, const VW& vw,
+                        ScanSmem& sm) {
   constexpr int kRound = 32 * E::kPerVec;
-  constexpr int kRounds = kSeg / kRound;
-  constexpr int kBatch = 2;  // rounds loaded at once
-  static_assert(kRounds == kScanRounds && kRounds % kBatch == 0, "whole rounds and batches");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t seg0 = j0 + (int64_t)warp * kSeg;
-
-  // ---- 1. lane sums and round totals (every warp) ----
-  float ls[kRounds];
-  int lastpos = -1;
-#pragma unroll
-  for (int b = 0; b < kRounds; b += kBatch) {
-    typename VW::Raw raw[kBatch];
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q)
-      raw[q] = vw.load(seg0 + (b + q) * kRound + lane * E::kPerVec);
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      float w[E::kPerVec];
-      vw.weights(raw[q], w);
-      float acc = 0.0f;
-#pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) {
-        acc += w[l];
-        if (w[l] > 0.0f) lastpos = (int)(seg0 + (b + q) * kRound + lane * E::kPerVec + l);
-      }
-      ls[b + q] = acc;
-    }
-  }
-  DF t[kRounds];
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) t[r] = DF{ls[r], 0.0f};
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int r = 0; r < kRounds; ++r) t[r] = df_add(t[r], df_shfl_xor(t[r], o));
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r)
-    if (lane == r) sm.rt[warp * kRounds + r] = t[r];
-  lastpos = __reduce_max_sync(0xffffffffu, lastpos);
-  if (lane == 0) sm.seg_last[warp] = lastpos;
-  cbar();
-
-  if (warp == 0) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     const DF tgt = df_from_double(target);
-    // ---- 2. the crossing round (lane l holds round totals 2l and 2l+1) ----
-    const DF e0 = sm.rt[2 * lane], e1 = sm.rt[2 * lane + 1];
-    const DF incl = df_warp_scan(df_add(e0, e1));
-    DF ex = df_shfl_up(incl, 1);
-    if (lane == 0) ex = DF{0.0f, 0.0f};
-    const DF p0 = df_add(ex, e0), p1 = df_add(p0, e1);
-    const unsigned b0 = __ballot_sync(0xffffffffu, !take_last && e0.hi > 0.0f && df_gt(p0, tgt));
-    const unsigned b1 = __ballot_sync(0xffffffffu, !take_last && e1.hi > 0.0f && df_gt(p1, tgt));
-    int first = 0x7fffffff;
-    if (b0) first = 2 * (__ffs(b0) - 1);
-    if (b1) first = min(first, 2 * (__ffs(b1) - 1) + 1);
-    int last = sm.seg_last[lane < kWarps ? lane : 0];
-    last = __reduce_max_sync(0xffffffffu, last);
-    if (first == 0x7fffffff) {
-      if (lane == 0) sm.result = last;
-    } else {
-      const float before = __shfl_sync(0xffffffffu, (first & 1) ? p0.hi : ex.hi, first >> 1);
-      const float before_lo = __shfl_sync(0xffffffffu, (first & 1) ? p0.lo : ex.lo, first >> 1);
-      // ---- 3. the crossing lane of that round, then the logit in its vector ----
-      const int w = first / kRounds, r = first - w * kRounds;
-      const int64_t base = j0 + (int64_t)w * kSeg + (int64_t)r * kRound;
-      const typename VW::Raw raw = vw.load(base + lane * E::kPerVec);
+    DF run{0.0f, 0.0f};
+    int lastpos = -1, found = -1;
+    for (int r = 0; r < kRounds && found < 0; ++r) {  // warp-uniform
+      const int64_t base = s0 + (int64_t)r * kRound + lane * E::kPerVec;
+      const typename VW::Raw raw = vw.load(base);
       float wt[E::kPerVec];
       vw.weights(raw, wt);
       float acc = 0.0f;
+      int lp = -1;
 #pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) acc += wt[l];
-      const DF li = df_warp_scan(DF{acc, 0.0f});
-      DF lex = df_shfl_up(li, 1);
-      if (lane == 0) lex = DF{0.0f, 0.0f};
-      const DF start = df_add(DF{before, before_lo}, lex);
-      const DF through = df_add(start, DF{acc, 0.0f});
-      const unsigned bl = __ballot_sync(0xffffffffu, acc > 0.0f && df_gt(through, tgt));
-      const unsigned pos = __ballot_sync(0xffffffffu, acc > 0.0f);
-      const int L = bl ? __ffs(bl) - 1 : (pos ? 31 - __clz(pos) : 0);
-      if (lane == L) {
-        DF run = start;
-        int tk = -1, lp = -1;
-#pragma unroll
-        for (int l = 0; l < E::kPerVec; ++l) {
-          run = df_add(run, DF{wt[l], 0.0f});
-          if (wt[l] > 0.0f) {
-            lp = (int)(base + lane * E::kPerVec + l);
-            if (tk < 0 && df_gt(run, tgt)) tk = lp;
-          }
-        }
-        sm.result = tk >= 0 ? tk : (lp >= 0 ? lp : last);
+      for (int l = 0; l < E::kPerVec; ++l) {
+        acc += wt[l];
+        if (wt[l] > 0.0f) lp = (int)(base + l);
       }
+      lastpos = max(lastpos, __reduce_max_sync(0xffffffffu, lp));
+      const DF incl = df_warp_scan(DF{acc, 0.0f});
+      DF lex = df_shfl_up(incl, 1);
+      if (lane == 0) lex = DF{0.0f, 0.0f};
+      const DF start = df_add(run, lex);
+      const DF through = df_add(start, DF{acc, 0.0f});
+      const unsigned bl =
+          __ballot_sync(0xffffffffu, !take_last && acc > 0.0f && df_gt(through, tgt));
+      if (bl) {
+        const int L = __ffs(bl) - 1;
+        int tk = -1;
+        if (lane == L) {
+          DF rr = start;
+#pragma unroll
+          for (int l = 0; l < E::kPerVec; ++l) {
+            rr = df_add(rr, DF{wt[l], 0.0f});
+            if (wt[l] > 0.0f && tk < 0 && df_gt(rr, tgt)) tk = (int)(base + l);
+          }
+          if (tk < 0) tk = lp;  // rounding inside the vector: its last positive weight
+        }
+        found = __shfl_sync(0xffffffffu, tk, L);
+      }
+      run = df_add(run, DF{__shfl_sync(0xffffffffu, incl.hi, 31),
+                           __shfl_sync(0xffffffffu, incl.lo, 31)});
     }
+    if (lane == 0) sm.result = found >= 0 ? found : lastpos;
   }
   cbar();
   return sm.result;
@@ -248,7 +186,7 @@ struct SampleArgs {
   float* out_resid;
   WarpSoftmax* part;  // [B * (2k+1)][nseg][kWarps]
   RowSoftmax* row;
-  DF* resid;          // [B][nch][kWarps] per-warp chunk masses of the request's draw
+  DF* resid;          // [B][nch * (2 * kWarps + 1)] sub-range then chunk masses of a draw
   unsigned int* row_cnt;
   unsigned int* req_cnt;
 };
@@ -372,41 +310,17 @@ struct DrawRing {
   static_assert(kVecPerLane >= 1, "a piece gives every thread at least one vector");
 };
 
-// Per-warp masses of every chunk of the rows of VW, into part[c][warp]; false if a copy
-// never landed (the masses are then NaN). With the TMA ring (aligned rows) the rows stream
-// through the two halves of the ring a piece at a time: a half holds the same piece of every
-// row, one bulk copy each, completing on its barrier, and the last warp out of a half starts
-// the copy of the piece two ahead. Without it, every thread loads its vectors from global
-// memory. Every thread calls this.
+// Masses of every sub-range of the rows of VW, into part[h * kWarps + warp]: piece h of the
+// rows (DrawRing's pieces, kPiecesPerChunk per chunk) splits into kWarps contiguous
+// sub-ranges of kVecPerLane*32 vectors, and warp w sums the w-th; false if a copy never
+// landed (the masses are then NaN). With the TMA ring (aligned rows) the rows stream through
+// the two halves of the ring a piece at a time: a half holds the same piece of every row, one
+// bulk copy each, completing on its barrier, and the last warp out of a half starts the copy
+// of the piece two ahead. Without it, every thread loads its vectors from global memory.
+// Every thread calls this.
 template <typename E, int RingBytes, class VW>
 __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!ring.usable || !SV_RESID_RING) {
-    for (int c = 0; c < nch; ++c) {
-      const int64_t j0 = (int64_t)c * E::kChunk;
-      VW q = vw;
-      q.j1 = chunk_end<E>(j0, V);
-      float acc = 0.0f;
-#pragma unroll
-      for (int h = 0; h < kVecPerThread; h += 2) {
-        typename VW::Raw raw[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          raw[t] = q.load(j0 + (int64_t)((h + t) * kThreads + tid) * E::kPerVec);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float w[E::kPerVec];
-          q.weights(raw[t], w);
-#pragma unroll
-          for (int l = 0; l < E::kPerVec; ++l) acc += w[l];
-        }
-      }
-      float hi = acc, lo = 0.0f;
-      warp_sum_compensated(hi, lo);
-      if (lane == 0) part[(int64_t)c * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
-    }
-    return true;
-  }
   using DR = DrawRing<VW, RingBytes>;
   constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
   constexpr int kPer = DR::kPiecesPerChunk;
@@ -416,6 +330,44 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
     b = (int64_t)(h / kPer) * E::kChunk + (int64_t)(h % kPer) * kPieceElems;
     e = b + kPieceElems < V ? b + kPieceElems : (int64_t)V;
   };
+  // each vector's weights in a pairwise tree of packed fp32x2 adds, then into the lane's
+  // running pair; a piece's warp sum is the mass of its sub-range
+  auto fold = [&](const typename VW::Raw (&raw)[kVec], float2& acc2) {
+#pragma unroll
+    for (int it = 0; it < kVec; ++it) {
+      float w[E::kPerVec];
+      vw.weights(raw[it], w);
+      float2 t[E::kPerVec / 2];
+#pragma unroll
+      for (int p = 0; p < E::kPerVec / 2; ++p) t[p] = make_float2(w[2 * p], w[2 * p + 1]);
+#pragma unroll
+      for (int q = E::kPerVec / 4; q >= 1; q >>= 1)
+#pragma unroll
+        for (int p = 0; p < q; ++p) t[p] = __fadd2_rn(t[p], t[p + q]);
+      acc2 = __fadd2_rn(acc2, t[0]);
+    }
+  };
+  auto store = [&](int h, float2 acc2) {
+    float hi = acc2.x + acc2.y, lo = 0.0f;
+    warp_sum_compensated(hi, lo);
+    if (lane == 0) part[(int64_t)h * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
+  };
+  if (!ring.usable || !SV_RESID_RING) {
+    for (int h = 0; h < np; ++h) {
+      int64_t b, e;
+      piece(h, b, e);
+      VW q = vw;
+      q.j1 = e;
+      typename VW::Raw raw[kVec];
+#pragma unroll
+      for (int it = 0; it < kVec; ++it)
+        raw[it] = q.load(b + (int64_t)(warp * (kVec * 32) + it * 32 + lane) * E::kPerVec);
+      float2 acc2 = make_float2(0.0f, 0.0f);
+      fold(raw, acc2);
+      store(h, acc2);
+    }
+    return true;
+  }
   auto issue = [&](int h) {
     const int st = h & 1;
     int64_t b, e;
@@ -431,7 +383,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
     for (int i = 0; i < VW::kRows; ++i) {
       void* dst = ring.buf + st * DR::kHalf + i * DR::kPieceBytes;
       const void* src = static_cast<const char*>(vw.row(i)) + b * (16 / E::kPerVec);
-      if (SV_L2_KEEP_POS > 0 && DR::kStagedScan)
+      if (SV_L2_KEEP_POS > 0)
         bulk_g2s(dst, src, bytes, &ring.full[st], l2_policy(false));  // the rows' last read
       else
         bulk_g2s(dst, src, bytes, &ring.full[st]);
@@ -440,7 +392,6 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
   if (tid == 0)
     for (int h = 0; h < 2 && h < np; ++h) issue(h);
   // every thread follows the same barrier phases
-  float2 acc2 = make_float2(0.0f, 0.0f);
   bool timed_out = false;
   for (int h = 0; h < np; ++h) {
     const int st = h & 1;
@@ -462,34 +413,15 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
       ring.released[st] = 0;
       if (h + 2 < np) issue(h + 2);
     }
-    // each vector's weights in a pairwise tree of packed fp32x2 adds, then into the
-    // lane's running pair (the chunk masses only choose the chunk; the scan recomputes)
-#pragma unroll
-    for (int it = 0; it < kVec; ++it) {
-      float w[E::kPerVec];
-      vw.weights(raw[it], w);
-      float2 t[E::kPerVec / 2];
-#pragma unroll
-      for (int p = 0; p < E::kPerVec / 2; ++p) t[p] = make_float2(w[2 * p], w[2 * p + 1]);
-#pragma unroll
-      for (int q = E::kPerVec / 4; q >= 1; q >>= 1)
-#pragma unroll
-        for (int p = 0; p < q; ++p) t[p] = __fadd2_rn(t[p], t[p + q]);
-      acc2 = __fadd2_rn(acc2, t[0]);
-    }
-    if (h % kPer == kPer - 1) {  // every piece of chunk h / kPer is in
-      float hi = acc2.x + acc2.y, lo = 0.0f;
-      warp_sum_compensated(hi, lo);
-      if (lane == 0)
-        part[(int64_t)(h / kPer) * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
-      acc2 = make_float2(0.0f, 0.0f);
-    }
+    float2 acc2 = make_float2(0.0f, 0.0f);
+    fold(raw, acc2);
+    store(h, acc2);
   }
   if (__any_sync(0xffffffffu, timed_out)) {
     if (lane == 0) {
       atomicOr(&ring.ctl->error, 1u);
-      for (int c = 0; c < nch; ++c)
-        part[(int64_t)c * kWarps + warp] = DF{__int_as_float(0x7fc00000), 0.0f};
+      for (int h = 0; h < np; ++h)
+        part[(int64_t)h * kWarps + warp] = DF{__int_as_float(0x7fc00000), 0.0f};
     }
     return false;
   }
@@ -527,7 +459,7 @@ struct SampleOp {
     int a, err, chunk, take_last;
     double W, before;
     ScanSmem scan;
-    DF cm[kSmemChunks * kWarps];  // per-warp chunk masses of the draw
+    DF cm[kSmemChunks * (2 * kWarps + 1)];  // the draw's sub-range masses, then chunk masses
   };
   // One lane's running softmax sum over the segment: hi + lo (an unevaluated pair) in units
   // of 2^K, K an integer with K >= s * (the largest logit seen), and whether it saw a NaN,
@@ -754,17 +686,23 @@ template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                                   Ring& ring, int& t, double& W) {
   const int tid = threadIdx.x, lane = tid & 31;
+  using DR = DrawRing<VW, T::kRingBytes>;
+  constexpr int kSubs = DR::kPiecesPerChunk * kWarps;  // sub-ranges of a chunk
+  constexpr int kSubElems = DR::kVecPerLane * 32 * E::kPerVec;
+  constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
+  static_assert(kSubs <= 32, "one warp holds a chunk's sub-range masses");
   const bool landed = chunk_masses<E, T::kRingBytes>(A.nch, A.V, vw, part, ring);
   __syncthreads();
-  // chunk masses M_c = sum over warps (fixed order), and W = sum_c M_c (warp 0), all in
-  // float-float sums
+  // the chunk masses M_c = sum of the chunk's sub-range masses (fixed order), and
+  // W = sum_c M_c (warp 0), all in float-float sums; M_c goes after the sub-range masses
+  DF* cmass = part + (int64_t)A.nch * kSubs;
   if (tid < 32) {
     DF wsum{0.0f, 0.0f};
     for (int c = lane; c < A.nch; c += 32) {
       DF mc{0.0f, 0.0f};
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) mc = df_add(mc, part[(int64_t)c * kWarps + w]);
-      part[(int64_t)c * kWarps] = mc;
+      for (int q = 0; q < kSubs; ++q) mc = df_add(mc, part[(int64_t)c * kSubs + q]);
+      cmass[c] = mc;
       wsum = df_add(wsum, mc);
     }
 #pragma unroll
@@ -777,42 +715,56 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
   if (!(W > 0.0)) return kDrawNoMass;
   const double target = (double)u * W;
   if (tid < 32) {
+    // the chunk in which u*W falls, then the sub-range of that chunk (one lane per sub-range)
     DF before;
     bool tl;
-    const int c = pick_chunk(
-        A.nch, df_from_double(target), [&](int cc) { return part[(int64_t)cc * kWarps]; },
-        before, tl);
+    int c = pick_chunk(A.nch, df_from_double(target), [&](int cc) { return cmass[cc]; },
+                       before, tl);
+    c = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
+    const double tc = target - ((double)before.hi + (double)before.lo);
+    const DF tcd = df_from_double(tc);
+    const DF m = lane < kSubs ? part[(int64_t)c * kSubs + lane] : DF{0.0f, 0.0f};
+    const DF incl = df_warp_scan(m);
+    DF ex = df_shfl_up(incl, 1);
+    if (lane == 0) ex = DF{0.0f, 0.0f};
+    const unsigned bal =
+        __ballot_sync(0xffffffffu, !tl && lane < kSubs && m.hi > 0.0f && df_gt(incl, tcd));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < kSubs && m.hi > 0.0f);
+    const int q = bal ? __ffs(bal) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const DF exq = DF{__shfl_sync(0xffffffffu, ex.hi, q), __shfl_sync(0xffffffffu, ex.lo, q)};
     if (lane == 0) {
-      sm.chunk = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
-      sm.before = (double)before.hi + (double)before.lo;
-      sm.take_last = tl;
+      sm.chunk = c * kSubs + q;
+      sm.before = tc - ((double)exq.hi + (double)exq.lo);
+      sm.take_last = tl || !bal;
     }
   }
   __syncthreads();
-  const int64_t j0 = (int64_t)sm.chunk * E::kChunk;
-  VW q = vw;
-  q.j1 = chunk_end<E>(j0, A.V);
-  if (!ring.usable || !DrawRing<VW, T::kRingBytes>::kStagedScan) {
-    t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, q, sm.scan);
+  const int c = sm.chunk / kSubs, q = sm.chunk - (sm.chunk / kSubs) * kSubs;
+  const int64_t s0 = (int64_t)c * E::kChunk + (int64_t)(q / kWarps) * kPieceElems +
+                     (int64_t)(q % kWarps) * kSubElems;
+  VW sq = vw;
+  sq.j1 = s0 + kSubElems < A.V ? s0 + kSubElems : (int64_t)A.V;
+  if (!ring.usable) {
+    t = scan_sub<E, DR::kVecPerLane>(s0, sm.before, sm.take_last != 0, sq, sm.scan);
     return kDrawOk;
   }
-  // nobody reads the ring any more (the barrier above): stage the chunk of every row
+  // nobody reads the ring any more (the barrier above): stage the sub-range of every row
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)((q.j1 - j0) * (16 / E::kPerVec));
+    const uint32_t bytes = (uint32_t)((sq.j1 - s0) * (16 / E::kPerVec));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < VW::kRows; ++i) {
       mbar_arrive_expect_tx(&ring.full[i], bytes);
       bulk_g2s(ring.buf + i * kChunkBytes,
-               static_cast<const char*>(vw.row(i)) + j0 * (16 / E::kPerVec), bytes,
+               static_cast<const char*>(vw.row(i)) + s0 * (16 / E::kPerVec), bytes,
                &ring.full[i]);
     }
   }
   bool ok = true;
 #pragma unroll
   for (int i = 0; i < VW::kRows; ++i) ok &= ring_wait(ring, i);
-  const StagedScan<E, VW> ss{&q, ring.buf, j0, q.j1};
-  t = scan_chunk<E>(j0, target - sm.before, sm.take_last != 0, ss, sm.scan);
+  const StagedScan<E, VW> ss{&sq, ring.buf, s0, sq.j1};
+  t = scan_sub<E, DR::kVecPerLane>(s0, sm.before, sm.take_last != 0, ss, sm.scan);
   if (!__syncthreads_and(ok)) {
     if (tid == 0) atomicOr(&ring.ctl->error, 1u);
     return kDrawFailed;
@@ -875,9 +827,9 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   if (!sm.err) {
     const float s = A.s;
     const float uk = __ldg(u + A.k);
-    DF* part = A.nch <= kSmemChunks  // [nch][kWarps]
+    DF* part = A.nch <= kSmemChunks  // [nch][up to 2 * kWarps], then [nch]
                        ? sm.cm
-                       : A.resid + (int64_t)r * A.nch * kWarps;
+                       : A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
     st = kDrawNoMass;
     if (a < n) {
       // ---- residual norm(max(0, p_a - q_a)) ----
