@@ -36,6 +36,12 @@ if ROOT not in sys.path:
 
 METRIC = "verified draft positions/sec and logit GB/s (fraction of GB300 HBM peak)"
 HEAD = 3  # index of the headline workload in synth.WORKLOADS
+# The sampled-verify workloads whose inputs exceed L2 (timed back to back without a flush):
+# the headline (B=512, k=8, V=128256 bf16) and the fp32 one (B=256, k=4, V=151936).
+TIMED_WORKLOADS = {
+    3: "z_p~N(0,2.5^2), z_q=0.6 z_p+N(0,1.5^2)",
+    2: "z_p~N(0,3^2) plus one planted peak +U(2,10) per row, z_q=z_p+N(0,0.7^2)",
+}
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
@@ -228,11 +234,11 @@ def init_ranks(world: int, device):
     return dist
 
 
-def rank_seed(rank: int) -> int:
+def rank_seed(rank: int, workload: int = HEAD) -> int:
     """Seed of a rank's shard of requests: every rank verifies its own batch."""
     import synth
 
-    return synth.SEED_BASE + HEAD + 7919 * rank
+    return synth.SEED_BASE + workload + 7919 * rank
 
 
 def max_over_ranks(dist, x: float, device) -> float:
@@ -264,13 +270,14 @@ def gb300_arm(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     dist = init_ranks(world, dev)
 
-    w = synth.WORKLOADS[HEAD]
-    d = synth.workload_inputs(w, device=dev, seed=rank_seed(rank), B=args.requests)
+    w = synth.WORKLOADS[args.workload]
+    d = synth.workload_inputs(w, device=dev, seed=rank_seed(rank, args.workload), B=args.requests)
     B, k, V = d["B"], d["k"], d["V"]
     n_total = B * k  # every request drafts k tokens in this workload
     elem = w.elem_bytes
     stream = torch.cuda.Stream(device=dev)
-    ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+    code = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
+    ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, code), dtype=torch.uint8,
                      device=dev)
     outs = dict(out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
                 out_accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
@@ -378,11 +385,11 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": w.dtype,
             "data": "synthetic (seeded; shapes and value distributions of the workload)",
             "config": {
-                "workload": f"sampled verify {w.name}: B={B}, k={k}, V={V}, bf16 logits, T={w.T}, "
-                            "z_p~N(0,2.5^2), z_q=0.6 z_p+N(0,1.5^2)",
+                "workload": f"sampled verify {w.name}: B={B}, k={k}, V={V}, {w.dtype} logits, "
+                            f"T={w.T}, {TIMED_WORKLOADS[w.index]}",
                 "global_batch": B * world,
                 "draft_positions_per_step": n_total * world,
                 "logit_bytes_per_step": abytes,
@@ -393,14 +400,14 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
             "mean_accept_len": acc,
             "roofline": {
                 "bound": "hbm",
-                "kernel": "segment_kernel<SampleOp<BF16>>",
+                "kernel": f"segment_kernel<SampleOp<{'F32' if w.dtype == 'f32' else 'BF16'}>>",
                 "achieved": achieved,
                 "peak": peak,
                 "unit": "GB/s",
                 "frac": achieved / peak,
                 "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "traffic": profiled_traffic("segment_kernel_sample", "b512_k8_v128256_bf16"),
+                "traffic": profiled_traffic("segment_kernel_sample", f"b{B}_k{k}_v{V}_{w.dtype}"),
                 "algorithmic_bytes_per_launch": abytes,
                 "launch_ms": mean_ms,
             },
@@ -686,13 +693,14 @@ def reference_arm(args, rank, world):
         return
     import synth
 
-    w = synth.WORKLOADS[HEAD]
+    w = synth.WORKLOADS[args.workload]
     e = w.extra
     threads = os.cpu_count() or 1
     per_step = max(threads, 16)
     d = synth.sample_inputs(per_step, w.k, w.V, w.dtype, w.T, device="cpu",
-                            seed=synth.SEED_BASE + HEAD, target_std=e["target_std"],
-                            draft_noise=e["draft_noise"], draft_scale=e["draft_scale"])
+                            seed=synth.SEED_BASE + w.index, target_std=e["target_std"],
+                            draft_noise=e["draft_noise"], draft_scale=e["draft_scale"],
+                            peak=e.get("peak"))
     for _ in range(args.warmup):
         _oracle_sample_rate(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], w.T,
                             threads)
@@ -714,8 +722,9 @@ def reference_arm(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and value distributions of the workload)",
-        "config": {"workload": f"sampled verify {w.name}: B={w.B}, k={w.k}, V={w.V}, bf16 logits, "
-                               f"T={w.T}; each step a bounded sample of {per_step} requests",
+        "config": {"workload": f"sampled verify {w.name}: B={w.B}, k={w.k}, V={w.V}, "
+                               f"{w.dtype} logits, T={w.T}, {TIMED_WORKLOADS[w.index]}; each step "
+                               f"a bounded sample of {per_step} requests",
                    "global_batch": per_step, "parallelism": f"{threads} host threads"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": threads,
                          "kind": "oracle",
@@ -777,8 +786,10 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", type=int, choices=sorted(TIMED_WORKLOADS), default=HEAD,
+                    help="the sampled-verify workload to time (default: the headline, 3)")
     ap.add_argument("--requests", type=int, default=None,
-                    help="batch size of the headline workload (default: its own, 512)")
+                    help="batch size of the timed workload (default: its own)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--kernels-once", action="store_true",
                     help="one untimed launch of each secondary call (for an ncu capture)")
