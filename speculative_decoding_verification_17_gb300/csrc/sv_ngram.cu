@@ -12,6 +12,11 @@
 // occurrence has length max_e l_e, and its earliest occurrence is the smallest e reaching
 // that maximum, which is the result of the page's longest-first search. One CTA per
 // request; a single packed (l_e, -e) maximum picks the winner.
+//
+// The history streams through shared memory in tiles of kTile end positions, each with the
+// n_max - 1 tokens before it: every thread issues its asynchronous 4-byte copies of a tile
+// at once (cp.async, no register round trip), so a tile costs one memory latency, and the
+// match counts then read shared memory only.
 #include <cstdint>
 
 #include "specverify.h"
@@ -22,12 +27,22 @@ namespace sv {
 
 constexpr int kNgramThreads = 256;
 constexpr int kMaxPhrase = 64;
+constexpr int kTile = 8192;  // end positions per shared-memory tile (32 KiB of tokens)
+
+__device__ __forceinline__ void cp_async4(int32_t* dst, const int32_t* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(
     const int32_t* __restrict__ history, const int32_t* __restrict__ hist_len, int L_max,
     int n_max, int n_min, int k, int32_t* __restrict__ out_draft,
     int32_t* __restrict__ out_num) {
   __shared__ int32_t suffix[kMaxPhrase];
+  __shared__ int32_t tile[kTile + kMaxPhrase];
   __shared__ unsigned int s_best[kNgramThreads / 32];
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -40,20 +55,31 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(
   }
   const int32_t* h = history + (int64_t)r * L_max;
   const int ns = n_max < L ? n_max : L;
-  if (tid < ns) suffix[tid] = __ldg(h + L - 1 - tid);  // suffix[t] = h[L-1-t]
-  __syncthreads();
+  // suffix[t] = h[L-1-t], copied along with the first tile
+  if (tid < ns) cp_async4(suffix + tid, h + L - 1 - tid);
 
   // key = (l_e << 24) | (2^24 - 1 - e): the larger match first, then the smaller e
   unsigned int best = 0;
-  for (int e = n_min - 1 + tid; e <= L - 2; e += kNgramThreads) {
-    int m = 0;
-    const int cap = n_max < e + 1 ? n_max : e + 1;
-    while (m < cap && __ldg(h + e - m) == suffix[m]) ++m;
-    if (m >= n_min) {
-      const unsigned int key = ((unsigned)m << 24) | (0xffffffu - (unsigned)e);
-      best = key > best ? key : best;
+  int lo = 0, t1 = 0;  // the tile in shared memory holds tokens [lo, t1)
+  for (int t0 = n_min - 1; t0 <= L - 2; t0 += kTile) {
+    // end positions [t0, t1) read tokens [lo, t1): lo <= e - (n_max - 1) for every e >= t0
+    t1 = t0 + kTile < L - 1 ? t0 + kTile : L - 1;
+    lo = t0 - (n_max - 1) > 0 ? t0 - (n_max - 1) : 0;
+    __syncthreads();  // the previous tile has been read
+    for (int i = tid; i < t1 - lo; i += kNgramThreads) cp_async4(tile + i, h + lo + i);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int e = t0 + tid; e < t1; e += kNgramThreads) {
+      int m = 0;
+      const int cap = n_max < e + 1 ? n_max : e + 1;
+      while (m < cap && tile[e - m - lo] == suffix[m]) ++m;
+      if (m >= n_min) {
+        const unsigned int key = ((unsigned)m << 24) | (0xffffffu - (unsigned)e);
+        best = key > best ? key : best;
+      }
     }
   }
+  cp_async_wait_all();  // the suffix's copies, when no tile was loaded
   best = __reduce_max_sync(0xffffffffu, best);
   if (lane == 0) s_best[w] = best;
   __syncthreads();
@@ -66,7 +92,15 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(
     start = e + 1;
     cnt = L - start < k ? L - start : k;
   }
-  for (int i = tid; i < k; i += kNgramThreads) d[i] = i < cnt ? __ldg(h + start + i) : -1;
+  // the proposal, from the last tile or the suffix where they hold it
+  for (int i = tid; i < k; i += kNgramThreads) {
+    int32_t v = -1;
+    if (i < cnt) {
+      const int j = start + i;
+      v = (j >= lo && j < t1) ? tile[j - lo] : (j >= L - ns ? suffix[L - 1 - j] : __ldg(h + j));
+    }
+    d[i] = v;
+  }
   if (tid == 0) out_num[r] = cnt;
 }
 

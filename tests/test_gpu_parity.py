@@ -288,6 +288,33 @@ def test_ngram_random(alphabet, nmax, nmin, k):
     assert np.array_equal(d.cpu().numpy(), orc["draft"])
 
 
+@pytest.mark.parametrize("nmax,nmin", [(4, 2), (6, 1), (64, 3)])
+def test_ngram_long_histories_across_tiles(nmax, nmin):
+    # histories past one 8192-position shared-memory tile, with the suffix phrase planted so
+    # that its earliest earlier occurrence ends at, or just before, a tile boundary (its
+    # first tokens then come from the previous tile's halo)
+    rng = np.random.default_rng(100 * nmax + nmin)
+    B, L_max, tile = 12, 20000, 8192
+    h = rng.integers(0, 5000, (B, L_max)).astype(np.int32)
+    lens = np.array([8192, 8193, 8194, 16385, 20000, 19999, 9000, 12000, 20000, 16384, 8191,
+                     17000], np.int32)
+    planted = []
+    for b in range(B):
+        L = int(lens[b])
+        n = min(nmax, L // 4)
+        e = (nmin - 1) + tile * (1 + b % 2) - (b % 3)  # a tile's first end position, or before
+        if e <= L - 2 - n and e - n + 1 >= 0:
+            h[b, e - n + 1:e + 1] = h[b, L - n:L]
+            planted.append(b)
+    d, cnt = sv.ngram_propose(torch.from_numpy(h).to(DEV), torch.from_numpy(lens).to(DEV),
+                              nmax, nmin, 5)
+    torch.cuda.synchronize()
+    orc = oracle.ngram_propose(h, lens, nmax, nmin, 5)
+    assert len(planted) >= 5 and (orc["num_draft"][planted] > 0).all()  # found by the oracle
+    assert np.array_equal(cnt.cpu().numpy(), orc["num_draft"])
+    assert np.array_equal(d.cpu().numpy(), orc["draft"])
+
+
 def test_ngram_greedy_workload4_full():
     w = synth.workload_inputs(4, device=DEV)
     d, n = sv.ngram_propose(w["history"], w["hist_len"], w["n_max"], w["n_min"], w["k"])
