@@ -277,6 +277,7 @@ def gb300_arm(args, rank, world, local_rank):
     elem = w.elem_bytes
     stream = torch.cuda.Stream(device=dev)
     code = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
+    args.launches_per_step = sv.spec_verify_sample_launches(B, k, V, code)
     ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, code), dtype=torch.uint8,
                      device=dev)
     outs = dict(out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
@@ -373,6 +374,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
         cpu = cpu_baseline(d, w, budget_s=args.cpu_seconds)
 
     if rank == 0:
+        ename = "F32" if w.dtype == "f32" else "BF16"
         clocks = clk.summary(*clk.window)
         line = {
             "metric": METRIC,
@@ -400,7 +402,8 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
             "mean_accept_len": acc,
             "roofline": {
                 "bound": "hbm",
-                "kernel": f"segment_kernel<SampleOp<{'F32' if w.dtype == 'f32' else 'BF16'}>>",
+                "kernel": f"segment_kernel<SampleOp<{ename}>>" + (
+                    f" + draw_kernel<{ename}>" if args.launches_per_step > 1 else ""),
                 "achieved": achieved,
                 "peak": peak,
                 "unit": "GB/s",
@@ -412,7 +415,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
                 "launch_ms": mean_ms,
             },
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * args.launches_per_step,
             "clocks": clocks,
             "wall_s_timed": wall,
         }

@@ -39,7 +39,7 @@
  *    device workspace of at least the size their *_workspace() query returns, 256-byte
  *    aligned. It needs no initialisation and may be reused across calls of any shape: each
  *    call first clears the counters it uses (an asynchronous memset on `stream`, ahead of
- *    its one kernel launch). Two calls in flight at the same time must not share one.
+ *    its kernel launches). Two calls in flight at the same time must not share one.
  *  - Nothing here is thread-unsafe on the host; the only process-wide state is the value
  *    returned by sv_last_cuda_error(), which is per host thread.
  */
@@ -126,6 +126,14 @@ int sv_last_cuda_error(void);
  * Returns SV_OK or an error status; see the general conventions.
  * ---------------------------------------------------------------------------------------- */
 size_t spec_verify_sample_workspace(int B, int k, int V, sv_dtype dtype);
+
+/* The number of kernel launches one spec_verify_sample call of this shape makes on the
+ * current device, besides its memset: 1, or 2 when the rows are long enough (at least 8
+ * chunks of 32 KiB, and at most 32) for the draws of the batch's last requests to run in a
+ * second launch split over their chunks; 0 for B = 0 or an invalid shape. The outputs do not
+ * depend on it. A library query; the pages have no counterpart. */
+int spec_verify_sample_launches(int B, int k, int V, sv_dtype dtype);
+
 sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
                              sv_dtype dtype, const int32_t* draft_tokens,
                              const int32_t* num_draft, const float* uniforms, int B, int k,

@@ -47,7 +47,7 @@ from . import _native
 
 __all__ = [
     "SVError", "SV_F32", "SV_BF16", "SV_MAX_K", "build", "library", "version",
-    "spec_verify_sample_workspace", "spec_verify_sample",
+    "spec_verify_sample_workspace", "spec_verify_sample_launches", "spec_verify_sample",
     "spec_verify_greedy_workspace", "spec_verify_greedy", "spec_verify_greedy_noalloc",
     "logit_gap_gate_workspace", "logit_gap_gate", "ngram_propose",
     "SV_CONF_TOP_PROB", "SV_CONF_INV_ENTROPY", "draft_confidence_workspace",
@@ -152,6 +152,10 @@ def _ok(status, where):
 # ------------------------------------------------------------------------------ sampled
 def spec_verify_sample_workspace(B: int, k: int, V: int, dtype: int) -> int:
     return int(library().spec_verify_sample_workspace(B, k, V, dtype))
+
+
+def spec_verify_sample_launches(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_sample_launches(B, k, V, dtype))
 
 
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,

@@ -107,6 +107,8 @@ def _declare(L):
     L.sv_last_cuda_error.argtypes = []
     L.spec_verify_sample_workspace.restype = Z
     L.spec_verify_sample_workspace.argtypes = [I, I, I, I]
+    L.spec_verify_sample_launches.restype = I
+    L.spec_verify_sample_launches.argtypes = [I, I, I, I]
     L.spec_verify_sample.restype = I
     L.spec_verify_sample.argtypes = [P, P, I, P, P, P, I, I, I, F, P, P, P, P, P, P, Z, P]
     L.spec_verify_greedy_workspace.restype = Z

@@ -10,7 +10,9 @@
 // works" (accept while the draft token is the target's own pick, then emit the target's
 // pick).
 //
-// One kernel launch per call (after a small memset of the call's counters). Unit = (request
+// One kernel launch per call (after a small memset of the call's counters), plus, for rows of
+// at least 8 chunks, a second one (draw_kernel) for the draws of the batch's last requests,
+// split over their chunks. Unit = (request
 // r, row slot, segment of up to kSegChunks 32 KiB chunks), one CTA each (sv_stream.cuh); a
 // request has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows
 // 0..k-1) and k+1 in the greedy verify. Units of rows a request does not need (past its n_r)
@@ -30,6 +32,8 @@
 //                           max(0, p_a - q_a) or the bonus p_n, each as one pass over its
 //                           row (pair) for per-chunk masses, then one chunk scanned in
 //                           vocabulary order (float-float sums throughout).
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -44,6 +48,8 @@
 #endif
 
 namespace sv {
+
+int device_sm_count();  // sv_common.cu
 
 constexpr int kPoisoned = -2;  // an index that marks a slice whose copy never landed
 
@@ -189,6 +195,9 @@ struct SampleArgs {
   DF* resid;          // [B][nch * (2 * kWarps + 1)] sub-range then chunk masses of a draw
   unsigned int* row_cnt;
   unsigned int* req_cnt;
+  int defer;                // the last `defer` requests draw in draw_kernel
+  int* draw_a;              // [B] their accepted prefix, or -1 for a data error
+  unsigned int* draw_cnt;   // [B] their arrival counters in draw_kernel
 };
 
 // Residual weight max(0, p_j - q_j) with both normalisers folded in (row units).
@@ -319,13 +328,13 @@ struct DrawRing {
 // of the piece two ahead. Without it, every thread loads its vectors from global memory.
 // Every thread calls this.
 template <typename E, int RingBytes, class VW>
-__device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring) {
+__device__ bool chunk_masses(int c0, int c1, int V, const VW& vw, DF* part, Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   using DR = DrawRing<VW, RingBytes>;
   constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
   constexpr int kPer = DR::kPiecesPerChunk;
   constexpr int kVec = DR::kVecPerLane;
-  const int np = nch * kPer;
+  const int h0 = c0 * kPer, np = c1 * kPer;  // the pieces [h0, np) of chunks [c0, c1)
   auto piece = [&](int h, int64_t& b, int64_t& e) {
     b = (int64_t)(h / kPer) * E::kChunk + (int64_t)(h % kPer) * kPieceElems;
     e = b + kPieceElems < V ? b + kPieceElems : (int64_t)V;
@@ -353,7 +362,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
     if (lane == 0) part[(int64_t)h * kWarps + warp] = df_add(DF{hi, 0.0f}, DF{lo, 0.0f});
   };
   if (!ring.usable || !SV_RESID_RING) {
-    for (int h = 0; h < np; ++h) {
+    for (int h = h0; h < np; ++h) {
       int64_t b, e;
       piece(h, b, e);
       VW q = vw;
@@ -369,7 +378,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
     return true;
   }
   auto issue = [&](int h) {
-    const int st = h & 1;
+    const int st = (h - h0) & 1;
     int64_t b, e;
     piece(h, b, e);
     const uint32_t bytes = e > b ? (uint32_t)((e - b) * (16 / E::kPerVec)) : 0u;
@@ -390,11 +399,11 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
     }
   };
   if (tid == 0)
-    for (int h = 0; h < 2 && h < np; ++h) issue(h);
+    for (int h = h0; h < h0 + 2 && h < np; ++h) issue(h);
   // every thread follows the same barrier phases
   bool timed_out = false;
-  for (int h = 0; h < np; ++h) {
-    const int st = h & 1;
+  for (int h = h0; h < np; ++h) {
+    const int st = (h - h0) & 1;
     if (!ring_wait(ring, st)) timed_out = true;
     int64_t b, e;
     piece(h, b, e);
@@ -420,7 +429,7 @@ __device__ bool chunk_masses(int nch, int V, const VW& vw, DF* part, Ring& ring)
   if (__any_sync(0xffffffffu, timed_out)) {
     if (lane == 0) {
       atomicOr(&ring.ctl->error, 1u);
-      for (int h = 0; h < np; ++h)
+      for (int h = h0; h < np; ++h)
         part[(int64_t)h * kWarps + warp] = DF{__int_as_float(0x7fc00000), 0.0f};
     }
     return false;
@@ -514,6 +523,9 @@ struct SampleOp {
   // A row of one segment is merged by this CTA: fetch its draft token's logit while the
   // first stages are in flight.
   __device__ static __forceinline__ void prologue(const Args& A, const Seg& g, Smem& sm) {
+    // a dependent draw_kernel (launched with programmatic serialization) may start its CTAs
+    // as this grid's slots free up; they wait for this grid's completion before any read
+    if (A.defer > 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x != 0 || g.nseg != 1) return;
     bool ok;
     const int n = n_of(A, g.r, ok);
@@ -607,6 +619,13 @@ struct SampleOp {
   template <class VW>
   __device__ static int draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                              Ring& ring, int& t, double& W);
+  template <class VW>
+  __device__ static int draw_select(const Args& A, const VW& vw, DF* part, bool landed, float u,
+                                    Smem& sm, Ring& ring, int& t, double& W);
+  __device__ static void emit(const Args& A, int r, int a, int n, int t, double W, int st);
+  template <class F>
+  __device__ static void with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
+                                           F&& f);
 };
 
 template <typename ET>
@@ -685,14 +704,25 @@ template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                                   Ring& ring, int& t, double& W) {
+  using DR = DrawRing<VW, T::kRingBytes>;
+  static_assert(DR::kPiecesPerChunk * kWarps <= 32, "one warp holds a chunk's sub-range masses");
+  const bool landed = chunk_masses<E, T::kRingBytes>(0, A.nch, A.V, vw, part, ring);
+  __syncthreads();
+  return draw_select(A, vw, part, landed, u, sm, ring, t, W);
+}
+
+// The rest of a draw, from the sub-range masses in part (every chunk's): the chunk masses
+// and their total W, the chunk and then the sub-range in which u*W falls, and that sub-range
+// scanned in vocabulary order. Every thread calls this.
+template <typename ET>
+template <class VW>
+__device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, bool landed,
+                                         float u, Smem& sm, Ring& ring, int& t, double& W) {
   const int tid = threadIdx.x, lane = tid & 31;
   using DR = DrawRing<VW, T::kRingBytes>;
   constexpr int kSubs = DR::kPiecesPerChunk * kWarps;  // sub-ranges of a chunk
   constexpr int kSubElems = DR::kVecPerLane * 32 * E::kPerVec;
   constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
-  static_assert(kSubs <= 32, "one warp holds a chunk's sub-range masses");
-  const bool landed = chunk_masses<E, T::kRingBytes>(A.nch, A.V, vw, part, ring);
-  __syncthreads();
   // the chunk masses M_c = sum of the chunk's sub-range masses (fixed order), and
   // W = sum_c M_c (warp 0), all in float-float sums; M_c goes after the sub-range masses
   DF* cmass = part + (int64_t)A.nch * kSubs;
@@ -772,12 +802,71 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
   return kDrawOk;
 }
 
+// The weights of request r's draw, handed to f: the residual max(0, p_a - q_a) (a < n, not
+// bonus), or the bonus draw from p of target row a (a = n after full acceptance, or a row
+// whose residual vanished through rounding), in units of 2^K of that row.
+template <typename ET>
+template <class F>
+__device__ void SampleOp<ET>::with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
+                                                F&& f) {
+  const int R = 2 * A.k + 1;
+  if (a < n && !bonus) {
+    const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
+    const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
+    ResidScan<E> rs;
+    rs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
+    rs.rq = row_ptr<E>(A.draft, (int64_t)r * A.k + a, A.V);
+    rs.j1 = A.V;
+    rs.aligned = A.aligned;
+    rs.wf.s = A.s;
+    rs.wf.cp = -tp.K;
+    rs.wf.cq = -dq.K;
+    rs.wf.ip = (float)(1.0 / tp.S);
+    rs.wf.iq = (float)(1.0 / dq.S);
+    f(rs);
+  } else {
+    const RowSoftmax rw = ld_row(A.row + (int64_t)r * R + a);
+    BonusScan<E> bs;
+    bs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
+    bs.j1 = A.V;
+    bs.aligned = A.aligned;
+    bs.s = A.s;
+    bs.c = -rw.K;
+    f(bs);
+  }
+}
+
+// Write request r's outputs: the accepted drafts, the drawn token t and -1 padding, the
+// accept length and the residual mass; or, when the draw did not succeed (st), the error
+// sentinel. Every thread calls this.
+template <typename ET>
+__device__ void SampleOp<ET>::emit(const Args& A, int r, int a, int n, int t, double W, int st) {
+  const int tid = threadIdx.x;
+  if (st != kDrawOk) {  // a data error, or a copy that never landed: the error sentinel
+    if (tid <= A.k) A.out_tokens[(int64_t)r * (A.k + 1) + tid] = -1;
+    if (tid == 0) {
+      A.out_accept_len[r] = -1;
+      if (A.out_resid) A.out_resid[r] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  if (tid <= A.k) {
+    int32_t val = -1;
+    if (tid < a) val = __ldg(A.tokens + (int64_t)r * A.k + tid);
+    else if (tid == a) val = t;
+    A.out_tokens[(int64_t)r * (A.k + 1) + tid] = val;
+  }
+  if (tid == 0) {
+    A.out_accept_len[r] = a;
+    if (A.out_resid) A.out_resid[r] = a < n ? (float)W : 0.0f;
+  }
+}
+
 template <typename ET>
 __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n_ok, Smem& sm,
                                              Ring& ring) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int R = 2 * A.k + 1;
-  const int32_t* x = A.tokens + (int64_t)r * A.k;
   const float* u = A.uniforms + (int64_t)r * (A.k + 1);
 
   // ---- accept tests (warp 0; lane i is draft position i) ----
@@ -821,67 +910,99 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   }
   __syncthreads();
   const int a = sm.a;
+  // a deferred request (one of the launch's last): its draw follows in draw_kernel, the
+  // launch after this one, split over its chunks
+  if (A.defer > 0 && r >= A.B - A.defer) {
+    if (tid == 0) A.draw_a[r] = sm.err ? -1 : a;
+    if (sm.err) emit(A, r, a, n, -1, 0.0, kDrawFailed);
+    return;
+  }
   int t = -1;
   double W = 0.0;
   int st = kDrawFailed;
   if (!sm.err) {
-    const float s = A.s;
     const float uk = __ldg(u + A.k);
     DF* part = A.nch <= kSmemChunks  // [nch][up to 2 * kWarps], then [nch]
                        ? sm.cm
                        : A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
     st = kDrawNoMass;
-    if (a < n) {
-      // ---- residual norm(max(0, p_a - q_a)) ----
-      const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
-      const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
-      ResidScan<E> rs;
-      rs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
-      rs.rq = row_ptr<E>(A.draft, (int64_t)r * A.k + a, A.V);
-      rs.j1 = A.V;
-      rs.aligned = A.aligned;
-      rs.wf.s = s;
-      rs.wf.cp = -tp.K;
-      rs.wf.cq = -dq.K;
-      rs.wf.ip = (float)(1.0 / tp.S);
-      rs.wf.iq = (float)(1.0 / dq.S);
-      st = draw(A, rs, part, uk, sm, ring, t, W);
-    }
+    if (a < n)  // the residual norm(max(0, p_a - q_a))
+      with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
+        st = draw(A, vw, part, uk, sm, ring, t, W);
+      });
     if (st == kDrawNoMass) {
-      // ---- bonus draw from p (row n after full acceptance; row a if the residual vanished
-      //      through rounding), in units of 2^K of that row ----
-      const RowSoftmax rw = ld_row(A.row + (int64_t)r * R + a);
-      BonusScan<E> bs;
-      bs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
-      bs.j1 = A.V;
-      bs.aligned = A.aligned;
-      bs.s = s;
-      bs.c = -rw.K;
+      // the bonus draw from p (row n after full acceptance; row a if the residual vanished
+      // through rounding)
       double Wb;
-      st = draw(A, bs, part, uk, sm, ring, t, Wb);
+      with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
+        st = draw(A, vw, part, uk, sm, ring, t, Wb);
+      });
       if (st == kDrawNoMass) st = kDrawFailed;
     }
   }
-  if (st != kDrawOk) {  // a data error, or a copy that never landed: the error sentinel
-    if (tid <= A.k) A.out_tokens[(int64_t)r * (A.k + 1) + tid] = -1;
-    if (tid == 0) {
-      A.out_accept_len[r] = -1;
-      if (A.out_resid) A.out_resid[r] = __int_as_float(0x7fc00000);
-    }
-    return;
-  }
+  emit(A, r, a, n, t, W, st);
+}
 
-  // ---- emit ----
-  if (tid <= A.k) {
-    int32_t val = -1;
-    if (tid < a) val = __ldg(x + tid);
-    else if (tid == a) val = t;
-    A.out_tokens[(int64_t)r * (A.k + 1) + tid] = val;
-  }
+// The draws of the deferred requests (the last `defer` of the batch), one CTA per (request,
+// chunk): each computes the sub-range masses of its chunk of the request's draw rows, as the
+// request's own finisher would, and the CTA that completes the request takes the rest of the
+// draw (the same code on the same masses, so the same token) and writes its outputs. Launched
+// right after segment_kernel<SampleOp> on the same stream, which wrote each deferred request's
+// accepted prefix (or -1 for a data error) and every row's statistics.
+template <typename E>
+__global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
+    draw_kernel(const SampleArgs A, CallCtl* ctl) {
+  using Op = SampleOp<E>;
+  constexpr int kSubsMax = 2 * kWarps;
+  extern __shared__ __align__(128) unsigned char ring_buf[];
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ int released[2];
+  __shared__ typename Op::Smem sm;
+  // the verify launch before this one must be complete, its writes visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int r = A.B - A.defer + (int)(blockIdx.x / (unsigned)A.nch);
+  const int c = (int)(blockIdx.x % (unsigned)A.nch);
+  const int a = __ldcg(A.draw_a + r);
+  if (a < 0) return;  // a data error: the verify wrote the sentinel
+  bool n_ok;
+  const int n = Op::n_of(A, r, n_ok);
+  const int tid = threadIdx.x;
   if (tid == 0) {
-    A.out_accept_len[r] = a;
-    if (A.out_resid) A.out_resid[r] = a < n ? (float)W : 0.0f;
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    released[0] = released[1] = 0;
+    fence_barrier_init();
   }
+  __syncthreads();
+  Ring ring{ring_buf, full, released, 0u, ctl, A.aligned};
+  DF* gpart = A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
+  bool landed = true;
+  Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
+    landed = chunk_masses<E, Op::T::kRingBytes>(c, c + 1, A.V, vw, gpart, ring);
+  });
+  __syncthreads();  // every warp's masses are stored
+  if (tid == 0) sm.req_last = arrive_last(A.draw_cnt + r, (unsigned)A.nch);
+  __syncthreads();
+  if (!sm.req_last) return;
+  __threadfence();
+  // the masses of every chunk, into shared memory (written by the request's other CTAs)
+  for (int i = tid; i < A.nch * kSubsMax; i += kThreads)
+    sm.cm[i] = DF{__ldcg(&gpart[i].hi), __ldcg(&gpart[i].lo)};
+  __syncthreads();
+  const float uk = __ldg(A.uniforms + (int64_t)r * (A.k + 1) + A.k);
+  int t = -1, st = kDrawFailed;
+  double W = 0.0;
+  Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
+    st = Op::draw_select(A, vw, sm.cm, landed, uk, sm, ring, t, W);
+  });
+  if (st == kDrawNoMass && a < n) {  // the residual vanished through rounding: p_a
+    double Wb;
+    Op::with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
+      st = Op::draw(A, vw, sm.cm, uk, sm, ring, t, Wb);
+    });
+  }
+  if (st == kDrawNoMass) st = kDrawFailed;
+  Op::emit(A, r, a, n, t, W, st);
 }
 
 // ============================================================================================
@@ -1087,11 +1208,79 @@ bool rows_aligned(const void* base, int V, sv_dtype d) {
   return aligned_to(base, 16) && ((int64_t)V * elem_bytes(d)) % 16 == 0;
 }
 
+// How many of the batch's last requests leave their draw to draw_kernel. A request's draw
+// runs in one CTA after its last row, one chunk after another, and re-reads 2 of the
+// request's 2k+1 rows; the last requests' draws run on while little else does. The requests
+// deferred are the last M, M = kDeferScale * slots * 2 / ((2k+1) * CTAs per request): the
+// share of the launch whose draw re-reads would outlast its streaming (kDeferScale = 16,
+// measured on B=512, k=8, V=128256 bf16 and B=256, k=4, V=151936 fp32). Rows of fewer than
+// kDeferMinChunks chunks gain less than the second launch costs; rows of more than
+// kSmemChunks chunks do not hold their masses in shared memory.
+#ifndef SV_DEFER_SCALE
+#define SV_DEFER_SCALE 16
+#endif
+#ifndef SV_DEFER_MIN_CHUNKS
+#define SV_DEFER_MIN_CHUNKS 8
+#endif
+#ifndef SV_DRAW_PDL
+#define SV_DRAW_PDL 1
+#endif
+constexpr int64_t kDeferMinChunks = SV_DEFER_MIN_CHUNKS;
+int deferred_requests(int B, int k, int nseg, int64_t nch) {
+  constexpr int kSmemChunks = SampleOp<F32>::kSmemChunks;
+  if (SV_DEFER_SCALE <= 0 || nch < kDeferMinChunks || nch > kSmemChunks) return 0;
+  const int64_t slots = (int64_t)device_sm_count() * SampleOp<F32>::T::kCtasPerSm;
+  const int64_t rows = 2 * k + 1;
+  const int64_t per_request = rows * nseg;
+  const int64_t m = (SV_DEFER_SCALE * slots * 2 + rows * per_request - 1) / (rows * per_request);
+  return (int)std::min<int64_t>(m, B);
+}
+
+// Launch draw_kernel for the deferred requests (one CTA per request and chunk).
+template <typename E>
+sv_status launch_draws(const SampleArgs& A, CallCtl* ctl, cudaStream_t st) {
+  constexpr int kRingBytes = SampleOp<E>::T::kRingBytes;
+  static std::atomic<unsigned long long> ready{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!(ready.load() & bit)) {
+    e = cudaFuncSetAttribute(draw_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRingBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(draw_kernel<E>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (bit) ready.fetch_or(bit);
+  }
+  // programmatic serialization: the CTAs may become resident while the verify launch
+  // finishes, and wait in griddepcontrol.wait for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)A.defer * A.nch), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kRingBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = SV_DRAW_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, draw_kernel<E>, A, ctl);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" size_t spec_verify_sample_workspace(int B, int k, int V, sv_dtype dtype) {
   if (B < 0 || k < 1 || k > SV_MAX_K || V < 2 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
   return sample_layout(B, k, V, dtype).total;
+}
+
+extern "C" int spec_verify_sample_launches(int B, int k, int V, sv_dtype dtype) {
+  if (B <= 0 || k < 1 || k > SV_MAX_K || V < 2 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
+  const int64_t nch = num_chunks(V, dtype);
+  return deferred_requests(B, k, num_segments(nch), nch) > 0 ? 2 : 1;
 }
 
 extern "C" sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
@@ -1150,13 +1339,18 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.resid = reinterpret_cast<DF*>(ws + L.resid);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
+  A.draw_a = reinterpret_cast<int*>(ws + L.draw_a);
+  A.draw_cnt = reinterpret_cast<unsigned int*>(ws + L.draw_cnt);
+  A.defer = deferred_requests(B, k, nseg, nch);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the control word and the counters (the last regions) start every call at zero
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
   if (e != cudaSuccess) return cuda_fail(e);
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
-  if (dtype == SV_F32) return launch_segments<SampleOp<F32>>(A, units, ctl, st);
-  return launch_segments<SampleOp<BF16>>(A, units, ctl, st);
+  sv_status s = dtype == SV_F32 ? launch_segments<SampleOp<F32>>(A, units, ctl, st)
+                                : launch_segments<SampleOp<BF16>>(A, units, ctl, st);
+  if (s != SV_OK || A.defer == 0) return s;
+  return dtype == SV_F32 ? launch_draws<F32>(A, ctl, st) : launch_draws<BF16>(A, ctl, st);
 }
 
 extern "C" size_t spec_verify_greedy_workspace(int B, int k, int V, sv_dtype dtype) {

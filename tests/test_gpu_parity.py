@@ -113,6 +113,33 @@ def test_sample_empty_batch_and_repeat_calls():
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("off", [0, 1])
+def test_sample_deferred_draws(off):
+    # rows of 15 fp32 chunks: the batch's last requests draw in the second launch, split over
+    # their chunks; among them bonus draws (q = p), a bad token and a NaN row. off = 1 puts
+    # the rows off the 16-byte grid (plain loads instead of the TMA ring)
+    B, k, V = 160, 3, 120000
+    assert sv.spec_verify_sample_launches(B, k, V, sv.SV_F32) == 2
+    d = synth.sample_inputs(B, k, V, "f32", 0.9, device=DEV, seed=21, ragged=True,
+                            target_std=2.5, draft_noise=0.8)
+    d["draft"][140:145] = d["target"][140:145, :k]  # every draft accepted: bonus draws
+    d["draft_tokens"][150, 0] = V                    # a token out of range
+    d["num_draft"][150] = k
+    d["target"][155, 0, 7] = float("nan")            # NaN in a needed row
+    if off:
+        for key in ("target", "draft"):
+            flat = torch.empty(d[key].numel() + 1, dtype=d[key].dtype, device=DEV)
+            view = flat[1:].view(d[key].shape)
+            view.copy_(d[key])
+            d[key] = view
+    stats, gpu, _ = run_sample(d)
+    print(f"deferred draws (off={off}): {stats}")
+    assert gpu["accept_len"][150] == -1 and gpu["accept_len"][155] == -1
+    nd = d["num_draft"].cpu().numpy()
+    assert (gpu["accept_len"][140:145] == nd[140:145]).all()
+    assert stats["flagged"] <= 8, stats
+
+
 @pytest.mark.parametrize("w", [0, 1, 2])
 def test_sample_workloads_full(w):
     d = synth.workload_inputs(w, device=DEV)
