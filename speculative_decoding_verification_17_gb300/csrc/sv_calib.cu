@@ -3,12 +3,15 @@
 //  gate_risk_coverage  "Speculative Pre-Positioning", section 2.4, Eq. (13)-(14): coverage and
 //                      false-accept risk of the gate over a threshold grid, with the Wilson
 //                      intervals of section 4, and the smallest threshold that meets a risk
-//                      budget. One launch: every CTA bins its decision points (four per
-//                      thread and step, 16-byte loads) by the number of thresholds below
-//                      their gap (branch-free binary searches in shared memory, four at a
-//                      time) into a shared histogram,
-//                      folds it into a global one, and the last CTA turns the histogram into
-//                      per-threshold counts with one suffix scan.
+//                      budget. One or two launches. In the first, every CTA bins its decision
+//                      points (four per thread and step, 16-byte loads) by the number of
+//                      thresholds below their gap (a bucket table over the grid, then the
+//                      gap's own bucket searched) into a shared histogram, folds it into a
+//                      global one, and the last CTA turns the histogram into per-threshold
+//                      counts with one suffix scan. The second (grids of more than 256
+//                      thresholds; the last CTA does it for smaller ones) forms every
+//                      threshold's rates and Wilson intervals in double, one thread each over
+//                      many SMs.
 //  conformal_residual  the "speculative-decoding-plan.md" conformal gate's calibration score:
 //                      the sup-norm distance of a draft row from the true row. A streaming
 //                      max over two rows (16-byte loads, four pairs in flight per thread),
@@ -18,6 +21,7 @@
 //                      8192 scores in one CTA with the keys in shared memory, beyond that one
 //                      launch per pass whose last CTA picks the digit.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -120,26 +124,102 @@ struct SweepArgs {
   unsigned int* acc;  // [T + 1]: accepted points by bin b = #{t : taus[t] < gap}
   unsigned int* bad;  // [T + 1]: the wrong ones among them
   unsigned int* cnt;  // CTA arrivals
+  int* state;         // [3]: broken grid flag, T - (smallest qualifying t) or 0, arrivals of
+                      // sweep_points_kernel
   bool vec;           // gap, token and full_token all start on a 16-byte boundary
 };
 
-inline size_t sweep_smem(int T) {
-  return (size_t)T * sizeof(float) + 2 * (size_t)(T + 1) * sizeof(unsigned int);
+// The bin of a gap g, b = #{t : tau[t] < g}, comes from a bucket table when the grid's ends
+// are finite: bucket(x) = floor((x - tau[0]) * NB / (tau[T-1] - tau[0])), clamped to
+// [0, NB), is non-decreasing in x, so every threshold of an earlier bucket lies below g and
+// every one of a later bucket above it. b is then first[bucket(g)] (the thresholds of the
+// earlier buckets) plus the count of g's own bucket's thresholds below g: a search over that
+// bucket only, no step at all for a uniform grid. The answer set is searched in shared memory
+// when it has at most kSmemAnswer entries.
+constexpr int kSmemAnswer = 4096;
+__host__ __device__ inline int sweep_buckets(int T) {
+  int nb = 64;
+  while (nb < 2 * T && nb < 8192) nb <<= 1;
+  return nb;
 }
+inline size_t sweep_smem(int T, int n_answer) {
+  return (size_t)T * sizeof(float) + 2 * (size_t)(T + 1) * sizeof(unsigned int) +
+         (size_t)(sweep_buckets(T) + 1) * sizeof(unsigned int) +
+         (size_t)(n_answer <= kSmemAnswer ? n_answer : 0) * sizeof(int32_t);
+}
+
+__device__ __forceinline__ int sweep_bucket(float x, float lo, float scale, int nb) {
+  const float v = (x - lo) * scale;
+  return (int)fminf(fmaxf(v, 0.0f), (float)(nb - 1));  // NaN (0 * inf) goes to bucket 0
+}
+
+// Threshold t's point from its counts: coverage, risk and their Wilson intervals, in double
+// as section 4's formulas are written; t joins the qualifying set (atomicMax on T - t in
+// *rev) when its risk is within r_max.
+__device__ void threshold_point(const SweepArgs& A, int t, unsigned int acc, unsigned int bad,
+                                int* rev) {
+  const double nan = __longlong_as_double(0x7ff8000000000000LL);
+  const double n = (double)A.N;
+  sv_calib_point p;
+  p.accepted = acc;
+  p.wrong = bad;
+  p.coverage = A.N > 0 ? (double)acc / n : nan;
+  wilson((double)acc, n, A.z, p.cov_lo, p.cov_hi);
+  if (acc > 0) {
+    p.risk = (double)bad / (double)acc;
+    wilson((double)bad, (double)acc, A.z, p.risk_lo, p.risk_hi);
+    if (p.risk <= A.r_max) atomicMax(rev, A.T - t);
+  } else {
+    p.risk = p.risk_lo = p.risk_hi = nan;
+  }
+  A.out[t] = p;
+}
+
+// Grids up to this size get their points from sweep_kernel's last CTA; larger ones from
+// sweep_points_kernel, over many SMs (the double-precision intervals of a large grid on one
+// SM take longer than a second launch).
+constexpr int kPointsInLastCta = 256;
 
 __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int T = A.T;
+  const int NB = sweep_buckets(T);
   float* tau = reinterpret_cast<float*>(smem);
   unsigned int* hacc = reinterpret_cast<unsigned int*>(tau + T);
   unsigned int* hbad = hacc + T + 1;
+  unsigned int* first = hbad + T + 1;  // [NB + 1]
+  int32_t* ans_s = reinterpret_cast<int32_t*>(first + NB + 1);
+  const bool ans_in_smem = A.n_answer <= kSmemAnswer;
+  const int32_t* ans = ans_in_smem ? ans_s : A.answer;
   __shared__ unsigned int warp_tot[kCalThreads / 32];
-  __shared__ int last, best;
+  __shared__ int last;
   for (int t = threadIdx.x; t < T; t += kCalThreads) tau[t] = __ldg(A.taus + t);
   for (int b = threadIdx.x; b <= T; b += kCalThreads) hacc[b] = hbad[b] = 0;
+  if (ans_in_smem)
+    for (int i = threadIdx.x; i < A.n_answer; i += kCalThreads) ans_s[i] = __ldg(A.answer + i);
   __syncthreads();
 
   const float t0 = tau[0];
+  const float tlo = tau[0], thi = tau[T - 1];
+  const bool table = isfinite(tlo) && isfinite(thi);
+  const float scale = table && thi > tlo ? (float)NB / (thi - tlo) : 0.0f;
+  if (table) {
+    // first[j] = #{t : bucket(tau[t]) < j}: a lower bound over the non-decreasing buckets
+    for (int j = threadIdx.x; j <= NB; j += kCalThreads) {
+      int lo = 0;
+      for (int n = T; n > 0;) {
+        const int half = n >> 1;
+        if (sweep_bucket(tau[lo + half], tlo, scale, NB) < j) {
+          lo += half + 1;
+          n -= half + 1;
+        } else {
+          n = half;
+        }
+      }
+      first[j] = (unsigned)lo;
+    }
+  }
+  __syncthreads();
   // Four decision points at a time: each point's bin b = #{t : tau[t] < g} (accepted at
   // every t < b) and its membership in A, both by branch-free lower bounds of a fixed number
   // of steps, so the four searches overlap and the lanes stay converged.
@@ -156,24 +236,47 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
       const int half = n >> 1;
 #pragma unroll
       for (int p = 0; p < 4; ++p)
-        if (__ldg(A.answer + ia[p] + half) < tok[p]) ia[p] += half;
+        if (ans[ia[p] + half] < tok[p]) ia[p] += half;
       n -= half;
     }
-    for (int n = T; n > 1;) {
-      const int half = n >> 1;
+    int b[4];
+    if (table) {
+      // the thresholds of earlier buckets, then those of g's bucket that lie below g
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
-        if (tau[ib[p] + half] < g[p]) ib[p] += half;
-      n -= half;
+      for (int p = 0; p < 4; ++p) {
+        const int j = ok[p] ? sweep_bucket(g[p], tlo, scale, NB) : 0;
+        int lo = (int)first[j];
+        const int hi = (int)first[j + 1];
+        for (int n = hi - lo; n > 0;) {
+          const int half = n >> 1;
+          if (tau[lo + half] < g[p]) {
+            lo += half + 1;
+            n -= half + 1;
+          } else {
+            n = half;
+          }
+        }
+        b[p] = lo;
+      }
+    } else {
+      for (int n = T; n > 1;) {
+        const int half = n >> 1;
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          if (tau[ib[p] + half] < g[p]) ib[p] += half;
+        n -= half;
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) b[p] = ib[p] + (tau[ib[p]] < g[p]);
     }
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       if (!ok[p]) continue;
-      const int la = ia[p] + (__ldg(A.answer + ia[p]) < tok[p]);  // first entry >= tok
-      if (la >= A.n_answer || __ldg(A.answer + la) != tok[p]) continue;
-      const int b = ib[p] + (tau[ib[p]] < g[p]);  // >= 1 since tau[0] < g
-      atomicAdd(&hacc[b], 1u);
-      if (tok[p] != full[p]) atomicAdd(&hbad[b], 1u);
+      const int la = ia[p] + (ans[ia[p]] < tok[p]);  // first entry >= tok
+      if (la >= A.n_answer || ans[la] != tok[p]) continue;
+      const int bb = b[p] < 1 ? 1 : (b[p] > T ? T : b[p]);  // >= 1 since tau[0] < g
+      atomicAdd(&hacc[bb], 1u);
+      if (tok[p] != full[p]) atomicAdd(&hbad[bb], 1u);
     }
   };
   const int64_t stride = (int64_t)gridDim.x * kCalThreads;
@@ -224,41 +327,57 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   if (broken) {
     for (int t = threadIdx.x; t < T; t += kCalThreads)
       A.out[t] = sv_calib_point{-1, -1, nan, nan, nan, nan, nan, nan};
-    if (threadIdx.x == 0) *A.out_idx = -2;
+    if (threadIdx.x == 0) {
+      *A.out_idx = -2;
+      *A.state = 1;
+    }
     return;
   }
-  // accepted(t) = sum of bins b > t
+  // accepted(t) = sum of bins b > t, written back over the histograms for
+  // sweep_points_kernel, which forms each threshold's rates and intervals
   for (int b = threadIdx.x; b <= T; b += kCalThreads) {
     hacc[b] = b ? __ldcg(A.acc + b) : 0u;
     hbad[b] = b ? __ldcg(A.bad + b) : 0u;
   }
-  if (threadIdx.x == 0) best = INT_MAX;
   __syncthreads();
   block_suffix_sums(hacc, T + 1, warp_tot);
   block_suffix_sums(hbad, T + 1, warp_tot);
-  const double n = (double)A.N;
-  for (int t = threadIdx.x; t < T; t += kCalThreads) {
-    const unsigned int acc = hacc[t + 1], bad = hbad[t + 1];
-    sv_calib_point p;
-    p.accepted = acc;
-    p.wrong = bad;
-    p.coverage = A.N > 0 ? (double)acc / n : nan;
-    wilson((double)acc, n, A.z, p.cov_lo, p.cov_hi);
-    if (acc > 0) {
-      p.risk = (double)bad / (double)acc;
-      wilson((double)bad, (double)acc, A.z, p.risk_lo, p.risk_hi);
-      if (p.risk <= A.r_max) atomicMin(&best, t);
-    } else {
-      p.risk = p.risk_lo = p.risk_hi = nan;
-    }
-    A.out[t] = p;
+  if (T <= kPointsInLastCta) {  // a small grid: the points here, no second launch
+    __shared__ int rev;
+    if (threadIdx.x == 0) rev = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += kCalThreads)
+      threshold_point(A, t, hacc[t + 1], hbad[t + 1], &rev);
+    __syncthreads();
+    if (threadIdx.x == 0) *A.out_idx = rev == 0 ? -1 : T - rev;
+    return;
   }
+  for (int t = threadIdx.x; t < T; t += kCalThreads) {
+    A.acc[t + 1] = hacc[t + 1];
+    A.bad[t + 1] = hbad[t + 1];
+  }
+}
+
+// The coverage, risk and Wilson intervals of every threshold (one thread each, in double, as
+// the formulas of section 4 are written), spread over many SMs, and the smallest t whose risk
+// is within r_max. Launched after sweep_kernel on the same stream.
+constexpr int kPointThreads = 64;
+__global__ void __launch_bounds__(kPointThreads) sweep_points_kernel(const SweepArgs A) {
+  __shared__ int last;
+  if (__ldcg(A.state) != 0) return;  // a broken grid: sweep_kernel wrote the outcome
+  const int t = blockIdx.x * kPointThreads + threadIdx.x;
+  if (t < A.T) threshold_point(A, t, __ldcg(A.acc + t + 1), __ldcg(A.bad + t + 1), A.state + 1);
   __syncthreads();
-  if (threadIdx.x == 0) *A.out_idx = best == INT_MAX ? -1 : best;
+  if (threadIdx.x == 0) last = arrive_last(reinterpret_cast<unsigned int*>(A.state + 2), gridDim.x);
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  __threadfence();
+  const int rev = __ldcg(A.state + 1);
+  *A.out_idx = rev == 0 ? -1 : A.T - rev;
 }
 
 struct SweepLayout {
-  size_t acc, bad, cnt, total;
+  size_t acc, bad, cnt, state, total;
 };
 SweepLayout sweep_layout(int T) {
   SweepLayout L{};
@@ -266,6 +385,7 @@ SweepLayout sweep_layout(int T) {
   L.acc = o; o = round_up(o + (size_t)(T + 1) * sizeof(unsigned int), 256);
   L.bad = o; o = round_up(o + (size_t)(T + 1) * sizeof(unsigned int), 256);
   L.cnt = o; o = round_up(o + sizeof(unsigned int), 256);
+  L.state = o; o = round_up(o + 3 * sizeof(int), 256);
   L.total = o;
   return L;
 }
@@ -546,21 +666,39 @@ extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
   A.acc = reinterpret_cast<unsigned int*>(ws + L.acc);
   A.bad = reinterpret_cast<unsigned int*>(ws + L.bad);
   A.cnt = reinterpret_cast<unsigned int*>(ws + L.cnt);
+  A.state = reinterpret_cast<int*>(ws + L.state);
   A.vec = aligned_to(gap, 16) && aligned_to(token, 16) && aligned_to(full_token, 16);
-  const size_t smem = sweep_smem(T);
+  const size_t smem = sweep_smem(T, n_answer);
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  // every resident CTA slot of the GPU, but no more than one CTA per 2048 points
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel, kCalThreads, smem);
+  // every resident CTA slot of the GPU, but no more than one CTA per 2048 points; the
+  // occupancy answer is kept per device for the last shared-memory size asked (a host query
+  // that would otherwise delay every launch)
+  static std::atomic<unsigned long long> occ_cache[64];  // (smem << 16) | per_sm
+  int dev = 0;
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
+  int per_sm = 0;
+  const unsigned long long cached = dev >= 0 && dev < 64 ? occ_cache[dev].load() : 0ull;
+  if (cached && (cached >> 16) == (unsigned long long)smem) {
+    per_sm = (int)(cached & 0xffffu);
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel, kCalThreads, smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < 64 && per_sm > 0)
+      occ_cache[dev].store(((unsigned long long)smem << 16) | (unsigned)(per_sm & 0xffff));
+  }
   const int64_t want = ((int64_t)N + 8 * kCalThreads - 1) / (8 * kCalThreads);
   const int64_t slots = (int64_t)std::max(per_sm, 1) * device_sm_count();
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
   sweep_kernel<<<grid, kCalThreads, smem, st>>>(A);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (T <= kPointsInLastCta) return SV_OK;
+  sweep_points_kernel<<<(T + kPointThreads - 1) / kPointThreads, kPointThreads, 0, st>>>(A);
   return launch_status();
 }
 

@@ -128,6 +128,37 @@ def test_sweep_inputs_off_the_16_byte_grid():
     assert int(idx.item()) == want["tau_index"]
 
 
+@pytest.mark.parametrize("grid", ["clustered", "infinite_ends", "largest", "one_value"])
+def test_sweep_threshold_grids(grid):
+    # the bin of a gap comes from a bucket table over [taus[0], taus[-1]]: dense clusters and
+    # exact duplicates (many thresholds in one bucket), gaps equal to thresholds, a grid with
+    # infinite ends (the table gives way to a search over the whole grid), the largest grid
+    # and a grid of one value
+    gap, token, full, A = _points(60000, 31, nan_every=11)
+    rng = np.random.default_rng(32)
+    if grid == "clustered":
+        taus = np.sort(np.concatenate([np.linspace(0, 1, 8), np.full(500, 2.5),
+                                       np.linspace(2.5, 2.5001, 300),
+                                       np.linspace(3, 9, 200)])).astype(np.float32)
+    elif grid == "infinite_ends":
+        taus = np.concatenate([[-np.inf], np.linspace(0, 8, 61), [np.inf]]).astype(np.float32)
+    elif grid == "largest":
+        taus = np.sort(rng.uniform(-1, 12, 4096)).astype(np.float32)
+    else:
+        taus = np.full(17, 1.5, np.float32)
+    gap[:3000] = rng.choice(taus[np.isfinite(taus)], 3000)  # gaps equal to thresholds
+    gap[3000:3010] = np.inf
+    check_sweep(gap, token, full, A, taus, r_max=0.3)
+
+
+def test_sweep_large_answer_set():
+    # an answer set past the shared-memory copy (searched in global memory)
+    gap, token, full, _ = _points(40000, 41, n_vocab=50000)
+    A = np.sort(np.random.default_rng(42).choice(50000, 6000, replace=False)).astype(np.int32)
+    token[:20000] = np.random.default_rng(43).choice(A, 20000)
+    check_sweep(gap, token, full, A, np.linspace(0, 9, 257).astype(np.float32), r_max=0.2)
+
+
 def test_sweep_a_million_points():
     gap, token, full, A = _points(1 << 20, 21, n_vocab=120, nan_every=1001)
     taus = np.linspace(0.0, 8.0, 64).astype(np.float32)
