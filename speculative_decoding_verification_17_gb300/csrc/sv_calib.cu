@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
 // The coverage, risk and Wilson intervals of every threshold (one thread each, in double, as
 // the formulas of section 4 are written), spread over many SMs, and the smallest t whose risk
 // is within r_max. Launched after sweep_kernel on the same stream.
-constexpr int kPointThreads = 64;
+constexpr int kPointThreads = 32;  // one warp per CTA: the FP64 chains spread over more SMs
 __global__ void __launch_bounds__(kPointThreads) sweep_points_kernel(const SweepArgs A) {
   __shared__ int last;
   if (__ldcg(A.state) != 0) return;  // a broken grid: sweep_kernel wrote the outcome
