@@ -73,11 +73,12 @@ struct Tile {
 #define SV_TILE(vec, stages, ctas) Tile<vec, stages, ctas>
 #endif
 
-// L2 priority of the pass-1 copies: with SV_L2_KEEP_POS = p > 0 the rows an operation marks
-// as likely to be read again (Seg::keep) are copied with evict_last and all others with
-// evict_first; with 0 every copy keeps its default priority.
+// L2 priority of the pass-1 copies: with SV_L2_KEEP_POS > 0 the rows an operation marks as
+// likely to be read again (Seg::keep) are copied with evict_last and all others with
+// evict_first; with 0 every copy keeps its default priority. (The sampled verify marks the
+// rows of its first draft positions, how many chosen per call from a budget of L2 bytes.)
 #ifndef SV_L2_KEEP_POS
-#define SV_L2_KEEP_POS 2
+#define SV_L2_KEEP_POS 1
 #endif
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far past any legitimate wait
 

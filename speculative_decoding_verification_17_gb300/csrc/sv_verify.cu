@@ -195,6 +195,7 @@ struct SampleArgs {
   DF* resid;          // [B][nch * (2 * kWarps + 1)] sub-range then chunk masses of a draw
   unsigned int* row_cnt;
   unsigned int* req_cnt;
+  int keep_pos;             // rows of draft positions < keep_pos are copied with evict_last
   int defer;                // the last `defer` requests draw in draw_kernel
   int* draw_a;              // [B] their accepted prefix, or -1 for a data error
   unsigned int* draw_cnt;   // [B] their arrival counters in draw_kernel
@@ -501,7 +502,7 @@ struct SampleOp {
     g.r = r;
     g.slot = slot;
     g.seg = seg;
-    g.keep = i < SV_L2_KEEP_POS;  // the early positions hold most rejections
+    g.keep = i < A.keep_pos;  // the early positions hold most rejections
     g.c0 = seg * kSegChunks;
     g.c1 = min(g.c0 + kSegChunks, A.nch);
     g.nseg = A.nseg;
@@ -1236,6 +1237,23 @@ int deferred_requests(int B, int k, int nseg, int64_t nch) {
   return (int)std::min<int64_t>(m, B);
 }
 
+// How many draft positions' rows (target and draft) pass 1 copies with evict_last. Most
+// rejections fall on the first positions, and the draw then finds that pair in L2 if it was
+// kept; keeping more than L2 can hold pushes the kept rows out of each other's way. The rows
+// kept while a wave of CTAs is resident stay within kKeepBytes: positions
+// kKeepBytes / (requests resident * 2 rows * row bytes), at least 1 (measured: 2 for B=512,
+// k=8, V=128256 bf16 and 1 for B=256, k=4, V=151936 fp32 were each the best setting).
+constexpr int64_t kKeepBytes = 32ll << 20;
+int keep_positions(int k, int nseg, int V, sv_dtype d) {
+  if (SV_L2_KEEP_POS <= 0) return 0;
+  const int64_t slots = (int64_t)device_sm_count() * SampleOp<F32>::T::kCtasPerSm;
+  const int64_t per_request = (int64_t)(2 * k + 1) * nseg;
+  const int64_t resident = std::max<int64_t>(1, slots / per_request);
+  const int64_t per_position = resident * 2 * (int64_t)V * elem_bytes(d);
+  const int64_t p = kKeepBytes / per_position;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(p, k));
+}
+
 // Launch draw_kernel for the deferred requests (one CTA per request and chunk).
 template <typename E>
 sv_status launch_draws(const SampleArgs& A, CallCtl* ctl, cudaStream_t st) {
@@ -1342,6 +1360,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.draw_a = reinterpret_cast<int*>(ws + L.draw_a);
   A.draw_cnt = reinterpret_cast<unsigned int*>(ws + L.draw_cnt);
   A.defer = deferred_requests(B, k, nseg, nch);
+  A.keep_pos = keep_positions(k, nseg, V, dtype);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the control word and the counters (the last regions) start every call at zero
   cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
