@@ -706,7 +706,11 @@ template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
                                   Ring& ring, int& t, double& W) {
   using DR = DrawRing<VW, T::kRingBytes>;
-  static_assert(DR::kPiecesPerChunk * kWarps <= 32, "one warp holds a chunk's sub-range masses");
+  // the masses' layouts (Smem::cm, the workspace's resid region, draw_kernel's copy) hold
+  // 2 * kWarps sub-ranges per chunk: a ring whose pieces are smaller than that would overflow
+  // them, so such a shape does not build
+  static_assert(DR::kPiecesPerChunk * kWarps <= 2 * kWarps,
+                "the draw's pieces give more sub-ranges per chunk than the masses' layout holds");
   const bool landed = chunk_masses<E, T::kRingBytes>(0, A.nch, A.V, vw, part, ring);
   __syncthreads();
   return draw_select(A, vw, part, landed, u, sm, ring, t, W);
