@@ -38,8 +38,8 @@
  *  - Workspaces: the sampled verify, the greedy verify and the gate need a caller-owned
  *    device workspace of at least the size their *_workspace() query returns, 256-byte
  *    aligned. It needs no initialisation and may be reused across calls of any shape: each
- *    call first clears the counters it uses (an asynchronous memset on `stream`, ahead of
- *    its kernel launches). Two calls in flight at the same time must not share one.
+ *    call first clears the counters it uses (a small kernel on `stream`, ahead of the call's
+ *    other launches). Two calls in flight at the same time must not share one.
  *  - Nothing here is thread-unsafe on the host; the only process-wide state is the value
  *    returned by sv_last_cuda_error(), which is per host thread.
  */
@@ -128,10 +128,10 @@ int sv_last_cuda_error(void);
 size_t spec_verify_sample_workspace(int B, int k, int V, sv_dtype dtype);
 
 /* The number of kernel launches one spec_verify_sample call of this shape makes on the
- * current device, besides its memset: 1, or 2 when the rows are long enough (at least 8
- * chunks of 32 KiB, and at most 32) for the draws of the batch's last requests to run in a
- * second launch split over their chunks; 0 for B = 0 or an invalid shape. The outputs do not
- * depend on it. A library query; the pages have no counterpart. */
+ * current device: 2 (the clear of its counters and the verify), or 3 when the rows are long
+ * enough (at least 8 chunks of 32 KiB, and at most 32) for the draws of the batch's last
+ * requests to run in a third launch split over their chunks; 0 for B = 0 or an invalid
+ * shape. The outputs do not depend on it. A library query; the pages have no counterpart. */
 int spec_verify_sample_launches(int B, int k, int V, sv_dtype dtype);
 
 sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
@@ -178,7 +178,7 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
  *   - The first call on a device (with that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream capture.
  *   - Every call on a device shares the one array: it clears the counters it needs at the
- *     start (an asynchronous memset on `stream`), and calls whose work overlaps on the GPU
+ *     start (a small kernel on `stream`), and calls whose work overlaps on the GPU
  *     (on different streams, or from different host threads) race and give wrong results.
  *     Issue them on one stream, or order them.
  *   - No cudaMalloc, cudaFree or other allocating call is made.

@@ -361,8 +361,8 @@ extern "C" sv_status ready_cache_record(sv_cache_slot* slots, int32_t* entry_sto
   A.part = reinterpret_cast<WarpTop2*>(ws + L.part);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_segments<RecordOp<F32>>(A, units, ctl, st);
   return launch_segments<RecordOp<BF16>>(A, units, ctl, st);

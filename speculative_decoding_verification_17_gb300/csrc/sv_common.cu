@@ -16,6 +16,30 @@ sv_status cuda_fail(cudaError_t e) {
   return SV_ERR_CUDA;
 }
 
+// Zero n16 16-byte words at p. The launch that follows on the stream (a segment kernel,
+// launched with programmatic serialization) may start its CTAs at once: they stream their
+// rows meanwhile and wait in griddepcontrol.wait before they touch what this clears.
+__global__ void clear_kernel(uint4* p, long long n16) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+sv_status launch_clear(void* p, size_t bytes, cudaStream_t st) {
+  const long long n16 = (long long)(bytes / 16);
+  if (n16 <= 0) return SV_OK;
+  if (!SV_CLEAR_KERNEL) {  // a build may compare against a plain memset
+    const cudaError_t e = cudaMemsetAsync(p, 0, bytes, st);
+    return e == cudaSuccess ? SV_OK : cuda_fail(e);
+  }
+  constexpr int kClearThreads = 256;
+  long long blocks = (n16 + 4 * kClearThreads - 1) / (4 * kClearThreads);
+  blocks = blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks);
+  clear_kernel<<<(unsigned)blocks, kClearThreads, 0, st>>>(static_cast<uint4*>(p), n16);
+  return launch_status();
+}
+
 // SMs of the current device (queried once per device; 152 if the query fails).
 int device_sm_count() {
   static std::atomic<int> cache[64];

@@ -394,8 +394,8 @@ extern "C" sv_status draft_confidence_stop(const void* draft_logits, sv_dtype dt
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   const bool ent = mode == SV_CONF_INV_ENTROPY;
   if (dtype == SV_F32)

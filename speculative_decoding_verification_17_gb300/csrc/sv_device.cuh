@@ -323,8 +323,8 @@ __device__ __forceinline__ double block_sum_fd_t0(float x, float* red) {
 // Count this CTA in on a completion counter; true for the CTA that arrives last. Called by
 // one thread after a CTA barrier that follows the stores the CTA publishes: the add is a
 // release at GPU scope (cumulative over what the barrier ordered before it) and an acquire
-// for the arriving thread. The counters are cleared by the host call (an async memset on the
-// same stream) before every launch.
+// for the arriving thread. The counters are cleared before every launch, by the call's clear
+// kernel on the same stream (the segment kernel waits for it before its finishing phase).
 __device__ __forceinline__ bool arrive_last(unsigned int* counter, unsigned int expected) {
   unsigned int prev;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"

@@ -165,8 +165,8 @@ extern "C" sv_status logit_gap_gate(const void* logits, sv_dtype dtype, int N, i
   A.part = reinterpret_cast<WarpTop2*>(ws + L.part);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_segments<GateOp<F32>>(A, units, ctl, st);
   return launch_segments<GateOp<BF16>>(A, units, ctl, st);
@@ -239,8 +239,8 @@ extern "C" sv_status conformal_admit(const void* logits, sv_dtype dtype, int N, 
   A.best = reinterpret_cast<unsigned long long*>(ws + L.best);
   A.step_cnt = reinterpret_cast<unsigned int*>(ws + L.step_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_segments<GateOp<F32, true>>(A, units, ctl, st);
   return launch_segments<GateOp<BF16, true>>(A, units, ctl, st);

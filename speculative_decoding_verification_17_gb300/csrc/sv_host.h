@@ -13,6 +13,14 @@ namespace sv {
 // Record a CUDA error for sv_last_cuda_error() and turn it into SV_ERR_CUDA.
 sv_status cuda_fail(cudaError_t e);
 
+// Zero `bytes` (a multiple of 16) at the 16-byte aligned device address p, on stream st,
+// with a small kernel after which a segment kernel launched with programmatic serialization
+// may start at once (sv_common.cu).
+sv_status launch_clear(void* p, size_t bytes, cudaStream_t st);
+#ifndef SV_CLEAR_KERNEL
+#define SV_CLEAR_KERNEL 1
+#endif
+
 // Status of the launch just issued on this thread.
 inline sv_status launch_status() {
   const cudaError_t e = cudaGetLastError();

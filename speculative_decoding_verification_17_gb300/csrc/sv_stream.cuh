@@ -240,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, Op::T::kCtasPerSm)
       ring_state.phase |= (uint32_t)(((ns - q + kStages - 1) / kStages) & 1) << q;
   ring_state.ctl = ctl;
   ring_state.usable = A.aligned;
+  // the counters this finish uses were cleared by the launch before this one on the stream:
+  // wait for it (nothing before this point touches them)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   Op::finish(A, g, sm, ring_state);
 }
 
@@ -272,14 +275,26 @@ sv_status launch_segments(const typename Op::Args& A, long long units, CallCtl* 
     e = set_attributes();
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
-  e = cudaGetLastError();
+  // programmatic serialization: the CTAs may start while the clear of the call's counters
+  // (the launch before this one) runs; they wait for it before the finishing phase
+  auto launch = [&]() -> cudaError_t {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)units, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kRingBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = SV_CLEAR_KERNEL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, segment_kernel<Op>, A, ctl);
+  };
+  e = launch();
   if (e != cudaSuccess && bit) {  // attributes lost with a reset context: set them, retry
+    (void)cudaGetLastError();
     ready.fetch_and(~bit);
-    if (set_attributes() == cudaSuccess) {
-      segment_kernel<Op><<<(unsigned)units, kThreads, kRingBytes, st>>>(A, ctl);
-      e = cudaGetLastError();
-    }
+    if (set_attributes() == cudaSuccess) e = launch();
   }
   return e == cudaSuccess ? SV_OK : cuda_fail(e);
 }

@@ -10,9 +10,9 @@
 // works" (accept while the draft token is the target's own pick, then emit the target's
 // pick).
 //
-// One kernel launch per call (after a small memset of the call's counters), plus, for rows of
-// at least 8 chunks, a second one (draw_kernel) for the draws of the batch's last requests,
-// split over their chunks. Unit = (request
+// One kernel launch per call (after a small kernel that clears the call's counters), plus, for
+// rows of at least 8 chunks, a second one (draw_kernel) for the draws of the batch's last
+// requests, split over their chunks. Unit = (request
 // r, row slot, segment of up to kSegChunks 32 KiB chunks), one CTA each (sv_stream.cuh); a
 // request has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows
 // 0..k-1) and k+1 in the greedy verify. Units of rows a request does not need (past its n_r)
@@ -1302,7 +1302,7 @@ extern "C" size_t spec_verify_sample_workspace(int B, int k, int V, sv_dtype dty
 extern "C" int spec_verify_sample_launches(int B, int k, int V, sv_dtype dtype) {
   if (B <= 0 || k < 1 || k > SV_MAX_K || V < 2 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
   const int64_t nch = num_chunks(V, dtype);
-  return deferred_requests(B, k, num_segments(nch), nch) > 0 ? 2 : 1;
+  return deferred_requests(B, k, num_segments(nch), nch) > 0 ? 3 : 2;  // with the clear
 }
 
 extern "C" sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
@@ -1367,8 +1367,8 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.keep_pos = keep_positions(k, nseg, V, dtype);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the control word and the counters (the last regions) start every call at zero
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   sv_status s = dtype == SV_F32 ? launch_segments<SampleOp<F32>>(A, units, ctl, st)
                                 : launch_segments<SampleOp<BF16>>(A, units, ctl, st);
@@ -1423,8 +1423,8 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws + L.ctl, 0, L.total - L.ctl, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
+  if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
   if (dtype == SV_F32) return launch_segments<GreedyOp<F32>>(A, units, ctl, st);
   return launch_segments<GreedyOp<BF16>>(A, units, ctl, st);

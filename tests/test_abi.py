@@ -45,13 +45,13 @@ def test_version_and_status_strings():
 def test_workspace_queries():
     assert sv.spec_verify_sample_workspace(512, 8, 128256, sv.SV_BF16) > 0
     assert sv.spec_verify_sample_workspace(1, 17, 100, sv.SV_F32) == 0
-    # rows of 8 or more chunks draw the last requests in a second launch
-    assert sv.spec_verify_sample_launches(512, 8, 128256, sv.SV_BF16) == 2
-    assert sv.spec_verify_sample_launches(64, 5, 32000, sv.SV_BF16) == 1
-    assert sv.spec_verify_sample_launches(256, 4, 151936, sv.SV_F32) == 2
-    assert sv.spec_verify_sample_launches(1, 4, 1000, sv.SV_F32) == 1
+    # the clear of the counters and the verify, plus draw_kernel for rows of 8 to 32 chunks
+    assert sv.spec_verify_sample_launches(512, 8, 128256, sv.SV_BF16) == 3
+    assert sv.spec_verify_sample_launches(64, 5, 32000, sv.SV_BF16) == 2
+    assert sv.spec_verify_sample_launches(256, 4, 151936, sv.SV_F32) == 3
+    assert sv.spec_verify_sample_launches(1, 4, 1000, sv.SV_F32) == 2
     assert sv.spec_verify_sample_launches(0, 4, 1000, sv.SV_F32) == 0
-    assert sv.spec_verify_sample_launches(4, 2, 600000, sv.SV_BF16) == 1  # 37 chunks
+    assert sv.spec_verify_sample_launches(4, 2, 600000, sv.SV_BF16) == 2  # 37 chunks
     assert sv.spec_verify_greedy_workspace(128, 5, 32000, sv.SV_BF16) > 0
     assert sv.logit_gap_gate_workspace(1280, 151936, sv.SV_F32) > 0
     for q in (sv.spec_verify_sample_workspace(0, 4, 1000, 0),

@@ -119,7 +119,7 @@ def test_sample_deferred_draws(off):
     # their chunks; among them bonus draws (q = p), a bad token and a NaN row. off = 1 puts
     # the rows off the 16-byte grid (plain loads instead of the TMA ring)
     B, k, V = 160, 3, 120000
-    assert sv.spec_verify_sample_launches(B, k, V, sv.SV_F32) == 2
+    assert sv.spec_verify_sample_launches(B, k, V, sv.SV_F32) == 3  # clear, verify, draws
     d = synth.sample_inputs(B, k, V, "f32", 0.9, device=DEV, seed=21, ragged=True,
                             target_std=2.5, draft_noise=0.8)
     d["draft"][140:145] = d["target"][140:145, :k]  # every draft accepted: bonus draws
