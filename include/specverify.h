@@ -58,7 +58,7 @@ typedef struct CUstream_st* sv_stream_t; /* the same type as cudaStream_t */
 typedef enum {
   SV_OK = 0,
   SV_ERR_INVALID_ARG = 1,  /* a null required pointer, a bad size, T <= 0, n_min > n_max ... */
-  SV_ERR_UNSUPPORTED = 2,  /* a legal request this build does not handle (k > 16, huge grids) */
+  SV_ERR_UNSUPPORTED = 2,  /* a legal request this library does not handle (k > 16, huge grids) */
   SV_ERR_WORKSPACE = 3,    /* workspace pointer null, misaligned or smaller than the query */
   SV_ERR_CUDA = 4,         /* a CUDA launch or attribute call failed; see sv_last_cuda_error */
   SV_ERR_TIMEOUT = 5       /* reserved: no kernel in this library waits on another CTA */
