@@ -140,6 +140,60 @@ def test_sample_deferred_draws(off):
     assert stats["flagged"] <= 8, stats
 
 
+def test_sample_and_greedy_in_a_cuda_graph():
+    # serving loops replay captured graphs: one sampled-verify call (the clear of its counters,
+    # the verify, and the draws of the last requests, chained with programmatic dependencies)
+    # and one greedy call, captured together and replayed twice, give what eager calls give
+    B, k, V = 32, 4, 131072  # 8 chunks of bf16: the draws run in their own launch
+    assert sv.spec_verify_sample_launches(B, k, V, sv.SV_BF16) == 3
+    d = synth.sample_inputs(B, k, V, "bf16", 0.8, device=DEV, seed=17, ragged=True)
+    sws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                      device=DEV)
+    gws = torch.zeros(sv.spec_verify_greedy_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
+                      device=DEV)
+
+    def outs():
+        return dict(out_tokens=torch.full((B, k + 1), -7, dtype=torch.int32, device=DEV),
+                    out_accept_len=torch.full((B,), -7, dtype=torch.int32, device=DEV),
+                    out_p_draft=torch.zeros((B, k), device=DEV),
+                    out_q_draft=torch.zeros((B, k), device=DEV),
+                    out_resid_mass=torch.zeros((B,), device=DEV))
+
+    def calls(o, go, stream=None):
+        sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], 0.8,
+                              d["num_draft"], workspace=sws, stream=stream, **o)
+        sv.spec_verify_greedy(d["target"], d["draft_tokens"], d["num_draft"],
+                              out_tokens=go[0], out_accept_len=go[1], workspace=gws,
+                              stream=stream)
+
+    eager, geager = outs(), (torch.empty((B, k + 1), dtype=torch.int32, device=DEV),
+                             torch.empty((B,), dtype=torch.int32, device=DEV))
+    calls(eager, geager)
+    torch.cuda.synchronize()
+    captured, gcap = outs(), (torch.full((B, k + 1), -7, dtype=torch.int32, device=DEV),
+                              torch.full((B,), -7, dtype=torch.int32, device=DEV))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # a warm-up outside the capture, as graph users do
+        calls(outs(), (torch.empty_like(gcap[0]), torch.empty_like(gcap[1])))
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls(captured, gcap)
+    for _ in range(2):
+        for t in list(captured.values()) + list(gcap):
+            t.fill_(float("nan") if t.is_floating_point() else -9)
+        graph.replay()
+        torch.cuda.synchronize()
+        for name in eager:
+            a, b = captured[name], eager[name]
+            if a.is_floating_point():
+                a, b = a.nan_to_num(-1.0), b.nan_to_num(-1.0)
+            assert torch.equal(a, b), name
+        assert torch.equal(gcap[0], geager[0]) and torch.equal(gcap[1], geager[1])
+    assert (eager["out_accept_len"] >= 0).all()
+
+
 @pytest.mark.parametrize("w", [0, 1, 2])
 def test_sample_workloads_full(w):
     d = synth.workload_inputs(w, device=DEV)
