@@ -633,6 +633,34 @@ def secondary_rows(args, dev, stream, peak, head=None):
                                       d["T"], None, stream=stream), steps, 3, stream, flush))
     rows["sample_b1_k4_v1000_f32_latency"] = dict(ms=ms, us=ms * 1e3)
 
+    # the two small workloads replayed from a CUDA graph, as a serving loop runs them: no host
+    # launch overhead, inputs warm in L2 (per call: the replay of 20 captured calls / 20)
+    for wi, tag in ((0, "sample_b1_k4_v1000_f32_graph"), (1, "sample_b64_k5_v32000_bf16_graph")):
+        d = synth.workload_inputs(wi, device=dev)
+        B, k, V = d["B"], d["k"], d["V"]
+        code = sv.SV_F32 if d["dtype"] == "f32" else sv.SV_BF16
+        ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, code), dtype=torch.uint8,
+                         device=dev)
+        per_graph = 20
+
+        def call():
+            sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                  d["T"], None, workspace=ws)
+
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                call()
+        ms = statistics.median(time_launches(graph.replay, steps, 3, stream)) / per_graph
+        rows[tag] = dict(ms=ms, us=ms * 1e3, positions_per_s=B * k / (ms * 1e-3))
+        del d, ws, graph
+
     # n-gram proposal feeding the greedy verify (B=128, L=8192, V=32000)
     w4 = synth.workload_inputs(4, device=dev)
     dr, nd = sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"], w4["k"])
