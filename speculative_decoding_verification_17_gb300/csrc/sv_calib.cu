@@ -134,18 +134,26 @@ struct SweepArgs {
 // [0, NB), is non-decreasing in x, so every threshold of an earlier bucket lies below g and
 // every one of a later bucket above it. b is then first[bucket(g)] (the thresholds of the
 // earlier buckets) plus the count of g's own bucket's thresholds below g: a search over that
-// bucket only, no step at all for a uniform grid. The answer set is searched in shared memory
-// when it has at most kSmemAnswer entries.
+// bucket only, no step at all for a uniform grid. Membership in the answer set is one bit of a
+// shared-memory bitmap over [answer[0], answer[n-1]] when that span has at most kAnswerBits
+// tokens (every vocabulary up to 262144 tokens); a wider set is searched, in shared memory when
+// it has at most kSmemAnswer entries.
 constexpr int kSmemAnswer = 4096;
+constexpr int kAnswerBits = 1 << 18;
 __host__ __device__ inline int sweep_buckets(int T) {
   int nb = 64;
   while (nb < 2 * T && nb < 8192) nb <<= 1;
   return nb;
 }
+// the answer region holds the bitmap or, for a wider set, its copy
+inline size_t sweep_answer_bytes(int n_answer) {
+  if (n_answer <= 0) return 0;
+  return std::max((size_t)kAnswerBits / 8,
+                  (size_t)(n_answer <= kSmemAnswer ? n_answer : 0) * sizeof(int32_t));
+}
 inline size_t sweep_smem(int T, int n_answer) {
   return (size_t)T * sizeof(float) + 2 * (size_t)(T + 1) * sizeof(unsigned int) +
-         (size_t)(sweep_buckets(T) + 1) * sizeof(unsigned int) +
-         (size_t)(n_answer <= kSmemAnswer ? n_answer : 0) * sizeof(int32_t);
+         (size_t)(sweep_buckets(T) + 1) * sizeof(unsigned int) + sweep_answer_bytes(n_answer);
 }
 
 __device__ __forceinline__ int sweep_bucket(float x, float lo, float scale, int nb) {
@@ -189,14 +197,30 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   unsigned int* hbad = hacc + T + 1;
   unsigned int* first = hbad + T + 1;  // [NB + 1]
   int32_t* ans_s = reinterpret_cast<int32_t*>(first + NB + 1);
-  const bool ans_in_smem = A.n_answer <= kSmemAnswer;
+  unsigned int* bits = reinterpret_cast<unsigned int*>(ans_s);  // the same region
+  // the bitmap's span; the set is sorted, so a span of 0 or less (an unsorted set) or one
+  // wider than the bitmap is searched instead
+  const unsigned amin = A.n_answer > 0 ? (unsigned)__ldg(A.answer) : 0u;
+  const int64_t span =
+      A.n_answer > 0 ? (int64_t)__ldg(A.answer + A.n_answer - 1) - (int32_t)amin + 1 : 0;
+  const bool bitmap = span > 0 && span <= kAnswerBits;
+  const unsigned range = bitmap ? (unsigned)span : 0u;
+  const bool ans_in_smem = !bitmap && A.n_answer <= kSmemAnswer;
   const int32_t* ans = ans_in_smem ? ans_s : A.answer;
   __shared__ unsigned int warp_tot[kCalThreads / 32];
   __shared__ int last;
   for (int t = threadIdx.x; t < T; t += kCalThreads) tau[t] = __ldg(A.taus + t);
   for (int b = threadIdx.x; b <= T; b += kCalThreads) hacc[b] = hbad[b] = 0;
-  if (ans_in_smem)
+  if (bitmap) {
+    for (unsigned w = threadIdx.x; w < (range + 31) / 32; w += kCalThreads) bits[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < A.n_answer; i += kCalThreads) {
+      const unsigned u = (unsigned)__ldg(A.answer + i) - amin;
+      if (u < range) atomicOr(&bits[u >> 5], 1u << (u & 31));
+    }
+  } else if (ans_in_smem) {
     for (int i = threadIdx.x; i < A.n_answer; i += kCalThreads) ans_s[i] = __ldg(A.answer + i);
+  }
   __syncthreads();
 
   const float t0 = tau[0];
@@ -220,24 +244,37 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
     }
   }
   __syncthreads();
-  // Four decision points at a time: each point's bin b = #{t : tau[t] < g} (accepted at
-  // every t < b) and its membership in A, both by branch-free lower bounds of a fixed number
-  // of steps, so the four searches overlap and the lanes stay converged.
+  // Four decision points at a time: each point's membership in A (a bit of the bitmap, or a
+  // branch-free lower bound of a fixed number of steps) and its bin b = #{t : tau[t] < g}
+  // (accepted at every t < b), so the four lookups overlap and the lanes stay converged.
   auto bin4 = [&](const float (&g)[4], const int (&tok)[4], const int (&full)[4]) {
     bool ok[4];
-    int ia[4], ib[4];
+    int ib[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       ok[p] = g[p] > t0 && A.n_answer > 0;  // below every threshold (or NaN): accepted nowhere
-      ia[p] = 0;
       ib[p] = 0;
     }
-    for (int n = A.n_answer; n > 1;) {
-      const int half = n >> 1;
+    if (bitmap) {
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
-        if (ans[ia[p] + half] < tok[p]) ia[p] += half;
-      n -= half;
+      for (int p = 0; p < 4; ++p) {
+        const unsigned u = (unsigned)tok[p] - amin;
+        ok[p] = ok[p] && u < range && ((bits[u >> 5] >> (u & 31)) & 1u);
+      }
+    } else {
+      int ia[4] = {0, 0, 0, 0};
+      for (int n = A.n_answer; n > 1;) {
+        const int half = n >> 1;
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          if (ans[ia[p] + half] < tok[p]) ia[p] += half;
+        n -= half;
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int la = ia[p] + (ans[ia[p]] < tok[p]);  // first entry >= tok
+        ok[p] = ok[p] && la < A.n_answer && ans[la] == tok[p];
+      }
     }
     int b[4];
     if (table) {
@@ -272,8 +309,6 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       if (!ok[p]) continue;
-      const int la = ia[p] + (ans[ia[p]] < tok[p]);  // first entry >= tok
-      if (la >= A.n_answer || ans[la] != tok[p]) continue;
       const int bb = b[p] < 1 ? 1 : (b[p] > T ? T : b[p]);  // >= 1 since tau[0] < g
       atomicAdd(&hacc[bb], 1u);
       if (tok[p] != full[p]) atomicAdd(&hbad[bb], 1u);
@@ -281,15 +316,33 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   };
   const int64_t stride = (int64_t)gridDim.x * kCalThreads;
   const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
-  // four points per thread and step, the three 16-byte loads issued together
+  // four points per thread and step, two steps' six 16-byte loads issued together
   const int64_t n4 = A.vec ? A.N / 4 : 0;
-  for (int64_t q = tid; q < n4; q += stride) {
-    const float4 g = __ldcs(reinterpret_cast<const float4*>(A.gap) + q);
-    const int4 t = __ldcs(reinterpret_cast<const int4*>(A.token) + q);
-    const int4 f = __ldcs(reinterpret_cast<const int4*>(A.full) + q);
-    const float gg[4] = {g.x, g.y, g.z, g.w};
-    const int tt[4] = {t.x, t.y, t.z, t.w}, ff[4] = {f.x, f.y, f.z, f.w};
-    bin4(gg, tt, ff);
+  const float4* gap4 = reinterpret_cast<const float4*>(A.gap);
+  const int4* tok4 = reinterpret_cast<const int4*>(A.token);
+  const int4* full4 = reinterpret_cast<const int4*>(A.full);
+  for (int64_t q = tid; q < n4; q += 2 * stride) {
+    const bool two = q + stride < n4;
+    const float4 g = __ldcs(gap4 + q);
+    const int4 t = __ldcs(tok4 + q);
+    const int4 f = __ldcs(full4 + q);
+    float4 g2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    int4 t2 = make_int4(0, 0, 0, 0), f2 = make_int4(0, 0, 0, 0);
+    if (two) {
+      g2 = __ldcs(gap4 + q + stride);
+      t2 = __ldcs(tok4 + q + stride);
+      f2 = __ldcs(full4 + q + stride);
+    }
+    {
+      const float gg[4] = {g.x, g.y, g.z, g.w};
+      const int tt[4] = {t.x, t.y, t.z, t.w}, ff[4] = {f.x, f.y, f.z, f.w};
+      bin4(gg, tt, ff);
+    }
+    if (two) {
+      const float gg[4] = {g2.x, g2.y, g2.z, g2.w};
+      const int tt[4] = {t2.x, t2.y, t2.z, t2.w}, ff[4] = {f2.x, f2.y, f2.z, f2.w};
+      bin4(gg, tt, ff);
+    }
   }
   // the rest (or everything, for inputs off the 16-byte grid), four points per step
   for (int64_t i0 = 4 * n4 + 4 * tid; i0 < A.N; i0 += 4 * stride) {

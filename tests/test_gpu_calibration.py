@@ -2,7 +2,9 @@
 
 - gate_risk_coverage: exact counts, selected threshold and rates (bit for bit), on the
   pre-positioning page's operating point, random decision points with NaN gaps and tied
-  thresholds, the largest grid, an empty set, an unsorted grid, and a million points.
+  thresholds, the largest grid, an empty set, an unsorted grid, answer sets of every span
+  (negative, int32 extremes, repeated answers, past the membership bitmap), and a million
+  points.
 - conformal_residual: bit-exact fp32 residuals on rows with masked tokens, one-sided masks,
   NaN and infinities, aligned and unaligned rows, both dtypes, and the sampled-verify
   benchmark batch's draft rows against its target rows (sampled rows).
@@ -152,11 +154,54 @@ def test_sweep_threshold_grids(grid):
 
 
 def test_sweep_large_answer_set():
-    # an answer set past the shared-memory copy (searched in global memory)
+    # 6000 answers over a 50000-token span: more than the shared-memory copy holds, but within
+    # the membership bitmap's span
     gap, token, full, _ = _points(40000, 41, n_vocab=50000)
     A = np.sort(np.random.default_rng(42).choice(50000, 6000, replace=False)).astype(np.int32)
     token[:20000] = np.random.default_rng(43).choice(A, 20000)
     check_sweep(gap, token, full, A, np.linspace(0, 9, 257).astype(np.float32), r_max=0.2)
+
+
+I32_MIN, I32_MAX = -(1 << 31), (1 << 31) - 1
+SPAN = 1 << 18  # the widest answer set whose membership is a bitmap
+
+
+SPAN_CASES = ["negative", "span_at_bitmap_limit", "span_past_bitmap_small",
+              "span_past_bitmap_large", "duplicates", "near_int32_max", "near_int32_min"]
+
+
+@pytest.mark.parametrize("case", SPAN_CASES)
+def test_sweep_answer_set_spans(case):
+    # membership is a bitmap over [A[0], A[-1]] up to SPAN tokens, a search beyond: both
+    # ends of each span, tokens just outside it, the int32 extremes, repeated answers, and
+    # sets wider than the bitmap held in shared memory (<= 4096 entries) or searched in
+    # global memory
+    rng = np.random.default_rng(50 + SPAN_CASES.index(case))
+    if case == "negative":
+        A = np.array([-70000, -5, -3, 0, 7, 100], np.int64)
+    elif case == "span_at_bitmap_limit":
+        A = np.concatenate([[1000, 1000 + SPAN - 1], rng.integers(1001, 1000 + SPAN - 1, 200)])
+    elif case == "span_past_bitmap_small":
+        A = np.concatenate([[1000, 1000 + SPAN], rng.integers(1001, 1000 + SPAN, 200)])
+    elif case == "span_past_bitmap_large":
+        A = rng.choice(1 << 22, 6000, replace=False)
+    elif case == "duplicates":
+        A = np.repeat(np.array([3, 9, 9, 40, 41, 500]), 3)
+    elif case == "near_int32_max":
+        A = np.array([I32_MAX - 40, I32_MAX - 3, I32_MAX], np.int64)
+    else:
+        A = np.array([I32_MIN, I32_MIN + 2, I32_MIN + 77], np.int64)
+    A = np.sort(A).astype(np.int32)
+    N = 30000
+    near = np.concatenate([A.astype(np.int64) + d for d in (-1, 0, 1)])
+    near = near[(near >= I32_MIN) & (near <= I32_MAX)]
+    extremes = np.array([I32_MIN, I32_MIN + 1, -1, 0, 1, I32_MAX - 1, I32_MAX], np.int64)
+    token = rng.choice(np.concatenate([near, extremes]), N)
+    token[: N // 3] = rng.choice(A, N // 3)
+    token = token.astype(np.int32)
+    gap = np.abs(rng.standard_normal(N) * 3).astype(np.float32)
+    full = np.where(rng.random(N) < 0.8, token, token ^ 1).astype(np.int32)
+    check_sweep(gap, token, full, A, np.linspace(0, 9, 300).astype(np.float32), r_max=0.2)
 
 
 def test_sweep_a_million_points():
