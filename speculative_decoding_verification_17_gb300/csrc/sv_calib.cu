@@ -19,7 +19,8 @@
 //  conformal_quantile  the split-conformal quantile of those scores: a radix select over the
 //                      scores' order-preserving keys in three passes (11, 11, 10 bits); up to
 //                      8192 scores in one CTA with the keys in shared memory, beyond that one
-//                      launch per pass whose last CTA picks the digit.
+//                      cooperative launch whose passes meet at grid barriers, after each of
+//                      which every CTA picks the digit from the pass's global histogram.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -526,14 +527,14 @@ __global__ void __launch_bounds__(kCalThreads) resid_kernel(const ResidArgs A) {
 
 // ------------------------------------------------------------------ conformal quantile
 constexpr int kSelBins = 2048;
+constexpr int kSelectPasses = 3;
+constexpr int kSelUnroll = 4;
+constexpr uint64_t kSelWaitNs = 2000000000ull;  // 2 s: far past any legitimate barrier wait
+constexpr unsigned int kSelTimedOut = 0x7fc00001u;  // quiet NaN, payload 1
 
 struct SelectState {
-  unsigned int prefix;     // the key's bits chosen so far
-  unsigned int remaining;  // the rank within the keys that share the prefix
-  unsigned int done;       // set when the result is already written
-  unsigned int pad;
-  unsigned int cnt[4];     // CTA arrivals per pass
-  unsigned int hist[3][kSelBins];
+  unsigned int cnt[4];     // CTA arrivals at each pass's grid barrier
+  unsigned int hist[kSelectPasses][kSelBins];
 };
 
 // Order-preserving key of a float (NaN canonicalised, above +inf; -0 below +0).
@@ -546,77 +547,120 @@ __device__ __forceinline__ float key_float(unsigned int k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int n, int64_t rank,
-                                                             int pass, SelectState* st,
-                                                             float* out) {
-  __shared__ unsigned int h[kSelBins];
-  __shared__ unsigned int warp_tot[kCalThreads / 32];
-  __shared__ int last;
-  if (__ldcg(&st->done)) return;
-  const int width = pass == 2 ? 10 : 11;
-  const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
-  const unsigned int mask = (1u << width) - 1u;
-  const unsigned int prefix = pass == 0 ? 0u : __ldcg(&st->prefix);
-  for (int b = threadIdx.x; b < kSelBins; b += kCalThreads) h[b] = 0;
-  __syncthreads();
-  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
-  auto count = [&](float x) {
-    const unsigned int key = float_key(x);
-    if (pass == 0 || (key >> (shift + width)) == prefix) atomicAdd(&h[(key >> shift) & mask], 1u);
-  };
-  // four scores per thread and step (one 16-byte load; the passes re-read them from L2)
-  const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
-  const int64_t n4 = (reinterpret_cast<uintptr_t>(r) % 16 == 0) ? n / 4 : 0;
-  for (int64_t q = tid; q < n4; q += stride) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(r) + q);
-    count(x.x);
-    count(x.y);
-    count(x.z);
-    count(x.w);
-  }
-  for (int64_t i = 4 * n4 + tid; i < n; i += stride) count(__ldg(r + i));
-  __syncthreads();
-  for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
-    if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
+// Grid barrier of a cooperative launch (every CTA resident): each CTA adds one to *count
+// (release, after the CTA's earlier writes) and waits until all gridDim.x have (acquire), for
+// at most kSelWaitNs. False, for the whole CTA, if the wait ran out.
+__device__ bool grid_barrier(unsigned int* count) {
+  __shared__ int ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    last = arrive_last(&st->cnt[pass], gridDim.x);
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const unsigned int want = pass == 0 ? (unsigned int)rank : __ldcg(&st->remaining);
-  for (int b = threadIdx.x; b < kSelBins; b += kCalThreads)
-    h[b] = b <= (int)mask ? __ldcg(&st->hist[pass][b]) : 0u;
-  __syncthreads();
-  // the digit d with (keys below it) < want <= (keys below it) + count(d)
-  unsigned int* cnt = h;
-  // counts before the prefix sums, kept per thread for the check below
-  const int per = kSelBins / kCalThreads;
-  unsigned int own[kSelBins / kCalThreads];
-#pragma unroll
-  for (int i = 0; i < per; ++i) own[i] = cnt[threadIdx.x * per + i];
-  __syncthreads();
-  block_prefix_sums(cnt, kSelBins, warp_tot);
-#pragma unroll
-  for (int i = 0; i < per; ++i) {
-    const int b = threadIdx.x * per + i;
-    const unsigned int before = cnt[b];
-    if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
-      const unsigned int p = (prefix << width) | (unsigned int)b;
-      if (pass == 2) {
-        *out = key_float(p);
-        st->done = 1u;
-      } else {
-        st->prefix = p;
-        st->remaining = want - before;
-      }
+    unsigned int seen;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(seen)
+                 : "l"(count)
+                 : "memory");
+    ++seen;
+    const uint64_t t0 = globaltimer_ns();
+    while (seen < gridDim.x) {
+      if (globaltimer_ns() - t0 > kSelWaitNs) break;
+      __nanosleep(64);
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(count) : "memory");
     }
+    __threadfence();
+    ok = seen >= gridDim.x;
   }
+  __syncthreads();
+  return ok != 0;
 }
 
-constexpr int kSelectPasses = 3;
+// The whole radix select in one cooperative launch. Each pass: every CTA counts the keys that
+// share the prefix chosen so far into a shared histogram of the next digit (sixteen scores per
+// thread and step, four 16-byte loads in flight) and adds it to the pass's global histogram;
+// after a grid barrier, every CTA reads that histogram and picks the same digit d, the one
+// with (keys below it) < want <= (keys below it) + count(d). The first two passes load the
+// scores with an L2 evict-last policy, so the next pass finds them in L2.
+__global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int n, int64_t rank,
+                                                             SelectState* st, float* out) {
+  __shared__ unsigned int h[kSelBins];
+  __shared__ unsigned int warp_tot[kCalThreads / 32];
+  __shared__ unsigned int s_digit, s_before;
+  const int64_t stride = (int64_t)gridDim.x * kCalThreads;
+  const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
+  const int64_t n4 = (reinterpret_cast<uintptr_t>(r) % 16 == 0) ? n / 4 : 0;
+  const float4* r4 = reinterpret_cast<const float4*>(r);
+  unsigned int prefix = 0u;
+  unsigned int want = (unsigned int)rank;
+  for (int pass = 0; pass < kSelectPasses; ++pass) {
+    const int width = pass == 2 ? 10 : 11;
+    const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+    const unsigned int mask = (1u << width) - 1u;
+    for (int b = threadIdx.x; b < kSelBins; b += kCalThreads) h[b] = 0;
+    if (threadIdx.x == 0) s_digit = s_before = 0u;
+    __syncthreads();
+    auto count = [&](float x) {
+      const unsigned int key = float_key(x);
+      if (pass == 0 || (key >> (shift + width)) == prefix) atomicAdd(&h[(key >> shift) & mask], 1u);
+    };
+    const uint64_t pol = l2_policy(pass + 1 < kSelectPasses);
+    int64_t q = tid;
+    for (; q + (kSelUnroll - 1) * stride < n4; q += kSelUnroll * stride) {
+      float4 x[kSelUnroll];
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u)
+        asm("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+            : "=f"(x[u].x), "=f"(x[u].y), "=f"(x[u].z), "=f"(x[u].w)
+            : "l"(r4 + q + u * stride), "l"(pol));
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u) {
+        count(x[u].x);
+        count(x[u].y);
+        count(x[u].z);
+        count(x[u].w);
+      }
+    }
+    for (; q < n4; q += stride) {
+      const float4 x = __ldg(r4 + q);
+      count(x.x);
+      count(x.y);
+      count(x.z);
+      count(x.w);
+    }
+    for (int64_t i = 4 * n4 + tid; i < n; i += stride) count(__ldg(r + i));
+    __syncthreads();
+    for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
+      if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
+    if (!grid_barrier(&st->cnt[pass])) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) *out = __uint_as_float(kSelTimedOut);
+      return;
+    }
+    for (int b = threadIdx.x; b < kSelBins; b += kCalThreads)
+      h[b] = b <= (int)mask ? __ldcg(&st->hist[pass][b]) : 0u;
+    __syncthreads();
+    // counts before the prefix sums, kept per thread for the check below
+    constexpr int per = kSelBins / kCalThreads;
+    unsigned int own[per];
+#pragma unroll
+    for (int i = 0; i < per; ++i) own[i] = h[threadIdx.x * per + i];
+    __syncthreads();
+    block_prefix_sums(h, kSelBins, warp_tot);
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int b = threadIdx.x * per + i;
+      const unsigned int before = h[b];
+      if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
+        s_digit = (unsigned int)b;
+        s_before = before;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | s_digit;
+    want -= s_before;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *out = key_float(prefix);
+}
+
 
 // The whole select in one CTA for small score sets: the keys stay in shared memory.
 constexpr int kSmallSelect = 8192;
@@ -816,13 +860,30 @@ extern "C" sv_status conformal_quantile(const float* resid, int n, double q, flo
   cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
   if (e != cudaSuccess) return cuda_fail(e);
   SelectState* S = static_cast<SelectState*>(workspace);
-  // every resident CTA slot (eight per SM), but no more than one CTA per 4096 scores
-  const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 8LL * device_sm_count()));
-  for (int p = 0; p < kSelectPasses; ++p) {
-    select_kernel<<<grid, kCalThreads, 0, st>>>(resid, n, rank, p, S, out_q);
-    e = cudaGetLastError();
+  // A cooperative launch: every CTA must be resident at once for the grid barriers. Up to
+  // four CTAs per SM (as many as fit), no more than one CTA per 4096 scores; the occupancy
+  // answer is kept per device (a host query that would otherwise delay every launch).
+  static std::atomic<int> occ_cache[64];
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int per_sm = dev >= 0 && dev < 64 ? occ_cache[dev].load() : 0;
+  if (per_sm <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel, kCalThreads, 0);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm <= 0) return SV_ERR_UNSUPPORTED;
+    if (dev >= 0 && dev < 64) occ_cache[dev].store(per_sm);
   }
+  const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
+  const int64_t slots = (int64_t)std::min(per_sm, 4) * device_sm_count();
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
+  const float* r = resid;
+  int nn = n;
+  int64_t rk64 = rank;
+  float* o = out_q;
+  void* args[] = {&r, &nn, &rk64, &S, &o};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(select_kernel), dim3(grid),
+                                  dim3(kCalThreads), args, 0, st);
+  if (e != cudaSuccess) return cuda_fail(e);
   return SV_OK;
 }
