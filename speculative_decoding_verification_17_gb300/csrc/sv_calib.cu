@@ -359,18 +359,22 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
     bin4(gg, tt, ff);
   }
   __syncthreads();
-  for (int b = 1 + threadIdx.x; b <= T; b += kCalThreads) {
-    if (hacc[b]) atomicAdd(A.acc + b, hacc[b]);
-    if (hbad[b]) atomicAdd(A.bad + b, hbad[b]);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  // a grid of one CTA keeps its histogram in shared memory: no global fold, no arrival
+  const bool solo = gridDim.x == 1;
+  if (!solo) {
+    for (int b = 1 + threadIdx.x; b <= T; b += kCalThreads) {
+      if (hacc[b]) atomicAdd(A.acc + b, hacc[b]);
+      if (hbad[b]) atomicAdd(A.bad + b, hbad[b]);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last = arrive_last(A.cnt, gridDim.x);
+    }
+    __syncthreads();
+    if (!last) return;
     __threadfence();
-    last = arrive_last(A.cnt, gridDim.x);
   }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
 
   // the grid must be non-decreasing without NaN
   int broken = 0;
@@ -389,11 +393,13 @@ __global__ void __launch_bounds__(kCalThreads) sweep_kernel(const SweepArgs A) {
   }
   // accepted(t) = sum of bins b > t, written back over the histograms for
   // sweep_points_kernel, which forms each threshold's rates and intervals
-  for (int b = threadIdx.x; b <= T; b += kCalThreads) {
-    hacc[b] = b ? __ldcg(A.acc + b) : 0u;
-    hbad[b] = b ? __ldcg(A.bad + b) : 0u;
+  if (!solo) {
+    for (int b = threadIdx.x; b <= T; b += kCalThreads) {
+      hacc[b] = b ? __ldcg(A.acc + b) : 0u;
+      hbad[b] = b ? __ldcg(A.bad + b) : 0u;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   block_suffix_sums(hacc, T + 1, warp_tot);
   block_suffix_sums(hbad, T + 1, warp_tot);
   if (T <= kPointsInLastCta) {  // a small grid: the points here, no second launch
@@ -744,8 +750,7 @@ extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
   if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
     return SV_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, L.total, st);
-  if (e != cudaSuccess) return cuda_fail(e);
+  cudaError_t e = cudaSuccess;
   SweepArgs A;
   A.gap = gap;
   A.token = token;
@@ -791,6 +796,12 @@ extern "C" sv_status gate_risk_coverage(const float* gap, const int32_t* token,
   const int64_t want = ((int64_t)N + 8 * kCalThreads - 1) / (8 * kCalThreads);
   const int64_t slots = (int64_t)std::max(per_sm, 1) * device_sm_count();
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
+  // the workspace's histograms and counters start at zero; a grid of one CTA with the points
+  // in that CTA (T <= kPointsInLastCta) uses none of them
+  if (grid > 1 || T > kPointsInLastCta) {
+    e = cudaMemsetAsync(workspace, 0, L.total, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   sweep_kernel<<<grid, kCalThreads, smem, st>>>(A);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);

@@ -204,6 +204,33 @@ def test_sweep_answer_set_spans(case):
     check_sweep(gap, token, full, A, np.linspace(0, 9, 300).astype(np.float32), r_max=0.2)
 
 
+def test_sweep_reuses_its_workspace():
+    # one workspace across calls of one CTA (no workspace state at all for grids of at most
+    # 256 thresholds) and of many CTAs (histograms and counters cleared first), with a
+    # broken grid in between: every call equals the oracle
+    ws = torch.zeros(sv.gate_risk_coverage_workspace(200000, 300), dtype=torch.uint8,
+                     device=DEV)
+    calls = [(200000, np.linspace(0, 6, 64)), (300, np.linspace(0, 6, 64)),
+             (300, np.array([1.0, 0.5, 2.0])), (200000, np.linspace(0, 6, 300)),
+             (700, np.linspace(0, 6, 300)), (0, np.linspace(0, 6, 5)),
+             (2000, np.linspace(0, 6, 64))]
+    for i, (N, taus) in enumerate(calls):
+        gap, token, full, A = _points(N, 60 + i, nan_every=9)
+        taus = taus.astype(np.float32)
+        pts, idx = sv.gate_risk_coverage(_dev(gap), _dev(token), _dev(full), _dev(A),
+                                         _dev(taus), Z95, 0.2, workspace=ws)
+        torch.cuda.synchronize()
+        got = sv.gate_points_dict(pts)
+        if np.all(np.diff(taus) >= 0):
+            want = oracle.risk_coverage(gap, token, full, A, taus, Z95, 0.2)
+            np.testing.assert_array_equal(got["accepted"].numpy(), want["accepted"])
+            np.testing.assert_array_equal(got["wrong"].numpy(), want["wrong"])
+            np.testing.assert_array_equal(got["risk_hi"].numpy(), want["risk_hi"])
+            assert int(idx.item()) == want["tau_index"], (i, N)
+        else:
+            assert int(idx.item()) == -2 and (got["accepted"].numpy() == -1).all()
+
+
 def test_sweep_a_million_points():
     gap, token, full, A = _points(1 << 20, 21, n_vocab=120, nan_every=1001)
     taus = np.linspace(0.0, 8.0, 64).astype(np.float32)
