@@ -772,7 +772,9 @@ def kernels_once():
     (1280 fp32 rows of V=151936), spec_verify_greedy, draft_confidence_stop (top probability,
     then inverse entropy) and conformal_admit (K=4) on the B=256 k=8 V=128256 bf16 batch,
     conformal_residual (its draft rows against target rows 0..k-1), gate_risk_coverage (16M
-    points, 1024 thresholds) and conformal_quantile (16M scores)."""
+    points, 1024 thresholds), conformal_quantile (16M scores), ready_cache_record (2048
+    sessions from that batch's target rows) and ready_cache_serve (16384 requests), and
+    ngram_propose (128 histories of 8192 tokens)."""
     import torch
 
     import speculative_decoding_verification_17_gb300 as sv
@@ -795,6 +797,18 @@ def kernels_once():
     A = torch.arange(0, 64, 2, dtype=torch.int32, device=dev)
     taus = torch.linspace(0, 8, 1024, device=dev)
     rs = torch.rand((npts,), generator=g, device=dev)
+    S, E, R = 2048, 16, 16384
+    zr = d["target"].reshape(-1, V)[:S]
+    sid = torch.arange(S, dtype=torch.int32, device=dev)
+    ent = torch.randint(0, 1000, (S, E), generator=g, device=dev, dtype=torch.int32)
+    n_s = torch.randint(0, 4096, (S,), generator=g, device=dev)
+    L = torch.full((S,), E, dtype=torch.int32, device=dev)
+    Bh = torch.full((S,), 64, dtype=torch.int64, device=dev)
+    table = sv.ReadyCacheTable(S, E, dev, V=V, dist_dtype=torch.bfloat16, keep_dist=False)
+    rq = torch.randint(0, S, (R,), generator=g, device=dev, dtype=torch.int32)
+    rstart, rtok, rlen = n_s[rq.long()], ent[rq.long()], L[rq.long()]
+    Av = torch.arange(0, V, 3, dtype=torch.int32, device=dev)
+    w4 = synth.workload_inputs(4, device=dev)
     for _ in range(2):
         sv.logit_gap_gate(rows2, w2["tau"], w2["answer_set"])
         sv.spec_verify_greedy(d["target"], d["draft_tokens"])
@@ -804,6 +818,9 @@ def kernels_once():
         sv.conformal_residual(d["draft"], tgt)
         sv.gate_risk_coverage(gp, tk, fl, A, taus, 1.959964, 0.1)
         sv.conformal_quantile(rs, 0.9)
+        table.record(sid, n_s, ent, L, Bh, zr)
+        table.serve(rq, rstart, rtok, rlen, 2.0, Av)
+        sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"], w4["k"])
     torch.cuda.synchronize()
     print("kernels-once ok")
 
