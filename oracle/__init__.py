@@ -55,7 +55,7 @@ def _bind(lib):
     D = ctypes.c_double
     lib.oracle_row_softmax.argtypes = [P, I, I, D, P]
     lib.oracle_spec_verify_sample.argtypes = [P, P, I, P, P, P, I, I, I, D,
-                                              P, P, P, P, P, P, P, P, P, I, I]
+                                              P, P, P, P, P, P, P, P, P, P, I, I]
     lib.oracle_spec_verify_greedy.argtypes = [P, I, P, P, I, I, I, P, P, I, I]
     lib.oracle_logit_gap_gate.argtypes = [P, I, I, I, D, P, I, P, P, P, P, I, I]
     lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, I, I]
@@ -247,6 +247,7 @@ def spec_verify_sample(target, draft, draft_tokens, num_draft, uniforms, T: floa
         margin=np.full(B, np.nan),
         t_lo=np.full(B, -2, np.int32),
         t_hi=np.full(B, -2, np.int32),
+        tie_prob=np.full(B, np.nan),
     )
     lib = _load()
     reqs = sorted(range(B) if requests is None else {int(r) for r in requests})
@@ -256,7 +257,7 @@ def spec_verify_sample(target, draft, draft_tokens, num_draft, uniforms, T: floa
             _ptr(tz), _ptr(dz), code, _ptr(x), _ptr(nd), _ptr(u), B, k, V, float(T),
             _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["p"]), _ptr(out["q"]),
             _ptr(out["resid"]), _ptr(out["flag_pos"]), _ptr(out["margin"]), _ptr(out["t_lo"]),
-            _ptr(out["t_hi"]), a, b)
+            _ptr(out["t_hi"]), _ptr(out["tie_prob"]), a, b)
 
     _run(fn, _ranges(reqs, threads), threads)
     return out

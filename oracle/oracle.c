@@ -135,13 +135,42 @@ static int select_at(const double* w, int V, double target) {
 
 static int uniform_ok(float u) { return u >= 0.0f && u < 1.0f; }
 
+/* The probability, over a target u*W with u uniform on [0, 1), that the inverse-CDF draw over
+ * w is flagged as a near tie: that the target lies within ORACLE_TIE_MARGIN * W of a boundary
+ * between two tokens of positive weight. The chosen token t covers [C_{t-1}, C_t); inside it,
+ * the flagged targets are the first margin*W (unless t is the first token of positive weight)
+ * and the last margin*W (unless t is the last), or all of it when it is shorter. */
+static double draw_tie_probability(const double* w, int V, double W) {
+  int first = -1, last = -1;
+  for (int j = 0; j < V; ++j)
+    if (w[j] > 0.0) {
+      if (first < 0) first = j;
+      last = j;
+    }
+  double prob = 0.0;
+  for (int j = 0; j < V; ++j) {
+    if (!(w[j] > 0.0)) continue;
+    const double window = ORACLE_TIE_MARGIN * ((j != first) + (j != last));
+    const double m = w[j] / W;
+    prob += m < window ? m : window;
+  }
+  return prob;
+}
+
+/* The probability, over u uniform on [0, 1), that |u - rho| < ORACLE_TIE_MARGIN. */
+static double accept_tie_probability(double rho) {
+  const double lo = rho - ORACLE_TIE_MARGIN > 0.0 ? rho - ORACLE_TIE_MARGIN : 0.0;
+  const double hi = rho + ORACLE_TIE_MARGIN < 1.0 ? rho + ORACLE_TIE_MARGIN : 1.0;
+  return hi > lo ? hi - lo : 0.0;
+}
+
 int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
                               const int32_t* draft_tokens, const int32_t* num_draft,
                               const float* uniforms, int B, int k, int V, double T,
                               int32_t* out_tokens, int32_t* out_accept_len, double* out_p,
                               double* out_q, double* out_resid, int32_t* out_flag_pos,
-                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi, int r0,
-                              int r1) {
+                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi,
+                              double* out_tie_prob, int r0, int r1) {
   if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 2 || !(T > 0.0) || !isfinite(T) ||
       (dtype != 0 && dtype != 1))
     return -1;
@@ -164,6 +193,7 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
     if (out_margin) out_margin[r] = INFINITY;
     if (out_t_lo) out_t_lo[r] = -1;
     if (out_t_hi) out_t_hi[r] = -1;
+    if (out_tie_prob) out_tie_prob[r] = 0.0;
 
     const int n = num_draft ? num_draft[r] : k;
     int err = (n < 0 || n > k);
@@ -204,9 +234,11 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
     /* Stage 3: accept x_i while u_i < p_i(x_i)/q_i(x_i); stop at the first rejection. */
     int flag = -1;
     double min_margin = INFINITY;
+    double tie_prob = 0.0;
     int a = n;
     for (int i = 0; i < n; ++i) {
       const double rho = px[i] / qx[i];
+      tie_prob += accept_tie_probability(rho);
       const double mg = fabs((double)u[i] - rho);
       if (mg < min_margin) min_margin = mg;
       if (mg < ORACLE_TIE_MARGIN && flag < 0) flag = i;
@@ -254,6 +286,7 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
     out_accept_len[r] = a;
     if (out_flag_pos) out_flag_pos[r] = flag;
     if (out_margin) out_margin[r] = min_margin;
+    if (out_tie_prob) out_tie_prob[r] = tie_prob + draw_tie_probability(w, V, W);
   }
   free(w);
   return 0;

@@ -36,7 +36,12 @@ int oracle_row_softmax(const void* row, int dtype, int V, double T, double* p_ou
  *                    position i, or the draw that emitted token a), or -1;
  *   out_margin[r]    the smallest margin among the decisions that fixed the result;
  *   out_t_lo[r], out_t_hi[r]  the first and last token the draw selects for any target
- *                    within ORACLE_TIE_MARGIN * W of u[r, k] * W (equal when no near tie).
+ *                    within ORACLE_TIE_MARGIN * W of u[r, k] * W (equal when no near tie);
+ *   out_tie_prob[r]  the chance that request r is flagged, given its path: for each accept
+ *                    test it took, the probability over u[r, i] that |u - rho_i| < the
+ *                    margin, plus the probability over u[r, k] that its draw is a near tie
+ *                    (the sum of min(w_t / W, margin per interior boundary of token t));
+ *                    0 for a data error. It sizes the expected count of flagged requests.
  * Every output pointer past out_accept_len may be NULL.
  * A request with a data error gets accept_len -1, tokens -1, p/q/resid NaN, flag -1. */
 int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
@@ -44,8 +49,8 @@ int oracle_spec_verify_sample(const void* target, const void* draft, int dtype,
                               const float* uniforms, int B, int k, int V, double T,
                               int32_t* out_tokens, int32_t* out_accept_len, double* out_p,
                               double* out_q, double* out_resid, int32_t* out_flag_pos,
-                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi, int r0,
-                              int r1);
+                              double* out_margin, int32_t* out_t_lo, int32_t* out_t_hi,
+                              double* out_tie_prob, int r0, int r1);
 
 /* Greedy verify; outputs as the library's spec_verify_greedy. */
 int oracle_spec_verify_greedy(const void* target, int dtype, const int32_t* draft_tokens,

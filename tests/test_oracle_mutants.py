@@ -49,6 +49,17 @@ MUTANTS = [
      "size_t off = ((size_t)r * (k + 1) + i) * (size_t)V;\n      if (softmax_stats(target",
      "size_t off = ((size_t)r * k + i) * (size_t)V;\n      if (softmax_stats(target",
      [S.test_q_equal_p_accepts_everything, S.test_residual_mass_identity_and_searchsorted]),
+    ("tie window on both sides of every token",
+     "const double window = ORACLE_TIE_MARGIN * ((j != first) + (j != last));",
+     "const double window = 2.0 * ORACLE_TIE_MARGIN;",
+     [S.test_tie_probability_is_the_measure_of_flagged_uniforms]),
+    ("tie probability without the token's own mass as a bound",
+     "prob += m < window ? m : window;", "prob += window;",
+     [S.test_tie_probability_is_the_measure_of_flagged_uniforms]),
+    ("accept tie window one-sided",
+     "const double hi = rho + ORACLE_TIE_MARGIN < 1.0 ? rho + ORACLE_TIE_MARGIN : 1.0;",
+     "const double hi = rho < 1.0 ? rho : 1.0;",
+     [S.test_tie_probability_is_the_measure_of_flagged_uniforms]),
     ("greedy emits the draft token at the mismatch", "tok[a] = g[a];",
      "tok[a] = a < n ? x[a] : g[a];", [R.test_greedy_argmax_and_walk]),
     ("greedy argmax keeps the last tie", "if (best < 0 || z > bv) {",

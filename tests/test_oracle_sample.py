@@ -321,3 +321,86 @@ def test_argument_validation():
     for T in (0.0, -1.0, np.inf, np.nan):
         with pytest.raises(ValueError):
             oracle.spec_verify_sample(z, d, x, None, u, T)
+
+
+def _flag_edge(flagged, lo, hi, iters=80):
+    """The point in [lo, hi] where flagged(u) changes (flagged(lo) != flagged(hi)), by
+    bisection over float32 values."""
+    f_lo = flagged(lo)
+    assert flagged(hi) != f_lo
+    for _ in range(iters):
+        mid = np.float32((np.float64(lo) + np.float64(hi)) / 2)
+        if mid in (lo, hi):
+            break
+        if flagged(mid) == f_lo:
+            lo = mid
+        else:
+            hi = mid
+    return (np.float64(lo) + np.float64(hi)) / 2
+
+
+def test_tie_probability_is_the_measure_of_flagged_uniforms():
+    """out_tie_prob is the chance, over the uniforms, that the oracle flags a near tie. Here
+    it is compared with the measure of the uniforms the oracle actually flags, found by
+    bisection on its own flag output: (1) a bonus draw whose first four tokens are tinier
+    than the margin (each flagged whole, the first one only at its upper boundary) ahead of
+    one large last token (flagged only at its lower boundary); (2) an accept test at
+    rho ~ 0.3 (flagged within the margin on either side)."""
+    # (1) n = 0: the bonus draw from p_0; every flagged target lies below ~5e-6
+    m = np.array([3e-7, 4e-7, 2e-6, 1e-6, 1.0], np.float64)
+    zt = np.log(m).astype(np.float32)[None, None, :].repeat(2, axis=1)
+    zd = np.zeros((1, 1, 5), np.float32)
+    x, nd = np.array([[0]], np.int32), np.array([0], np.int32)
+
+    def draw_flag(uk):
+        u = np.array([[0.5, uk]], np.float32)
+        return oracle.spec_verify_sample(zt, zd, x, nd, u, 1.0)["flag_pos"][0] >= 0
+
+    assert draw_flag(np.float32(0.0)) and not draw_flag(np.float32(0.5))
+    edge = _flag_edge(draw_flag, np.float32(0.0), np.float32(1e-4))
+    u = np.array([[0.5, 0.5]], np.float32)
+    tp = oracle.spec_verify_sample(zt, zd, x, nd, u, 1.0)["tie_prob"][0]
+    assert abs(tp - edge) < 1e-11, (tp, edge)
+    # nothing else is flagged: the last token has no upper boundary
+    for uk in (0.1, 0.9, np.nextafter(np.float32(1), np.float32(0))):
+        assert not draw_flag(np.float32(uk))
+
+    # (2) one accept test: p_0 uniform over 3 tokens, q_0(0) = 3/5, so rho = 5/9; a
+    # rejection draws from the residual over tokens 1 and 2 (one boundary, at W/2), an
+    # acceptance from the uniform p_1 (boundaries at 1/3 and 2/3)
+    V = 3
+    zt = np.zeros((1, 2, V), np.float32)
+    zd = np.zeros((1, 1, V), np.float32)
+    zd[0, 0, 0] = np.float32(np.log(3.0))
+    x, nd = np.array([[0]], np.int32), np.array([1], np.int32)
+
+    def run(u0, uk):
+        return oracle.spec_verify_sample(zt, zd, x, nd, np.array([[u0, uk]], np.float32), 1.0)
+
+    o = run(0.0, 0.25)
+    rho = o["p"][0, 0] / o["q"][0, 0]
+    assert abs(rho - 5.0 / 9.0) < 1e-6
+
+    def acc_flag(u0):
+        return run(u0, 0.25)["flag_pos"][0] == 0
+
+    lo = _flag_edge(acc_flag, np.float32(rho - 1e-5), np.float32(rho))
+    hi = _flag_edge(acc_flag, np.float32(rho), np.float32(rho + 1e-5))
+    accept_part = hi - lo
+    assert abs(accept_part - 2e-6) < 2 * np.spacing(np.float32(rho)), accept_part
+
+    def draw_width(u0, b):
+        """Measure of the flagged draw targets around the boundary b (in units of u_k)."""
+        def f(uk):
+            return run(u0, uk)["flag_pos"][0] >= 0
+        return (_flag_edge(f, np.float32(b), np.float32(b + 1e-5))
+                - _flag_edge(f, np.float32(b - 1e-5), np.float32(b)))
+
+    # rejected (u0 above rho): one residual boundary
+    u0 = np.float32(rho + 0.2)
+    want = accept_part + draw_width(u0, 0.5)
+    assert abs(run(u0, 0.25)["tie_prob"][0] - want) < 1e-12 + 4 * np.spacing(np.float32(0.5))
+    # accepted (u0 below rho): two bonus boundaries
+    u0 = np.float32(rho - 0.2)
+    want = accept_part + draw_width(u0, 1.0 / 3.0) + draw_width(u0, 2.0 / 3.0)
+    assert abs(run(u0, 0.25)["tie_prob"][0] - want) < 1e-12 + 8 * np.spacing(np.float32(0.7))
