@@ -61,7 +61,11 @@ typedef enum {
   SV_ERR_UNSUPPORTED = 2,  /* a legal request this library does not handle (k > 16, huge grids) */
   SV_ERR_WORKSPACE = 3,    /* workspace pointer null, misaligned or smaller than the query */
   SV_ERR_CUDA = 4,         /* a CUDA launch or attribute call failed; see sv_last_cuda_error */
-  SV_ERR_TIMEOUT = 5       /* reserved: no kernel in this library waits on another CTA */
+  SV_ERR_TIMEOUT = 5       /* reserved: no call returns it. The library's bounded device
+                              waits (the copy waits of every streaming kernel, and the grid
+                              barriers of conformal_quantile, whose CTAs wait on one another)
+                              report a wait that ran out through the call's outputs instead:
+                              see each call's error sentinel */
 } sv_status;
 
 typedef enum {
@@ -177,6 +181,11 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
  *     bytes); a larger shape returns SV_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on a device (with that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *     The address is kept for the life of the process, so resetting the device
+ *     (cudaDeviceReset, or releasing and re-creating its primary context) after the first
+ *     call is not supported.
+ *   - The host checks are spec_verify_greedy's, in the same order (sizes and dtype, then the
+ *     pointers and their alignment, then the grid size); the scratch limit is checked last.
  *   - Every call on a device shares the one array: it clears the counters it needs at the
  *     start (a small kernel on `stream`), and calls whose work overlaps on the GPU
  *     (on different streams, or from different host threads) race and give wrong results.

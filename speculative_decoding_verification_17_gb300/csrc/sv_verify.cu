@@ -1381,15 +1381,22 @@ extern "C" size_t spec_verify_greedy_workspace(int B, int k, int V, sv_dtype dty
   return greedy_layout(B, k, V, dtype).total;
 }
 
-extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
-                                        const int32_t* draft_tokens, const int32_t* num_draft,
-                                        int B, int k, int V, int32_t* out_tokens,
-                                        int32_t* out_accept_len, void* workspace,
-                                        size_t workspace_bytes, sv_stream_t stream) {
+namespace {
+
+// The host checks of a greedy-verify call, in the order both greedy entry points apply them:
+// sizes and dtype, then the pointers and their alignment, then the grid size. SV_OK for a
+// call that has work to launch; `empty` is set for B = 0 (a no-op).
+sv_status greedy_check(const void* target_logits, sv_dtype dtype, const int32_t* draft_tokens,
+                       const int32_t* num_draft, int B, int k, int V, const int32_t* out_tokens,
+                       const int32_t* out_accept_len, bool& empty) {
+  empty = false;
   if (B < 0 || k < 1 || V < 2) return SV_ERR_INVALID_ARG;
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
   if (k > SV_MAX_K) return SV_ERR_UNSUPPORTED;
-  if (B == 0) return SV_OK;
+  if (B == 0) {
+    empty = true;
+    return SV_OK;
+  }
   const int eb = elem_bytes(dtype);
   if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len)
     return SV_ERR_INVALID_ARG;
@@ -1397,10 +1404,25 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
       !aligned_to(out_tokens, 4) || !aligned_to(out_accept_len, 4) ||
       (num_draft && !aligned_to(num_draft, 4)))
     return SV_ERR_INVALID_ARG;
+  const int64_t units = (int64_t)B * (k + 1) * num_segments(num_chunks(V, dtype));
+  if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype,
+                                        const int32_t* draft_tokens, const int32_t* num_draft,
+                                        int B, int k, int V, int32_t* out_tokens,
+                                        int32_t* out_accept_len, void* workspace,
+                                        size_t workspace_bytes, sv_stream_t stream) {
+  bool empty = false;
+  const sv_status chk = greedy_check(target_logits, dtype, draft_tokens, num_draft, B, k, V,
+                                     out_tokens, out_accept_len, empty);
+  if (chk != SV_OK || empty) return chk;
   const int64_t nch = num_chunks(V, dtype);
   const int nseg = num_segments(nch);
   const int64_t units = (int64_t)B * (k + 1) * nseg;
-  if (units > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
   const GreedyLayout L = greedy_layout(B, k, V, dtype);
   if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total)
     return SV_ERR_WORKSPACE;
@@ -1438,7 +1460,9 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
 // is not allowed. For them the greedy verify can use a scratch buffer that lives in this
 // library's own device image: a fixed array every GPU that loads the library holds until the
 // process exits. Its device address is looked up once per device, on the first call made with
-// that device current.
+// that device current, and kept for the life of the process: a cudaDeviceReset (or any other
+// teardown of the device's primary context) after that first call is not supported, since
+// the kept address would then name memory the new context does not hold.
 namespace {
 
 constexpr size_t kGreedyScratchBytes = size_t(8) << 20;  // 8 MiB
@@ -1473,10 +1497,11 @@ extern "C" sv_status spec_verify_greedy_noalloc(const void* target_logits, sv_dt
                                                 const int32_t* num_draft, int B, int k, int V,
                                                 int32_t* out_tokens, int32_t* out_accept_len,
                                                 sv_stream_t stream) {
-  if (B < 0 || k < 1 || V < 2) return SV_ERR_INVALID_ARG;
-  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
-  if (k > SV_MAX_K) return SV_ERR_UNSUPPORTED;
-  if (B == 0) return SV_OK;
+  // the same checks, in the same order, as spec_verify_greedy; then the scratch limit
+  bool empty = false;
+  const sv_status chk = greedy_check(target_logits, dtype, draft_tokens, num_draft, B, k, V,
+                                     out_tokens, out_accept_len, empty);
+  if (chk != SV_OK || empty) return chk;
   if (greedy_layout(B, k, V, dtype).total > kGreedyScratchBytes) return SV_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const sv_status st = greedy_scratch_address(&scratch);
