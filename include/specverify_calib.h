@@ -130,6 +130,27 @@ sv_status conformal_quantile(const float* resid, int n, double q, float* out_q,
                              void* workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * Self-test of the quantile's bounded grid barriers.
+ *
+ * A library diagnostic; the pages have no counterpart. It makes the one launch of this
+ * library whose CTAs wait on one another give up, on purpose, so that a test can see the
+ * wait end and the timeout reported, with no fault and no hang: the same cooperative
+ * select launch as conformal_quantile over n > 8192 scores, except that every grid barrier
+ * waits for one arrival more than the grid has. No barrier can complete; each CTA waits
+ * wait_us microseconds, gives up and returns. out_q then holds the timeout sentinel, the
+ * quiet NaN with payload 1 (bits 0x7fc00001), and the device stays usable (the workspace
+ * too: conformal_quantile clears it at every call).
+ * Arguments
+ *   resid, out_q, workspace   as for conformal_quantile (the scores are read, not ranked).
+ *   n                         > 8192 (smaller sets take the one-CTA path, which never waits).
+ *   wait_us                   1 .. 100000: how long each barrier waits before giving up.
+ * Returns SV_ERR_INVALID_ARG / SV_ERR_WORKSPACE on bad arguments, else the launch status.
+ * ---------------------------------------------------------------------------------------- */
+sv_status conformal_quantile_barrier_selftest(const float* resid, int n, float* out_q,
+                                              void* workspace, size_t workspace_bytes,
+                                              unsigned int wait_us, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * Conformal gate over K layers.
  *
  * Defined by: the same note, "conformal_admit(cal_k, q, gamma)": per decoding step, the

@@ -138,6 +138,8 @@ def _declare(L):
     L.conformal_quantile_workspace.argtypes = [I]
     L.conformal_quantile.restype = I
     L.conformal_quantile.argtypes = [P, I, D, P, P, Z, P]
+    L.conformal_quantile_barrier_selftest.restype = I
+    L.conformal_quantile_barrier_selftest.argtypes = [P, I, P, P, Z, ctypes.c_uint, P]
     L.conformal_admit_workspace.restype = Z
     L.conformal_admit_workspace.argtypes = [I, I, I, I]
     L.conformal_admit.restype = I

@@ -554,9 +554,10 @@ __device__ __forceinline__ float key_float(unsigned int k) {
 }
 
 // Grid barrier of a cooperative launch (every CTA resident): each CTA adds one to *count
-// (release, after the CTA's earlier writes) and waits until all gridDim.x have (acquire), for
-// at most kSelWaitNs. False, for the whole CTA, if the wait ran out.
-__device__ bool grid_barrier(unsigned int* count) {
+// (release, after the CTA's earlier writes) and waits until `target` have (acquire; target is
+// gridDim.x, or more in the barrier self-test), for at most limit_ns. False, for the whole
+// CTA, if the wait ran out.
+__device__ bool grid_barrier(unsigned int* count, unsigned int target, uint64_t limit_ns) {
   __shared__ int ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -568,13 +569,13 @@ __device__ bool grid_barrier(unsigned int* count) {
                  : "memory");
     ++seen;
     const uint64_t t0 = globaltimer_ns();
-    while (seen < gridDim.x) {
-      if (globaltimer_ns() - t0 > kSelWaitNs) break;
+    while (seen < target) {
+      if (globaltimer_ns() - t0 > limit_ns) break;
       __nanosleep(64);
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(count) : "memory");
     }
     __threadfence();
-    ok = seen >= gridDim.x;
+    ok = seen >= target;
   }
   __syncthreads();
   return ok != 0;
@@ -585,9 +586,13 @@ __device__ bool grid_barrier(unsigned int* count) {
 // thread and step, four 16-byte loads in flight) and adds it to the pass's global histogram;
 // after a grid barrier, every CTA reads that histogram and picks the same digit d, the one
 // with (keys below it) < want <= (keys below it) + count(d). The first two passes load the
-// scores with an L2 evict-last policy, so the next pass finds them in L2.
+// scores with an L2 evict-last policy, so the next pass finds them in L2. Each barrier waits
+// for gridDim.x + extra arrivals (extra = 0; 1 only in the barrier self-test, where no
+// barrier can complete) for at most limit_ns.
 __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int n, int64_t rank,
-                                                             SelectState* st, float* out) {
+                                                             SelectState* st, float* out,
+                                                             unsigned int extra,
+                                                             uint64_t limit_ns) {
   __shared__ unsigned int h[kSelBins];
   __shared__ unsigned int warp_tot[kCalThreads / 32];
   __shared__ unsigned int s_digit, s_before;
@@ -636,7 +641,7 @@ __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int
     __syncthreads();
     for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
       if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
-    if (!grid_barrier(&st->cnt[pass])) {
+    if (!grid_barrier(&st->cnt[pass], gridDim.x + extra, limit_ns)) {
       if (blockIdx.x == 0 && threadIdx.x == 0) *out = __uint_as_float(kSelTimedOut);
       return;
     }
@@ -843,6 +848,48 @@ extern "C" sv_status conformal_residual(const void* draft_logits, const void* tr
   return launch_status();
 }
 
+namespace sv {
+
+// The cooperative radix-select launch of conformal_quantile (more than kSmallSelect scores):
+// clear the state, size the grid, launch. extra and limit_ns go to the grid barriers.
+sv_status launch_select(const float* resid, int n, int64_t rank, float* out_q, void* workspace,
+                        unsigned int extra, uint64_t limit_ns, cudaStream_t st) {
+  const size_t need = round_up(sizeof(SelectState), 256);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  SelectState* S = static_cast<SelectState*>(workspace);
+  // A cooperative launch: every CTA must be resident at once for the grid barriers. Up to
+  // four CTAs per SM (as many as fit), no more than one CTA per 4096 scores; the occupancy
+  // answer is kept per device (a host query that would otherwise delay every launch).
+  static std::atomic<int> occ_cache[64];
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int per_sm = dev >= 0 && dev < 64 ? occ_cache[dev].load() : 0;
+  if (per_sm <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel, kCalThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm <= 0) return SV_ERR_UNSUPPORTED;
+    if (dev >= 0 && dev < 64) occ_cache[dev].store(per_sm);
+  }
+  const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
+  const int64_t slots = (int64_t)std::min(per_sm, 4) * device_sm_count();
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
+  const float* r = resid;
+  int nn = n;
+  int64_t rk64 = rank;
+  float* o = out_q;
+  unsigned int ex = extra;
+  uint64_t lim = limit_ns;
+  void* args[] = {&r, &nn, &rk64, &S, &o, &ex, &lim};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(select_kernel), dim3(grid),
+                                  dim3(kCalThreads), args, 0, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return SV_OK;
+}
+
+}  // namespace sv
+
 extern "C" size_t conformal_quantile_workspace(int n) {
   if (n < 1) return 0;
   return round_up(sizeof(SelectState), 256);
@@ -868,33 +915,22 @@ extern "C" sv_status conformal_quantile(const float* resid, int n, double q, flo
     select_small_kernel<<<1, kCalThreads, 0, st>>>(resid, n, (int)rank, out_q);
     return launch_status();
   }
-  cudaError_t e = cudaMemsetAsync(workspace, 0, need, st);
-  if (e != cudaSuccess) return cuda_fail(e);
-  SelectState* S = static_cast<SelectState*>(workspace);
-  // A cooperative launch: every CTA must be resident at once for the grid barriers. Up to
-  // four CTAs per SM (as many as fit), no more than one CTA per 4096 scores; the occupancy
-  // answer is kept per device (a host query that would otherwise delay every launch).
-  static std::atomic<int> occ_cache[64];
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  int per_sm = dev >= 0 && dev < 64 ? occ_cache[dev].load() : 0;
-  if (per_sm <= 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel, kCalThreads, 0);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm <= 0) return SV_ERR_UNSUPPORTED;
-    if (dev >= 0 && dev < 64) occ_cache[dev].store(per_sm);
-  }
-  const int64_t want = ((int64_t)n + 16 * kCalThreads - 1) / (16 * kCalThreads);
-  const int64_t slots = (int64_t)std::min(per_sm, 4) * device_sm_count();
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, slots));
-  const float* r = resid;
-  int nn = n;
-  int64_t rk64 = rank;
-  float* o = out_q;
-  void* args[] = {&r, &nn, &rk64, &S, &o};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(select_kernel), dim3(grid),
-                                  dim3(kCalThreads), args, 0, st);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return SV_OK;
+  return launch_select(resid, n, rank, out_q, workspace, 0u, kSelWaitNs, st);
 }
+
+extern "C" sv_status conformal_quantile_barrier_selftest(const float* resid, int n,
+                                                         float* out_q, void* workspace,
+                                                         size_t workspace_bytes,
+                                                         unsigned int wait_us,
+                                                         sv_stream_t stream) {
+  if (n <= kSmallSelect || wait_us < 1 || wait_us > 100000) return SV_ERR_INVALID_ARG;
+  if (!resid || !out_q || !aligned_to(resid, 4) || !aligned_to(out_q, 4))
+    return SV_ERR_INVALID_ARG;
+  const size_t need = round_up(sizeof(SelectState), 256);
+  if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < need)
+    return SV_ERR_WORKSPACE;
+  // one arrival more than the grid at every barrier: none completes, every wait runs out
+  return launch_select(resid, n, (int64_t)(n / 2 + 1), out_q, workspace, 1u,
+                       (uint64_t)wait_us * 1000ull, reinterpret_cast<cudaStream_t>(stream));
+}
+

@@ -155,6 +155,13 @@ def test_calibration_validation():
     assert cq(wsb=64) == WORKSPACE
     assert L.conformal_quantile_workspace(0) == 0 and L.conformal_quantile_workspace(5) > 0
 
+    bs = lambda **kw: L.conformal_quantile_barrier_selftest(
+        kw.get("r", FAKE), kw.get("n", 10000), kw.get("out", FAKE), kw.get("ws", ws),
+        kw.get("wsb", 1 << 30), kw.get("us", 1000), None)
+    assert bs(n=8192) == INVALID and bs(us=0) == INVALID and bs(us=100001) == INVALID
+    assert bs(r=None) == INVALID and bs(out=None) == INVALID and bs(wsb=64) == WORKSPACE
+    assert bs(r=ctypes.c_void_p(0x10002)) == INVALID
+
     ca = lambda **kw: L.conformal_admit(kw.get("z", FAKE), kw.get("dtype", 1), kw.get("N", 3),
                                         kw.get("K", 2), kw.get("V", 50), kw.get("Q", FAKE),
                                         kw.get("lay", FAKE), FAKE, None, kw.get("ws", ws),

@@ -338,6 +338,41 @@ def test_quantile_reuses_its_workspace():
         assert got == oracle.conformal_quantile(r, q)
 
 
+def test_quantile_barrier_wait_runs_out_and_reports_it():
+    """The quantile's cooperative launch is the one place where CTAs wait on one another.
+    Its self-test entry sets every grid barrier's arrival target one above the grid, so no
+    barrier completes: each wait must give up after its limit (here 1 ms), the launch must
+    end on its own, and out_q must carry the timeout sentinel (quiet NaN, payload 1). The
+    device, and the same workspace, must then serve a normal call."""
+    import ctypes
+
+    n = 1 << 20
+    rng = np.random.default_rng(11)
+    r = rng.exponential(1.0, n).astype(np.float32)
+    d = _dev(r)
+    ws = torch.zeros(sv.conformal_quantile_workspace(n), dtype=torch.uint8, device=DEV)
+    out = torch.zeros(1, dtype=torch.float32, device=DEV)
+    P = ctypes.c_void_p
+    L = sv.library()
+    h = torch.cuda.current_stream().cuda_stream
+    for wait_us in (1000, 200):
+        out.fill_(0.0)
+        st = L.conformal_quantile_barrier_selftest(P(d.data_ptr()), n, P(out.data_ptr()),
+                                                   P(ws.data_ptr()), ws.numel(), wait_us, P(h))
+        assert st == 0, L.sv_status_string(st)
+        torch.cuda.synchronize()
+        assert out.view(torch.int32).item() == 0x7FC00001
+    # bad arguments are refused on the host
+    assert L.conformal_quantile_barrier_selftest(P(d.data_ptr()), 8192, P(out.data_ptr()),
+                                                 P(ws.data_ptr()), ws.numel(), 1000, P(h)) == 1
+    assert L.conformal_quantile_barrier_selftest(P(d.data_ptr()), n, P(out.data_ptr()),
+                                                 P(ws.data_ptr()), ws.numel(), 0, P(h)) == 1
+    # the context and the workspace still serve a normal call
+    got = sv.conformal_quantile(d, 0.9, workspace=ws)
+    torch.cuda.synchronize()
+    assert _same_f32(got.cpu().numpy(), [oracle.conformal_quantile(r, 0.9)])
+
+
 # ------------------------------------------------------------------------------ admission
 def _layer_logits(N, K, V, dt, seed, peak_hi=8.0):
     g = torch.Generator().manual_seed(seed)
