@@ -67,110 +67,144 @@ __device__ __forceinline__ int64_t chunk_end(int64_t j0, int V) {
 // In-order draw inside one sub-range of a chunk
 // ============================================================================================
 struct ScanSmem {
+  DF wtot[kWarps];  // each warp's total weight
+  int first;        // the first vector whose running weight passes the target
+  int lastpos;      // the sub-range's last token of positive weight
   int result;
 };
 
-// Inverse-CDF draw inside the sub-range that starts at s0 (kRounds rounds of 32 16-byte
-// vectors; the weights are zero past its end): the first logit j, in vocabulary order, whose
-// running weight exceeds `target` (in the sub-range's units); when rounding leaves the target
-// at or past the sub-range's total, or take_last is set, the last logit with positive weight.
-// One warp walks the rounds in order: a lane sums its vector's weights in order in fp32, a
-// float-float warp scan of the lane sums places the crossing lane, and that lane walks its
-// vector. The scan adds in another order than the masses that chose the sub-range; where
-// that moves the answer, the target lies within rounding of a boundary, and the walk falls
-// back to the last positive weight. Every consumer thread calls this; warp 0 works.
+// Inverse-CDF draw inside the sub-range that starts at s0 (kRounds * 32 16-byte vectors; the
+// weights are zero past its end): the first logit j, in vocabulary order, whose running
+// weight exceeds `target` (in the sub-range's units); when rounding leaves the target at or
+// past the sub-range's total, or take_last is set, the last logit with positive weight.
+// Thread t < kRounds * 32 takes vector t and sums its weights in order in fp32; a float-float
+// scan of those sums over the block places the crossing vector, and its thread walks it. The
+// scan adds in another order than the masses that chose the sub-range; where that moves the
+// answer, the target lies within rounding of a boundary, and the walk falls back to the last
+// positive weight. Every consumer thread calls this.
 // VW provides: using Raw; Raw load(int64_t j) const; void weights(const Raw&, float (&)[]).
 template <typename E, int kRounds, typename VW>
-__device__ int scan_sub(int64_t s0, double target, bool take_last, const VW& vw,
-                        ScanSmem& sm) {
-  constexpr int kRound = 32 * E::kPerVec;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const DF tgt = df_from_double(target);
-    DF run{0.0f, 0.0f};
-    int lastpos = -1, found = -1;
-    for (int r = 0; r < kRounds && found < 0; ++r) {  // warp-uniform
-      const int64_t base = s0 + (int64_t)r * kRound + lane * E::kPerVec;
-      const typename VW::Raw raw = vw.load(base);
-      float wt[E::kPerVec];
-      vw.weights(raw, wt);
-      float acc = 0.0f;
-      int lp = -1;
-#pragma unroll
-      for (int l = 0; l < E::kPerVec; ++l) {
-        acc += wt[l];
-        if (wt[l] > 0.0f) lp = (int)(base + l);
-      }
-      lastpos = max(lastpos, __reduce_max_sync(0xffffffffu, lp));
-      const DF incl = df_warp_scan(DF{acc, 0.0f});
-      DF lex = df_shfl_up(incl, 1);
-      if (lane == 0) lex = DF{0.0f, 0.0f};
-      const DF start = df_add(run, lex);
-      const DF through = df_add(start, DF{acc, 0.0f});
-      const unsigned bl =
-          __ballot_sync(0xffffffffu, !take_last && acc > 0.0f && df_gt(through, tgt));
-      if (bl) {
-        const int L = __ffs(bl) - 1;
-        int tk = -1;
-        if (lane == L) {
-          DF rr = start;
-#pragma unroll
-          for (int l = 0; l < E::kPerVec; ++l) {
-            rr = df_add(rr, DF{wt[l], 0.0f});
-            if (wt[l] > 0.0f && tk < 0 && df_gt(rr, tgt)) tk = (int)(base + l);
-          }
-          if (tk < 0) tk = lp;  // rounding inside the vector: its last positive weight
-        }
-        found = __shfl_sync(0xffffffffu, tk, L);
-      }
-      run = df_add(run, DF{__shfl_sync(0xffffffffu, incl.hi, 31),
-                           __shfl_sync(0xffffffffu, incl.lo, 31)});
-    }
-    if (lane == 0) sm.result = found >= 0 ? found : lastpos;
+__device__ int scan_sub(int64_t s0, DF target, bool take_last, const VW& vw, ScanSmem& sm) {
+  constexpr int kVec = kRounds * 32;
+  static_assert(kVec <= kThreads, "one vector per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sm.first = kThreads;
+    sm.lastpos = -1;
   }
+  const int64_t base = s0 + (int64_t)tid * E::kPerVec;
+  float wt[E::kPerVec];
+  float acc = 0.0f;
+  int lp = -1;
+  if (tid < kVec) {
+    const typename VW::Raw raw = vw.load(base);
+    vw.weights(raw, wt);
+#pragma unroll
+    for (int l = 0; l < E::kPerVec; ++l) {
+      acc += wt[l];
+      if (wt[l] > 0.0f) lp = (int)(base + l);
+    }
+  } else {
+#pragma unroll
+    for (int l = 0; l < E::kPerVec; ++l) wt[l] = 0.0f;
+  }
+  const DF incl = df_warp_scan(DF{acc, 0.0f});
+  DF ex = df_shfl_up(incl, 1);
+  if (lane == 0) ex = DF{0.0f, 0.0f};
+  if (lane == 31) sm.wtot[warp] = incl;
+  cbar();
+  DF start{0.0f, 0.0f};
+  for (int w = 0; w < warp; ++w) start = df_add(start, sm.wtot[w]);
+  start = df_add(start, ex);
+  const DF through = df_add(start, DF{acc, 0.0f});
+  const unsigned bl =
+      __ballot_sync(0xffffffffu, !take_last && acc > 0.0f && df_gt(through, target));
+  if (bl && lane == __ffs(bl) - 1) atomicMin(&sm.first, tid);
+  const int lpw = __reduce_max_sync(0xffffffffu, lp);
+  if (lane == 0 && lpw >= 0) atomicMax(&sm.lastpos, lpw);
+  cbar();
+  const int first = sm.first;
+  if (tid == first) {
+    int tk = -1;
+    DF rr = start;
+#pragma unroll
+    for (int l = 0; l < E::kPerVec; ++l) {
+      rr = df_add(rr, DF{wt[l], 0.0f});
+      if (wt[l] > 0.0f && tk < 0 && df_gt(rr, target)) tk = (int)(base + l);
+    }
+    sm.result = tk < 0 ? lp : tk;  // rounding inside the vector: its last positive weight
+  }
+  if (tid == 0 && first == kThreads) sm.result = sm.lastpos;
   cbar();
   return sm.result;
 }
 
-// Chunk choice for an inverse-CDF draw over per-chunk masses mass(c), c in [0, nch): the
-// first chunk whose running total exceeds target. Run by one full warp, in float-float sums.
-// Returns the chunk (or, when rounding leaves none, the last chunk with positive mass and
-// take_last = true) and the running total before it.
+// u * a for a float u, as a float-float number (about 48 bits).
+__device__ __forceinline__ DF df_mul_f(DF a, float u) {
+  const float p = a.hi * u;
+  float e = fmaf(a.hi, u, -p);
+  e = fmaf(a.lo, u, e);
+  const float h = __fadd_rn(p, e);
+  return {h, __fsub_rn(e, __fsub_rn(h, p))};
+}
+
+// The inverse-CDF choice of a sub-range, by one full warp: over the n masses mass(f),
+// f in [0, n), in vocabulary order, the first f whose running total exceeds u * W, W the
+// total. Lane l sums the block [l*m, (l+1)*m), m = ceil(n/32), in float-float; a warp scan
+// of the block sums gives each block's running total and W; the lane whose block first
+// passes the target walks it. When rounding leaves no such f, the last f of positive mass,
+// with take_last. Returns f (-1 when nothing has positive mass) and, in every lane, W and the
+// target's offset into f (target minus the running total before f).
 template <typename MF>
-__device__ int pick_chunk(int nch, DF target, MF mass, DF& before, bool& take_last) {
+__device__ int pick_flat(int n, float u, MF mass, DF& W, DF& offset, bool& take_last) {
   const int lane = threadIdx.x & 31;
-  DF run{0.0f, 0.0f};
-  int last_pos = -1;
-  DF last_before{0.0f, 0.0f};
-  for (int c0 = 0; c0 < nch; c0 += 32) {
-    const int c = c0 + lane;
-    const DF m = c < nch ? mass(c) : DF{0.0f, 0.0f};
-    const DF incl = df_warp_scan(m);
-    DF ex = df_shfl_up(incl, 1);
-    if (lane == 0) ex = DF{0.0f, 0.0f};
-    const DF through = df_add(run, df_add(ex, m));
-    const unsigned bal = __ballot_sync(0xffffffffu, c < nch && m.hi > 0.0f &&
-                                                        df_gt(through, target));
-    if (bal) {
-      const int fl = __ffs(bal) - 1;
-      before = df_add(run, DF{__shfl_sync(0xffffffffu, ex.hi, fl),
-                              __shfl_sync(0xffffffffu, ex.lo, fl)});
-      take_last = false;
-      return c0 + fl;
-    }
-    const unsigned pos = __ballot_sync(0xffffffffu, c < nch && m.hi > 0.0f);
-    if (pos) {
-      const int ll = 31 - __clz(pos);
-      last_pos = c0 + ll;
-      last_before = df_add(run, DF{__shfl_sync(0xffffffffu, ex.hi, ll),
-                                   __shfl_sync(0xffffffffu, ex.lo, ll)});
-    }
-    run = df_add(run, DF{__shfl_sync(0xffffffffu, incl.hi, 31),
-                         __shfl_sync(0xffffffffu, incl.lo, 31)});
+  const int m = (n + 31) / 32;
+  const int f0 = lane * m, f1 = min(f0 + m, n);
+  DF bs{0.0f, 0.0f};
+  int lastf = -1;
+  for (int f = f0; f < f1; ++f) {
+    const DF x = mass(f);
+    bs = df_add(bs, x);
+    if (x.hi > 0.0f) lastf = f;
   }
-  before = last_before;
-  take_last = true;
-  return last_pos;
+  const DF incl = df_warp_scan(bs);
+  W = DF{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+  const DF tgt = df_mul_f(W, u);
+  DF ex = df_shfl_up(incl, 1);
+  if (lane == 0) ex = DF{0.0f, 0.0f};
+  const unsigned bal = __ballot_sync(0xffffffffu, lastf >= 0 && df_gt(incl, tgt));
+  int pick = -1;
+  DF before{0.0f, 0.0f};
+  bool tl = true;
+  int L;
+  if (bal) {
+    L = __ffs(bal) - 1;
+    if (lane == L) {
+      DF run = ex;
+      for (int f = f0; f < f1; ++f) {
+        const DF x = mass(f);
+        const DF nr = df_add(run, x);
+        if (x.hi > 0.0f && df_gt(nr, tgt)) {
+          pick = f;
+          before = run;
+          tl = false;
+          break;
+        }
+        run = nr;
+      }
+      if (pick < 0) pick = lastf;  // rounding inside the block: its last positive mass
+    }
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, lastf >= 0);
+    L = pos ? 31 - __clz(pos) : 0;
+    if (lane == L) pick = lastf;
+  }
+  pick = __shfl_sync(0xffffffffu, pick, L);
+  tl = __shfl_sync(0xffffffffu, tl ? 1 : 0, L) != 0;
+  before = DF{__shfl_sync(0xffffffffu, before.hi, L), __shfl_sync(0xffffffffu, before.lo, L)};
+  offset = df_add(tgt, DF{-before.hi, -before.lo});
+  take_last = tl;
+  return pick;
 }
 
 // ============================================================================================
@@ -467,7 +501,8 @@ struct SampleOp {
     float zx;              // the logit of the row's draft token, when prefetched
     int row_last, req_last;
     int a, err, chunk, take_last;
-    double W, before;
+    double W;
+    DF before;
     ScanSmem scan;
     DF cm[kSmemChunks * (2 * kWarps + 1)];  // the draw's sub-range masses, then chunk masses
   };
@@ -716,9 +751,9 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
   return draw_select(A, vw, part, landed, u, sm, ring, t, W);
 }
 
-// The rest of a draw, from the sub-range masses in part (every chunk's): the chunk masses
-// and their total W, the chunk and then the sub-range in which u*W falls, and that sub-range
-// scanned in vocabulary order. Every thread calls this.
+// The rest of a draw, from the sub-range masses in part (every chunk's, in vocabulary
+// order): their total W and the sub-range in which u*W falls (one warp, pick_flat), then that
+// sub-range scanned in vocabulary order by the whole CTA. Every thread calls this.
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, bool landed,
@@ -728,52 +763,23 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
   constexpr int kSubs = DR::kPiecesPerChunk * kWarps;  // sub-ranges of a chunk
   constexpr int kSubElems = DR::kVecPerLane * 32 * E::kPerVec;
   constexpr int kPieceElems = DR::kPieceBytes / 16 * E::kPerVec;
-  // the chunk masses M_c = sum of the chunk's sub-range masses (fixed order), and
-  // W = sum_c M_c (warp 0), all in float-float sums; M_c goes after the sub-range masses
-  DF* cmass = part + (int64_t)A.nch * kSubs;
+  // one warp: W and the sub-range in which u*W falls (the flat pick over every chunk's
+  // sub-range masses, in vocabulary order)
   if (tid < 32) {
-    DF wsum{0.0f, 0.0f};
-    for (int c = lane; c < A.nch; c += 32) {
-      DF mc{0.0f, 0.0f};
-#pragma unroll
-      for (int q = 0; q < kSubs; ++q) mc = df_add(mc, part[(int64_t)c * kSubs + q]);
-      cmass[c] = mc;
-      wsum = df_add(wsum, mc);
+    DF Wd, off;
+    bool tl;
+    const int f = pick_flat(A.nch * kSubs, u, [&](int i) { return part[i]; }, Wd, off, tl);
+    if (lane == 0) {
+      sm.W = (double)Wd.hi + (double)Wd.lo;
+      sm.chunk = f < 0 ? 0 : f;
+      sm.before = off;
+      sm.take_last = tl;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum = df_add(wsum, df_shfl_xor(wsum, o));
-    if (lane == 0) sm.W = (double)wsum.hi + (double)wsum.lo;
   }
   __syncthreads();
   W = sm.W;
   if (!landed || W != W) return kDrawFailed;
   if (!(W > 0.0)) return kDrawNoMass;
-  const double target = (double)u * W;
-  if (tid < 32) {
-    // the chunk in which u*W falls, then the sub-range of that chunk (one lane per sub-range)
-    DF before;
-    bool tl;
-    int c = pick_chunk(A.nch, df_from_double(target), [&](int cc) { return cmass[cc]; },
-                       before, tl);
-    c = c < 0 ? 0 : (c >= A.nch ? A.nch - 1 : c);
-    const double tc = target - ((double)before.hi + (double)before.lo);
-    const DF tcd = df_from_double(tc);
-    const DF m = lane < kSubs ? part[(int64_t)c * kSubs + lane] : DF{0.0f, 0.0f};
-    const DF incl = df_warp_scan(m);
-    DF ex = df_shfl_up(incl, 1);
-    if (lane == 0) ex = DF{0.0f, 0.0f};
-    const unsigned bal =
-        __ballot_sync(0xffffffffu, !tl && lane < kSubs && m.hi > 0.0f && df_gt(incl, tcd));
-    const unsigned pos = __ballot_sync(0xffffffffu, lane < kSubs && m.hi > 0.0f);
-    const int q = bal ? __ffs(bal) - 1 : (pos ? 31 - __clz(pos) : 0);
-    const DF exq = DF{__shfl_sync(0xffffffffu, ex.hi, q), __shfl_sync(0xffffffffu, ex.lo, q)};
-    if (lane == 0) {
-      sm.chunk = c * kSubs + q;
-      sm.before = tc - ((double)exq.hi + (double)exq.lo);
-      sm.take_last = tl || !bal;
-    }
-  }
-  __syncthreads();
   const int c = sm.chunk / kSubs, q = sm.chunk - (sm.chunk / kSubs) * kSubs;
   const int64_t s0 = (int64_t)c * E::kChunk + (int64_t)(q / kWarps) * kPieceElems +
                      (int64_t)(q % kWarps) * kSubElems;
