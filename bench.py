@@ -85,15 +85,16 @@ def source_digest(unit: str = "sv_verify.cu") -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+def profiled_traffic(kernel: str, workload: str, unit: str = "sv_verify.cu"):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source
+    (the translation unit `unit` and what it includes)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_digest():
+    if not m or not s or s.group(1) != source_digest(unit):
         return None
     return float(m.group(1))
 
@@ -316,6 +317,7 @@ def gb300_arm(args, rank, world, local_rank):
     per = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(per)
     mean_ms = total_ms / len(per)
+    args.median_ms = statistics.median(per)
     total_ms = max_over_ranks(dist, total_ms, dev)
     acc = outs["out_accept_len"].float().mean().item()
 
@@ -368,6 +370,8 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
     rows = {}
     if rank == 0 and not args.no_rows:
         rows = secondary_rows(args, dev, stream, peak, head=d)
+        # the secondary rows on a line of their own, ahead of the headline line
+        print(json.dumps({"rows": rows}), flush=True)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -398,6 +402,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
                 "l2": f"inputs {abytes / 1e9:.2f} GB per step vs the 129 MB L2: no flush",
                 "parallelism": f"request-sharded replicas x{world}" if world > 1 else "single GPU",
             },
+            "ms_per_step_median": getattr(args, "median_ms", None),
             "logit_gbs": achieved,
             "mean_accept_len": acc,
             "roofline": {
@@ -413,6 +418,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
                 "traffic": profiled_traffic("segment_kernel_sample", f"b{B}_k{k}_v{V}_{w.dtype}"),
                 "algorithmic_bytes_per_launch": abytes,
                 "launch_ms": mean_ms,
+                "launch_ms_median": getattr(args, "median_ms", None),
             },
             "e2e": e2e,
             "gpu_launches": args.steps * args.launches_per_step,
@@ -422,11 +428,34 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
         if cpu is not None:
             line["cpu_baseline"] = cpu
         if rows:
-            line["rows"] = rows
+            line["configs_2_3"] = target_configs(rows, line)
         print(json.dumps(line))
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def target_configs(rows, line):
+    """The two configurations the >= 70 % bandwidth target names, in brief: the fp32 sampled
+    verify (B=256, k=4, V=151936) with its 1280-row gate, and the bf16 sampled verify (B=512,
+    k=8, V=128256; the headline, or its row when another workload was timed). Each gives ms
+    per launch (median), GB/s, the fraction of the peak and, where a committed ncu summary
+    was taken on the current source, the DRAM traffic per launch."""
+    out = {}
+    for key, src, kern, unit in (
+            ("sample_b256_k4_v151936_f32", "sample_b256_k4_v151936_f32", "segment_kernel",
+             "sv_verify.cu"),
+            ("gate_n1280_v151936_f32", "gate_n1280_v151936_f32", "segment_kernel", "sv_gate.cu")):
+        r = rows.get(src)
+        if r:
+            out[key] = {"ms": r["ms"], "gbs": r["gbs"], "frac": r["frac"], "bytes": r["bytes"],
+                        "traffic": profiled_traffic(kern, key, unit)}
+    rf = line["roofline"]
+    if line["config"]["workload"].startswith("sampled verify b512_k8_v128256_bf16"):
+        out["sample_b512_k8_v128256_bf16"] = {
+            "ms": rf["launch_ms_median"], "gbs": rf["achieved"], "frac": rf["frac"],
+            "bytes": rf["algorithmic_bytes_per_launch"], "traffic": rf["traffic"]}
+    return out
 
 
 def secondary_rows(args, dev, stream, peak, head=None):
@@ -450,7 +479,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
     B, k, V = d["B"], d["k"], d["V"]
     ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_F32), dtype=torch.uint8,
                      device=dev)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
                                       d["T"], None, workspace=ws, stream=stream),
         steps, 3, stream))
@@ -461,7 +490,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
     rows_t = d["target"].reshape(-1, V)
     gws = torch.zeros(sv.logit_gap_gate_workspace(rows_t.shape[0], V, sv.SV_F32),
                       dtype=torch.uint8, device=dev)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.logit_gap_gate(rows_t, d["tau"], d["answer_set"], workspace=gws, stream=stream),
         steps, 3, stream))
     nb = rows_t.numel() * 4
@@ -474,7 +503,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         B, k, V = head["B"], head["k"], head["V"]
         gws = torch.zeros(sv.spec_verify_greedy_workspace(B, k, V, sv.SV_BF16),
                           dtype=torch.uint8, device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: sv.spec_verify_greedy(head["target"], head["draft_tokens"], None,
                                           workspace=gws, stream=stream),
             steps, 3, stream))
@@ -491,7 +520,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         cc = torch.empty((B, k), dtype=torch.float32, device=dev)
         for mode, name, floor in ((sv.SV_CONF_TOP_PROB, "top", 0.05),
                                   (sv.SV_CONF_INV_ENTROPY, "inv_entropy", 0.2)):
-            ms = statistics.mean(time_launches(
+            ms = statistics.median(time_launches(
                 lambda: sv.draft_confidence_stop(head["draft"], head["T"], mode, floor,
                                                  out_num_draft=cnd, out_conf=cc,
                                                  workspace=cws, stream=stream),
@@ -503,7 +532,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         # conformal residual of the draft rows against the target rows at the same positions
         tgt = head["target"][:, :k].contiguous()
         rr = torch.empty((B * k,), dtype=torch.float32, device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: sv.conformal_residual(head["draft"], tgt, out_resid=rr, stream=stream),
             steps, 3, stream))
         nb = 2 * B * k * V * 2
@@ -518,7 +547,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         Q4 = torch.tensor([3.0, 2.0, 1.5, 1.0], dtype=torch.float32, device=dev)
         aws = torch.zeros(sv.conformal_admit_workspace(ns, 4, V, sv.SV_BF16), dtype=torch.uint8,
                           device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: sv.conformal_admit(z4, Q4, want_gap=False, workspace=aws, stream=stream),
             steps, 3, stream))
         nb = ns * 4 * V * 2
@@ -546,7 +575,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         for keep, tag in ((False, ""), (True, "_keep_dist")):
             table = sv.ReadyCacheTable(S, E, dev, V=V, dist_dtype=torch.bfloat16,
                                        keep_dist=keep)
-            ms = statistics.mean(time_launches(
+            ms = statistics.median(time_launches(
                 lambda: table.record(sid, n_s, ent, L, Bh, zr, out_status=st_out,
                                      workspace=rws, stream=stream), steps, 3, stream))
             nb = S * V * 2 * (2 if keep else 1)
@@ -559,7 +588,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         A = torch.arange(0, V, 3, dtype=torch.int32, device=dev)
         otok = torch.empty((R,), dtype=torch.int32, device=dev)
         orea = torch.empty((R,), dtype=torch.int32, device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: table.serve(rs, rstart, rtok, rlen, 2.0, A, out_token=otok, out_reason=orea,
                                 stream=stream), steps, 3, stream, flush))
         rows[f"ready_cache_serve_r{R}"] = dict(ms=ms, requests_per_s=R / (ms * 1e-3),
@@ -579,7 +608,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
                           device=dev)
         pts = torch.empty((T, 8), dtype=torch.float64, device=dev)
         ti = torch.empty((1,), dtype=torch.int32, device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: sv.gate_risk_coverage(gp, tk, fl, A, taus, 1.959964, 0.1, out_points=pts,
                                           out_tau_index=ti, workspace=sws, stream=stream),
             steps, 3, stream, flush if npts < (1 << 20) else None))
@@ -593,7 +622,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         rs = torch.rand((n,), generator=g, device=dev)
         qws = torch.zeros(sv.conformal_quantile_workspace(n), dtype=torch.uint8, device=dev)
         qo = torch.empty((1,), dtype=torch.float32, device=dev)
-        ms = statistics.mean(time_launches(
+        ms = statistics.median(time_launches(
             lambda: sv.conformal_quantile(rs, 0.9, out_q=qo, workspace=qws, stream=stream),
             steps, 3, stream, flush))
         rows[f"conformal_quantile_{tag}"] = dict(ms=ms, scores_per_s=n / (ms * 1e-3),
@@ -606,7 +635,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
     B, k, V = d["B"], d["k"], d["V"]
     ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
                      device=dev)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
                                       d["T"], None, workspace=ws, stream=stream),
         steps, 3, stream, flush))
@@ -616,7 +645,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
         bytes=nb)
     gws = torch.zeros(sv.spec_verify_greedy_workspace(B, k, V, sv.SV_BF16), dtype=torch.uint8,
                       device=dev)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.spec_verify_greedy(d["target"], d["draft_tokens"], None, workspace=gws,
                                       stream=stream),
         steps, 3, stream, flush))
@@ -628,7 +657,7 @@ def secondary_rows(args, dev, stream, peak, head=None):
 
     # tiny fp32 case: latency
     d = synth.workload_inputs(0, device=dev)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
                                       d["T"], None, stream=stream), steps, 3, stream, flush))
     rows["sample_b1_k4_v1000_f32_latency"] = dict(ms=ms, us=ms * 1e3)
@@ -675,13 +704,13 @@ def secondary_rows(args, dev, stream, peak, head=None):
                          out_draft=od, out_num_draft=on, stream=stream)
         sv.spec_verify_greedy(tgt, od, on, workspace=gws, stream=stream)
 
-    ms = statistics.mean(time_launches(chain, steps, 3, stream, flush))
+    ms = statistics.median(time_launches(chain, steps, 3, stream, flush))
     npos = int(nd.sum().item())
     nb = w4["history"].numel() * 4 + int((nd.clamp(min=0) + 1).sum().item()) * w4["V"] * 2
     rows["ngram_greedy_b128_l8192_v32000_bf16_l2flushed"] = dict(
         ms=ms, proposed_positions=npos, requests_with_proposal=int((nd > 0).sum().item()),
         positions_per_s=npos / (ms * 1e-3), gbs=gbs(nb, ms), bytes=nb)
-    ms = statistics.mean(time_launches(
+    ms = statistics.median(time_launches(
         lambda: sv.ngram_propose(w4["history"], w4["hist_len"], w4["n_max"], w4["n_min"],
                                  w4["k"], out_draft=od, out_num_draft=on, stream=stream),
         steps, 3, stream, flush))
@@ -698,9 +727,20 @@ def _oracle_sample_rate(target, draft, tokens, uniforms, T, threads):
     return time.perf_counter() - t0
 
 
+def _one_thread(target, draft, tokens, uniforms, T, budget_s):
+    """The oracle on one host thread, over the first requests of the sample that fit in
+    about budget_s seconds: (positions per second, requests, seconds)."""
+    k = tokens.shape[1]
+    t1 = _oracle_sample_rate(target[:1], draft[:1], tokens[:1], uniforms[:1], T, 1)
+    n1 = int(min(target.shape[0], max(1, budget_s / max(t1, 1e-6))))
+    t = _oracle_sample_rate(target[:n1], draft[:n1], tokens[:n1], uniforms[:n1], T, 1)
+    return n1 * k / t, n1, t
+
+
 def cpu_baseline(d, w, budget_s=15.0):
     """The oracle, as it stands, on the host cores, over a bounded sample of the requests
-    of the same workload (inputs copied from the device)."""
+    of the same workload (inputs copied from the device): the rate on every core, and the
+    rate of one thread on a smaller sample."""
     threads = os.cpu_count() or 1
     k = d["k"]
     # calibrate on a few requests, then size the sample for ~budget_s of CPU time
@@ -711,11 +751,15 @@ def cpu_baseline(d, w, budget_s=15.0):
     cpu_per_req = t * threads / n0
     n = int(min(d["B"], max(n0, budget_s / max(cpu_per_req, 1e-6))))
     sl = slice(0, n)
-    t = _oracle_sample_rate(d["target"][sl].cpu(), d["draft"][sl].cpu(),
-                            d["draft_tokens"][sl].cpu(), d["uniforms"][sl].cpu(), d["T"], threads)
+    tgt, dft = d["target"][sl].cpu(), d["draft"][sl].cpu()
+    tok, uni = d["draft_tokens"][sl].cpu(), d["uniforms"][sl].cpu()
+    t = _oracle_sample_rate(tgt, dft, tok, uni, d["T"], threads)
+    v1, n1, t1 = _one_thread(tgt, dft, tok, uni, d["T"], budget_s / 3)
     return {"value": n * k / t, "unit": "positions/s", "cores": threads, "kind": "oracle",
             "sample": f"first {n} of {d['B']} requests of {w.name} ({n * k} draft positions), "
-                      f"{t:.2f} s wall on {threads} threads"}
+                      f"{t:.2f} s wall on {threads} threads",
+            "one_thread": {"value": v1, "unit": "positions/s",
+                           "sample": f"first {n1} requests on 1 thread, {t1:.2f} s"}}
 
 
 def reference_arm(args, rank, world):
@@ -739,6 +783,9 @@ def reference_arm(args, rank, world):
                                  threads) for _ in range(args.steps)]
     total = sum(times)
     value = per_step * w.k * args.steps / total
+    # one thread, on the step's sample (after the timed steps)
+    v1, n1, t1 = _one_thread(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], w.T,
+                             args.cpu_seconds / 3)
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -759,7 +806,9 @@ def reference_arm(args, rank, world):
                    "global_batch": per_step, "parallelism": f"{threads} host threads"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": f"{per_step} requests per step ({per_step * w.k} positions)"},
+                         "sample": f"{per_step} requests per step ({per_step * w.k} positions)",
+                         "one_thread": {"value": v1, "unit": "positions/s",
+                                        "sample": f"{n1} requests on 1 thread, {t1:.2f} s"}},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
