@@ -74,11 +74,11 @@ struct WarpSoftmax {
   float pad;
 };
 
-// Merged softmax statistics of one row: S = sum of 2^(z*s - K) over the row, K = the
-// largest reference of its partials (an integer), and zx = the logit of the row's draft
-// token; its probability is 2^(zx*s - K) / S.
+// Merged softmax statistics of one row: S = S_hi + S_lo (a float-float pair) = sum of
+// 2^(z*s - K) over the row, K = the largest reference of its partials (an integer), and
+// zx = the logit of the row's draft token; its probability is 2^(zx*s - K) / S.
 struct RowSoftmax {
-  double S;
+  float S_hi, S_lo;
   float zx;
   float K;
   int status;  // 0 ok, 1 not a distribution, 2 draft token out of range

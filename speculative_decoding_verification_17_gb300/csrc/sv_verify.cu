@@ -27,7 +27,8 @@
 //                           2^(K - K_row), exact powers of two, in float-float; the row
 //                           publishes S, K_row and its draft token's logit z_x.
 //  request finish (the CTA that completes the request)  the accept tests u_i < p_i/q_i, as
-//                           u*S_p < 2^(y_p - y_q)*S_q with y = z_x*s - K exact in double,
+//                           u*S_p < 2^(y_p - y_q)*S_q with y = z_x*s - K (fp32 with a double
+//                           re-test near the decision boundary),
 //                           the accepted prefix a, then one draw: the residual
 //                           max(0, p_a - q_a) or the bonus p_n, each as one pass over its
 //                           row (pair) for per-chunk masses, then one chunk scanned in
@@ -148,15 +149,15 @@ __device__ __forceinline__ DF df_mul_f(DF a, float u) {
   return {h, __fsub_rn(e, __fsub_rn(h, p))};
 }
 
-// The inverse-CDF choice of a sub-range, by one full warp: over the n masses mass(f),
+// The inverse-CDF choice of a sub-range, by one full warp: over the n masses part[f],
 // f in [0, n), in vocabulary order, the first f whose running total exceeds u * W, W the
 // total. Lane l sums the block [l*m, (l+1)*m), m = ceil(n/32), in float-float; a warp scan
 // of the block sums gives each block's running total and W; the lane whose block first
 // passes the target walks it. When rounding leaves no such f, the last f of positive mass,
 // with take_last. Returns f (-1 when nothing has positive mass) and, in every lane, W and the
 // target's offset into f (target minus the running total before f).
-template <typename MF>
-__device__ int pick_flat(int n, float u, MF mass, DF& W, DF& offset, bool& take_last) {
+__device__ int pick_flat(int n, float u, const DF* part, DF& W, DF& offset, bool& take_last) {
+  auto mass = [&](int f) { return part[f]; };
   const int lane = threadIdx.x & 31;
   const int m = (n + 31) / 32;
   const int f0 = lane * m, f1 = min(f0 + m, n);
@@ -478,12 +479,42 @@ __device__ __forceinline__ WarpSoftmax ld_part(const WarpSoftmax* p) {
 }
 
 __device__ __forceinline__ RowSoftmax ld_row(const RowSoftmax* p) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
   RowSoftmax r;
-  r.S = __ldcg(&p->S);
-  r.zx = __ldcg(&p->zx);
-  r.K = __ldcg(&p->K);
+  r.S_hi = v.x;
+  r.S_lo = v.y;
+  r.zx = v.z;
+  r.K = v.w;
   r.status = __ldcg(&p->status);
   return r;
+}
+
+// The accept test of one drafted position, u < p(x)/q(x), with p(x) = 2^(yp)/Sp and
+// q(x) = 2^(yq)/Sq, y = zx*s - K. The ratio is formed in fp32: the exponent difference
+// d = yp - yq as a float-float (each product zx*s split exactly by an FMA), 2^round(d) times
+// ex2 of the remainder, times Sq/Sp. Its relative error is a few 1e-7; where u lies within
+// 4e-6 * max(1, ratio) of it (or d is out of the fast path's range), the test is redone in
+// double with the exponent exact, as u*Sp < 2^(yp - yq)*Sq (q(x) = 0 accepts, p(x) = q(x) =
+// 0 rejects). So the decision equals the exact one wherever the exact margin is above ~1e-6.
+__device__ __forceinline__ bool accept_test(float u, const RowSoftmax& t, const RowSoftmax& q,
+                                            float s) {
+  const float ph = t.zx * s, pl = fmaf(t.zx, s, -ph);
+  const float qh = q.zx * s, ql = fmaf(q.zx, s, -qh);
+  float dh, de, d2, de2;
+  two_sum(ph, -qh, dh, de);
+  two_sum(dh, q.K - t.K, d2, de2);
+  const float dl = de + de2 + (pl - ql);
+  if (fabsf(d2) <= 64.0f && fabsf(t.K) < 8.0e6f && fabsf(q.K) < 8.0e6f) {
+    const float n = rintf(d2);
+    const float e = ex2((d2 - n) + dl);
+    const float rho = scalbnf(e * (q.S_hi / t.S_hi), (int)n);
+    if (fabsf(u - rho) > 4.0e-6f * fmaxf(1.0f, rho)) return u < rho;
+  }
+  const double sd = (double)s;
+  const double yp = (double)t.zx * sd - (double)t.K;
+  const double yq = (double)q.zx * sd - (double)q.K;
+  return (double)u * ((double)t.S_hi + (double)t.S_lo) <
+         exp2(yp - yq) * ((double)q.S_hi + (double)q.S_lo);
 }
 
 enum DrawStatus { kDrawOk = 0, kDrawNoMass = 1, kDrawFailed = 2 };
@@ -501,7 +532,7 @@ struct SampleOp {
     float zx;              // the logit of the row's draft token, when prefetched
     int row_last, req_last;
     int a, err, chunk, take_last;
-    double W;
+    DF W;
     DF before;
     ScanSmem scan;
     DF cm[kSmemChunks * (2 * kWarps + 1)];  // the draw's sub-range masses, then chunk masses
@@ -654,11 +685,11 @@ struct SampleOp {
                                         Ring& ring);
   template <class VW>
   __device__ static int draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
-                             Ring& ring, int& t, double& W);
+                             Ring& ring, int& t, DF& W);
   template <class VW>
   __device__ static int draw_select(const Args& A, const VW& vw, DF* part, bool landed, float u,
-                                    Smem& sm, Ring& ring, int& t, double& W);
-  __device__ static void emit(const Args& A, int r, int a, int n, int t, double W, int st);
+                                    Smem& sm, Ring& ring, int& t, DF& W);
+  __device__ static void emit(const Args& A, int r, int a, int n, int t, DF W, int st);
   template <class F>
   __device__ static void with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
                                            F&& f);
@@ -709,9 +740,8 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
       }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Sd = df_add(Sd, df_shfl_xor(Sd, o));
-    const double S = (double)Sd.hi + (double)Sd.lo;
     if (lane == 0) {
-      int status = (!poison && K > -INFINITY && isfinite(S) && S > 0.0) ? 0 : 1;
+      int status = (!poison && K > -INFINITY && isfinite(Sd.hi) && Sd.hi > 0.0f) ? 0 : 1;
       float zx = 0.0f;
       if (i < n) {
         const int32_t xi = __ldg(A.tokens + (int64_t)r * A.k + i);
@@ -719,7 +749,8 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
         else if (status == 0) zx = g.nseg == 1 ? sm.zx : E::load1(g.row, xi);
       }
       RowSoftmax* rs = A.row + g.rid;
-      rs->S = S;
+      rs->S_hi = Sd.hi;
+      rs->S_lo = Sd.lo;
       rs->zx = zx;
       rs->K = K;
       rs->status = status;
@@ -739,7 +770,7 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
-                                  Ring& ring, int& t, double& W) {
+                                  Ring& ring, int& t, DF& W) {
   using DR = DrawRing<VW, T::kRingBytes>;
   // the masses' layouts (Smem::cm, the workspace's resid region, draw_kernel's copy) hold
   // 2 * kWarps sub-ranges per chunk: a ring whose pieces are smaller than that would overflow
@@ -757,7 +788,7 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, bool landed,
-                                         float u, Smem& sm, Ring& ring, int& t, double& W) {
+                                         float u, Smem& sm, Ring& ring, int& t, DF& W) {
   const int tid = threadIdx.x, lane = tid & 31;
   using DR = DrawRing<VW, T::kRingBytes>;
   constexpr int kSubs = DR::kPiecesPerChunk * kWarps;  // sub-ranges of a chunk
@@ -768,9 +799,9 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
   if (tid < 32) {
     DF Wd, off;
     bool tl;
-    const int f = pick_flat(A.nch * kSubs, u, [&](int i) { return part[i]; }, Wd, off, tl);
+    const int f = pick_flat(A.nch * kSubs, u, part, Wd, off, tl);
     if (lane == 0) {
-      sm.W = (double)Wd.hi + (double)Wd.lo;
+      sm.W = Wd;
       sm.chunk = f < 0 ? 0 : f;
       sm.before = off;
       sm.take_last = tl;
@@ -778,8 +809,8 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
   }
   __syncthreads();
   W = sm.W;
-  if (!landed || W != W) return kDrawFailed;
-  if (!(W > 0.0)) return kDrawNoMass;
+  if (!landed || W.hi != W.hi) return kDrawFailed;
+  if (!(W.hi > 0.0f)) return kDrawNoMass;
   const int c = sm.chunk / kSubs, q = sm.chunk - (sm.chunk / kSubs) * kSubs;
   const int64_t s0 = (int64_t)c * E::kChunk + (int64_t)(q / kWarps) * kPieceElems +
                      (int64_t)(q % kWarps) * kSubElems;
@@ -832,8 +863,8 @@ __device__ void SampleOp<ET>::with_draw_weights(const Args& A, int r, int a, int
     rs.wf.s = A.s;
     rs.wf.cp = -tp.K;
     rs.wf.cq = -dq.K;
-    rs.wf.ip = (float)(1.0 / tp.S);
-    rs.wf.iq = (float)(1.0 / dq.S);
+    rs.wf.ip = 1.0f / tp.S_hi;  // S_lo is below half an ulp of S_hi
+    rs.wf.iq = 1.0f / dq.S_hi;
     f(rs);
   } else {
     const RowSoftmax rw = ld_row(A.row + (int64_t)r * R + a);
@@ -851,7 +882,7 @@ __device__ void SampleOp<ET>::with_draw_weights(const Args& A, int r, int a, int
 // accept length and the residual mass; or, when the draw did not succeed (st), the error
 // sentinel. Every thread calls this.
 template <typename ET>
-__device__ void SampleOp<ET>::emit(const Args& A, int r, int a, int n, int t, double W, int st) {
+__device__ void SampleOp<ET>::emit(const Args& A, int r, int a, int n, int t, DF W, int st) {
   const int tid = threadIdx.x;
   if (st != kDrawOk) {  // a data error, or a copy that never landed: the error sentinel
     if (tid <= A.k) A.out_tokens[(int64_t)r * (A.k + 1) + tid] = -1;
@@ -869,7 +900,7 @@ __device__ void SampleOp<ET>::emit(const Args& A, int r, int a, int n, int t, do
   }
   if (tid == 0) {
     A.out_accept_len[r] = a;
-    if (A.out_resid) A.out_resid[r] = a < n ? (float)W : 0.0f;
+    if (A.out_resid) A.out_resid[r] = a < n ? W.hi : 0.0f;
   }
 }
 
@@ -890,16 +921,10 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       const RowSoftmax q = ld_row(A.row + (int64_t)r * R + A.k + 1 + lane);
       const float ui = __ldg(u + lane);
       bad = t.status != 0 || q.status != 0 || !(ui >= 0.0f && ui < 1.0f);
-      // p = 2^(yp)/Sp and q = 2^(yq)/Sq with y = zx*s - K, exact in double. The test
-      // u < p/q, as u*Sp < 2^(yp - yq)*Sq: one exp2 and no division (q(x) = 0 accepts,
-      // p(x) = q(x) = 0 rejects, as the quotient would).
-      const double sd = (double)A.s;
-      const double yp = (double)t.zx * sd - (double)t.K;
-      const double yq = (double)q.zx * sd - (double)q.K;
-      reject = !((double)ui * t.S < exp2(yp - yq) * q.S);
+      reject = !accept_test(ui, t, q, A.s);
       // the optional p and q outputs, in fp32
-      pt = ex2(fmaf(t.zx, A.s, -t.K)) / (float)t.S;
-      pq = ex2(fmaf(q.zx, A.s, -q.K)) / (float)q.S;
+      pt = ex2(fmaf(t.zx, A.s, -t.K)) / t.S_hi;
+      pq = ex2(fmaf(q.zx, A.s, -q.K)) / q.S_hi;
     }
     if (n_ok && lane == 0) {
       const RowSoftmax t = ld_row(A.row + (int64_t)r * R + n);
@@ -925,11 +950,11 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   // launch after this one, split over its chunks
   if (A.defer > 0 && r >= A.B - A.defer) {
     if (tid == 0) A.draw_a[r] = sm.err ? -1 : a;
-    if (sm.err) emit(A, r, a, n, -1, 0.0, kDrawFailed);
+    if (sm.err) emit(A, r, a, n, -1, DF{0.0f, 0.0f}, kDrawFailed);
     return;
   }
   int t = -1;
-  double W = 0.0;
+  DF W{0.0f, 0.0f};
   int st = kDrawFailed;
   if (!sm.err) {
     const float uk = __ldg(u + A.k);
@@ -944,7 +969,7 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     if (st == kDrawNoMass) {
       // the bonus draw from p (row n after full acceptance; row a if the residual vanished
       // through rounding)
-      double Wb;
+      DF Wb;
       with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
         st = draw(A, vw, part, uk, sm, ring, t, Wb);
       });
@@ -1002,12 +1027,12 @@ __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
   __syncthreads();
   const float uk = __ldg(A.uniforms + (int64_t)r * (A.k + 1) + A.k);
   int t = -1, st = kDrawFailed;
-  double W = 0.0;
+  DF W{0.0f, 0.0f};
   Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
     st = Op::draw_select(A, vw, sm.cm, landed, uk, sm, ring, t, W);
   });
   if (st == kDrawNoMass && a < n) {  // the residual vanished through rounding: p_a
-    double Wb;
+    DF Wb;
     Op::with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
       st = Op::draw(A, vw, sm.cm, uk, sm, ring, t, Wb);
     });
