@@ -60,6 +60,34 @@ def compare_sample(gpu: dict, orc: dict, requests) -> dict:
     return stats
 
 
+def flag_bound(orc: dict, requests) -> tuple[float, int]:
+    """The expected number of flagged requests and a cap on the count, from the 1e-6 rule.
+
+    The oracle's tie_prob[r] is the chance, over the uniforms, that request r is flagged
+    given its path (accept tests within 1e-6 of rho, or a draw target within 1e-6*W of a
+    boundary between tokens of positive weight; a token lighter than the margin is flagged
+    wherever the target falls in it, so long-tailed rows raise it). Requests draw their
+    uniforms independently, so the flagged count is a sum of independent Bernoulli(p_r)
+    terms: mean E = sum p_r, variance sum p_r(1 - p_r). The cap is E + 5 standard deviations
+    + 3 (the +3 covers tiny batches, where the normal tail bound is loose)."""
+    p = np.array([orc["tie_prob"][r] for r in requests if orc["accept_len"][r] >= 0],
+                 dtype=np.float64)
+    mean = float(p.sum())
+    sd = float(np.sqrt((p * (1.0 - p)).sum()))
+    return mean, int(np.floor(mean + 5.0 * sd + 3.0))
+
+
+def check_flags(name: str, stats: dict, orc: dict, requests) -> None:
+    """Report a sampled-verify comparison on one line (pytest -s shows it) and check the
+    flagged count against flag_bound."""
+    mean, cap = flag_bound(orc, requests)
+    print(f"PARITY {name}: requests={stats['requests']} errors={stats['errors']} "
+          f"flagged={stats['flagged']} flagged_differ={stats['flagged_differ']} "
+          f"expected_flagged={mean:.2f} cap={cap} max_p_err={stats['max_p_err']:.2e} "
+          f"max_resid_err={stats['max_resid_err']:.2e}")
+    assert stats["flagged"] <= cap, (name, stats, mean, cap)
+
+
 def compare_greedy(gpu_tokens, gpu_accept, orc) -> None:
     assert np.array_equal(gpu_accept, orc["accept_len"]), "greedy accept lengths differ"
     assert np.array_equal(gpu_tokens, orc["tokens"]), "greedy tokens differ"

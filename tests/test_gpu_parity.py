@@ -1,10 +1,12 @@
 """CUDA path vs the oracle, through the C ABI (via the thin binding), on seeded inputs.
 
-Small cases span several chunks, ragged tails, unaligned rows and ragged draft counts and
-run the oracle on every request; the five workloads run at full size in the launch
-configuration the benchmark times, with the oracle on every request where it finishes in
-seconds and on a seeded sample of requests for the largest one.
+Small cases span several chunks, ragged tails, unaligned rows and ragged draft counts; the
+five workloads run at full size in the launch configuration the benchmark times. The oracle
+runs on every request of every case. Near ties (the 1e-6 rule) are counted, printed on a
+PARITY line and bounded by the count the rule itself predicts (parity.flag_bound).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -12,13 +14,13 @@ import torch
 import oracle
 import speculative_decoding_verification_17_gb300 as sv
 import synth
-from parity import compare_gate, compare_greedy, compare_sample
+from parity import check_flags, compare_gate, compare_greedy, compare_sample
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def run_sample(d, requests=None, threads=16):
+def run_sample(d, requests=None, threads=os.cpu_count() or 16):
     tok, acc, p, q, W = sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"],
                                               d["uniforms"], d["T"], d["num_draft"])
     torch.cuda.synchronize()
@@ -55,9 +57,8 @@ def test_sample_small(case):
     B, k, V, dt, T, ragged, ts, dn, ds = case
     d = synth.sample_inputs(B, k, V, dt, T, device=DEV, seed=V + B, ragged=ragged,
                             target_std=ts, draft_noise=dn, draft_scale=ds)
-    stats, _, _ = run_sample(d)
-    print(f"B={B} k={k} V={V} {dt} T={T}: {stats}")
-    assert stats["flagged"] <= max(2, B // 4), stats
+    stats, _, orc = run_sample(d)
+    check_flags(f"B={B} k={k} V={V} {dt} T={T}", stats, orc, range(B))
 
 
 @pytest.mark.parametrize("B,k,V", [(32, 6, 20000), (6, 3, 151936)])
@@ -132,12 +133,11 @@ def test_sample_deferred_draws(off):
             view = flat[1:].view(d[key].shape)
             view.copy_(d[key])
             d[key] = view
-    stats, gpu, _ = run_sample(d)
-    print(f"deferred draws (off={off}): {stats}")
+    stats, gpu, orc = run_sample(d)
+    check_flags(f"deferred draws off={off}", stats, orc, range(B))
     assert gpu["accept_len"][150] == -1 and gpu["accept_len"][155] == -1
     nd = d["num_draft"].cpu().numpy()
     assert (gpu["accept_len"][140:145] == nd[140:145]).all()
-    assert stats["flagged"] <= 8, stats
 
 
 def test_sample_and_greedy_in_a_cuda_graph():
@@ -197,19 +197,18 @@ def test_sample_and_greedy_in_a_cuda_graph():
 @pytest.mark.parametrize("w", [0, 1, 2])
 def test_sample_workloads_full(w):
     d = synth.workload_inputs(w, device=DEV)
-    stats, gpu, _ = run_sample(d)
-    print(f"workload {w}: {stats}")
+    stats, gpu, orc = run_sample(d)
     # near ties are a property of the data (long-tailed rows put many draws within 1e-6 of
-    # a CDF boundary); they are reported, and checked against the oracle's tie window
-    assert stats["flagged"] <= max(2, d["B"] // 6), stats
+    # a CDF boundary); they are counted against the rule's own expectation, reported, and
+    # checked against the oracle's tie window
+    check_flags(f"workload {w}", stats, orc, range(d["B"]))
 
 
-def test_sample_workload3_full_sampled_requests():
+def test_sample_workload3_full_every_request():
     d = synth.workload_inputs(3, device=DEV)
-    reqs = sorted(np.random.default_rng(3).choice(d["B"], 96, replace=False).tolist())
-    stats, gpu, _ = run_sample(d, requests=reqs)
-    print(f"workload 3 (96 of {d['B']} requests): {stats}")
-    assert stats["flagged"] <= 16, stats
+    stats, gpu, orc = run_sample(d)
+    check_flags("workload 3", stats, orc, range(d["B"]))
+    assert stats["requests"] == d["B"]
     # every request: a well-formed result (prefix of drafts, one drawn token, -1 padding)
     a = gpu["accept_len"]
     assert ((a >= 0) & (a <= d["k"])).all()
