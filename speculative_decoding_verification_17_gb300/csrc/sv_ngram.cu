@@ -14,9 +14,11 @@
 // request; a single packed (l_e, -e) maximum picks the winner.
 //
 // The history streams through shared memory in tiles of kTile end positions, each with the
-// n_max - 1 tokens before it: every thread issues its asynchronous 4-byte copies of a tile
-// at once (cp.async, no register round trip), so a tile costs one memory latency, and the
-// match counts then read shared memory only.
+// n_max - 1 tokens before it: every thread issues its asynchronous copies of a tile at once
+// (cp.async, no register round trip), so a tile costs one memory latency, and the match
+// counts then read shared memory only. The first tile always starts at token 0, so its
+// copies (16 bytes each where the row allows) are issued before the history length is
+// known, and the two loads overlap; the suffix is read from that tile when it holds it.
 #include <cstdint>
 
 #include "specverify.h"
@@ -33,6 +35,10 @@ __device__ __forceinline__ void cp_async4(int32_t* dst, const int32_t* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async16(int32_t* dst, const int32_t* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -42,21 +48,35 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(
     int n_max, int n_min, int k, int32_t* __restrict__ out_draft,
     int32_t* __restrict__ out_num) {
   __shared__ int32_t suffix[kMaxPhrase];
-  __shared__ int32_t tile[kTile + kMaxPhrase];
+  __shared__ __align__(16) int32_t tile[kTile + kMaxPhrase];
   __shared__ unsigned int s_best[kNgramThreads / 32];
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int32_t* h = history + (int64_t)r * L_max;
+  // the first tile, tokens [0, n0), requested before the length arrives
+  const int n0 = L_max < kTile + kMaxPhrase ? L_max : kTile + kMaxPhrase;
+  if ((reinterpret_cast<uintptr_t>(h) & 15) == 0) {
+    const int n16 = n0 / 4;
+    for (int i = tid; i < n16; i += kNgramThreads) cp_async16(tile + 4 * i, h + 4 * i);
+    for (int i = 4 * n16 + tid; i < n0; i += kNgramThreads) cp_async4(tile + i, h + i);
+  } else {
+    for (int i = tid; i < n0; i += kNgramThreads) cp_async4(tile + i, h + i);
+  }
   const int L = __ldg(hist_len + r);
   int32_t* d = out_draft + (int64_t)r * k;
   if (L < 0 || L > L_max) {
+    cp_async_wait_all();  // no copy outlives the CTA
     for (int i = tid; i < k; i += kNgramThreads) d[i] = -1;
     if (tid == 0) out_num[r] = -1;
     return;
   }
-  const int32_t* h = history + (int64_t)r * L_max;
   const int ns = n_max < L ? n_max : L;
-  // suffix[t] = h[L-1-t], copied along with the first tile
-  if (tid < ns) cp_async4(suffix + tid, h + L - 1 - tid);
+  // suffix[t] = h[L-1-t]: from the first tile when it holds the last token
+  const bool suffix_in_tile = L <= n0;
+  if (!suffix_in_tile && tid < ns) cp_async4(suffix + tid, h + L - 1 - tid);
+  cp_async_wait_all();
+  __syncthreads();
+  if (suffix_in_tile && tid < ns) suffix[tid] = tile[L - 1 - tid];
 
   // key = (l_e << 24) | (2^24 - 1 - e): the larger match first, then the smaller e
   unsigned int best = 0;
@@ -65,10 +85,12 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(
     // end positions [t0, t1) read tokens [lo, t1): lo <= e - (n_max - 1) for every e >= t0
     t1 = t0 + kTile < L - 1 ? t0 + kTile : L - 1;
     lo = t0 - (n_max - 1) > 0 ? t0 - (n_max - 1) : 0;
-    __syncthreads();  // the previous tile has been read
-    for (int i = tid; i < t1 - lo; i += kNgramThreads) cp_async4(tile + i, h + lo + i);
-    cp_async_wait_all();
-    __syncthreads();
+    __syncthreads();  // the previous tile has been read; the suffix is in place
+    if (lo > 0) {  // later tiles (the first one, from token 0, is in place)
+      for (int i = tid; i < t1 - lo; i += kNgramThreads) cp_async4(tile + i, h + lo + i);
+      cp_async_wait_all();
+      __syncthreads();
+    }
     for (int e = t0 + tid; e < t1; e += kNgramThreads) {
       int m = 0;
       const int cap = n_max < e + 1 ? n_max : e + 1;

@@ -1077,11 +1077,14 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
   idx = (int)best;
 }
 
-template <typename ET>
+// TileT: half-chunk stages, two deep, 4 CTAs per SM for grids of many waves (a light scan);
+// four deep, 3 CTAs per SM for grids of up to two waves, where each CTA's first bytes in
+// flight set the time (a 64 KiB row is then requested at once).
+template <typename ET, class TileT = SV_TILE(4, 2, 4)>
 struct GreedyOp {
   using Args = GreedyArgs;
   using E = ET;
-  using T = SV_TILE(4, 2, 4);  // a light scan: half-chunk stages, 4 CTAs per SM
+  using T = TileT;
   static constexpr uint32_t kPad = E::kNaNBits;  // NaN padding is never chosen
   struct Smem {
     float2 wpart[kWarps];  // the warp partials of this segment
@@ -1479,6 +1482,11 @@ extern "C" sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtyp
   const sv_status cleared = launch_clear(ws + L.ctl, L.total - L.ctl, st);
   if (cleared != SV_OK) return cleared;
   CallCtl* ctl = reinterpret_cast<CallCtl*>(ws + L.ctl);
+  using Deep = SV_TILE(4, 4, 3);
+  if (units <= 2 * (int64_t)device_sm_count() * Deep::kCtasPerSm) {  // up to two waves
+    if (dtype == SV_F32) return launch_segments<GreedyOp<F32, Deep>>(A, units, ctl, st);
+    return launch_segments<GreedyOp<BF16, Deep>>(A, units, ctl, st);
+  }
   if (dtype == SV_F32) return launch_segments<GreedyOp<F32>>(A, units, ctl, st);
   return launch_segments<GreedyOp<BF16>>(A, units, ctl, st);
 }
