@@ -380,6 +380,7 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
     if rank == 0:
         ename = "F32" if w.dtype == "f32" else "BF16"
         clocks = clk.summary(*clk.window)
+        med = getattr(args, "median_ms", None)
         line = {
             "metric": METRIC,
             "value": value,
@@ -388,22 +389,20 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": total_ms / args.steps,
+            "ms_per_step_median": med,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": w.dtype,
-            "data": "synthetic (seeded; shapes and value distributions of the workload)",
+            "data": "synthetic (seeded)",
             "config": {
-                "workload": f"sampled verify {w.name}: B={B}, k={k}, V={V}, {w.dtype} logits, "
-                            f"T={w.T}, {TIMED_WORKLOADS[w.index]}",
+                "workload": f"sampled verify B={B} k={k} V={V} {w.dtype} T={w.T}: "
+                            f"{TIMED_WORKLOADS[w.index]}",
                 "global_batch": B * world,
                 "draft_positions_per_step": n_total * world,
-                "logit_bytes_per_step": abytes,
-                "l2": f"inputs {abytes / 1e9:.2f} GB per step vs the 129 MB L2: no flush",
+                "l2": f"inputs {abytes / 1e9:.2f} GB > 129 MB L2: no flush",
                 "parallelism": f"request-sharded replicas x{world}" if world > 1 else "single GPU",
             },
-            "ms_per_step_median": getattr(args, "median_ms", None),
-            "logit_gbs": achieved,
             "mean_accept_len": acc,
             "roofline": {
                 "bound": "hbm",
@@ -413,26 +412,36 @@ def finish_line(args, rank, world, dev, dist, d, w, stream, total_ms, mean_ms, a
                 "peak": peak,
                 "unit": "GB/s",
                 "frac": achieved / peak,
-                "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                               if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "peak_source": "measured hbm_gbs" if peak_kind == "measured" else "fallback",
                 "traffic": profiled_traffic("segment_kernel_sample", f"b{B}_k{k}_v{V}_{w.dtype}"),
-                "algorithmic_bytes_per_launch": abytes,
+                "bytes_per_launch": abytes,
                 "launch_ms": mean_ms,
-                "launch_ms_median": getattr(args, "median_ms", None),
             },
             "e2e": e2e,
             "gpu_launches": args.steps * args.launches_per_step,
             "clocks": clocks,
-            "wall_s_timed": wall,
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
         if rows:
             line["configs_2_3"] = target_configs(rows, line)
+        line = _rounded(line, 4)
         print(json.dumps(line))
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def _rounded(x, digits: int = 5):
+    """x with every float rounded to `digits` significant digits (the headline line stays
+    short)."""
+    if isinstance(x, float):
+        return float(f"{x:.{digits}g}")
+    if isinstance(x, dict):
+        return {k: _rounded(v, digits) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_rounded(v, digits) for v in x]
+    return x
 
 
 def target_configs(rows, line):
@@ -448,13 +457,13 @@ def target_configs(rows, line):
             ("gate_n1280_v151936_f32", "gate_n1280_v151936_f32", "segment_kernel", "sv_gate.cu")):
         r = rows.get(src)
         if r:
-            out[key] = {"ms": r["ms"], "gbs": r["gbs"], "frac": r["frac"], "bytes": r["bytes"],
+            out[key] = {"ms": r["ms"], "gbs": r["gbs"], "frac": r["frac"],
                         "traffic": profiled_traffic(kern, key, unit)}
     rf = line["roofline"]
-    if line["config"]["workload"].startswith("sampled verify b512_k8_v128256_bf16"):
+    if line["config"]["workload"].startswith("sampled verify B=512 k=8 V=128256 bf16"):
         out["sample_b512_k8_v128256_bf16"] = {
-            "ms": rf["launch_ms_median"], "gbs": rf["achieved"], "frac": rf["frac"],
-            "bytes": rf["algorithmic_bytes_per_launch"], "traffic": rf["traffic"]}
+            "ms": line["ms_per_step_median"], "gbs": rf["achieved"], "frac": rf["frac"],
+            "traffic": rf["traffic"]}
     return out
 
 
@@ -756,8 +765,8 @@ def cpu_baseline(d, w, budget_s=15.0):
     t = _oracle_sample_rate(tgt, dft, tok, uni, d["T"], threads)
     v1, n1, t1 = _one_thread(tgt, dft, tok, uni, d["T"], budget_s / 3)
     return {"value": n * k / t, "unit": "positions/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {d['B']} requests of {w.name} ({n * k} draft positions), "
-                      f"{t:.2f} s wall on {threads} threads",
+            "sample": f"first {n} of {d['B']} requests ({n * k} positions), {t:.2f} s on "
+                      f"{threads} threads",
             "one_thread": {"value": v1, "unit": "positions/s",
                            "sample": f"first {n1} requests on 1 thread, {t1:.2f} s"}}
 
