@@ -108,7 +108,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 10):
+    def __init__(self, gpu_index: int, period_ms: int = 2):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
@@ -883,6 +883,31 @@ def kernels_once():
     print("kernels-once ok")
 
 
+def small_once():
+    """Three calls each of the two small sampled-verify workloads (B=1, k=4, V=1000 fp32, then
+    B=64, k=5, V=32000 bf16), each after an L2 flush, and nothing timed: the command line for
+    an ncu capture of the small batches' kernels."""
+    import torch
+
+    import speculative_decoding_verification_17_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda")
+    flush = make_flush(dev)
+    for wi in (0, 1):
+        d = synth.workload_inputs(wi, device=dev)
+        B, k, V = d["B"], d["k"], d["V"]
+        code = sv.SV_F32 if d["dtype"] == "f32" else sv.SV_BF16
+        ws = torch.zeros(sv.spec_verify_sample_workspace(B, k, V, code), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            flush()
+            sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                  d["T"], None, workspace=ws)
+    torch.cuda.synchronize()
+    print("small-once ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -899,9 +924,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--kernels-once", action="store_true",
                     help="one untimed launch of each secondary call (for an ncu capture)")
+    ap.add_argument("--small-once", action="store_true",
+                    help="three untimed calls of each small sampled workload (for an ncu capture)")
     args = ap.parse_args()
     if args.kernels_once:
         kernels_once()
+        return
+    if args.small_once:
+        small_once()
         return
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     rank = int(os.environ.get("RANK", "0"))
