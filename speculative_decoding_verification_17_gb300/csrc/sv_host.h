@@ -119,7 +119,7 @@ struct WarpTop2 {
 
 // Workspace regions. Everything from `ctl` to `total` is cleared at the start of a call.
 struct SampleLayout {
-  size_t part, row, resid, draw_a, ctl, row_cnt, req_cnt, draw_cnt, total;
+  size_t part, row, resid, bmass, draw_a, ctl, row_cnt, req_cnt, draw_cnt, total;
 };
 inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   const size_t R = 2 * static_cast<size_t>(k) + 1;
@@ -130,6 +130,7 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
   L.resid = o;   o = round_up(o + B * nch * (2 * kWarpsPerChunk + 1) * sizeof(double), 256);
+  L.bmass = o;   o = round_up(o + B * nch * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.draw_a = o;  o = round_up(o + B * sizeof(int), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);
   L.row_cnt = o; o = round_up(o + B * R * sizeof(unsigned int), 256);

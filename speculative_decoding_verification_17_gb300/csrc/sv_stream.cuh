@@ -92,6 +92,7 @@ struct Seg {
   int seg;      // index of this segment in the row
   int nseg;     // segments of this row
   bool keep;    // likely to be read again soon (a hint for the L2)
+  bool sums = false;  // the operation keeps per-stage sums of this row (its own use)
 };
 
 // The CTA's shared-memory ring as the finishing code may reuse it once pass 1 is done:

@@ -38,12 +38,16 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "specverify.h"
 #include "sv_device.cuh"
 #include "sv_host.h"
 #include "sv_stream.cuh"
 
+#ifndef SV_KEEP_BONUS_MASSES
+#define SV_KEEP_BONUS_MASSES 1  // pass 1 keeps row n's sub-range masses for the bonus draw
+#endif
 #ifndef SV_RESID_RING
 #define SV_RESID_RING 1  // residual pass through the TMA ring (0: register loads)
 #endif
@@ -228,6 +232,8 @@ struct SampleArgs {
   WarpSoftmax* part;  // [B * (2k+1)][nseg][kWarps]
   RowSoftmax* row;
   DF* resid;          // [B][nch * (2 * kWarps + 1)] sub-range then chunk masses of a draw
+  WarpSoftmax* bmass;  // [B][nch * kWarps] pass 1's masses of every 4 KiB sub-range of each
+                       // request's target row n, (K, hi, lo): its bonus draw's masses
   unsigned int* row_cnt;
   unsigned int* req_cnt;
   int keep_pos;             // rows of draft positions < keep_pos are copied with evict_last
@@ -527,6 +533,13 @@ struct SampleOp {
   static constexpr uint32_t kPad = E::kNegInfBits;
   static constexpr int kSmemChunks = 32;  // rows of up to this many chunks keep the
                                           // draw's chunk masses in shared memory
+  // For fp32 rows pass 1 keeps the masses of row n's sub-ranges for the bonus draw: a ring
+  // stage is one chunk, and warp w's eighth of it one sub-range of that draw. bf16 rows
+  // re-read row n instead: their pass 1 issues twice the logits per byte, and there the
+  // per-stage reduction cost more than the passes it saves. A ring of smaller stages, in a
+  // build that forces one, keeps none.
+  static constexpr bool kStageSums = SV_KEEP_BONUS_MASSES && std::is_same<ET, F32>::value &&
+                                     T::kStageBytes == kChunkBytes;
   struct Smem {
     float4 wpart[kWarps];  // the warp partials of this segment
     float zx;              // the logit of the row's draft token, when prefetched
@@ -569,6 +582,7 @@ struct SampleOp {
     g.slot = slot;
     g.seg = seg;
     g.keep = i < A.keep_pos;  // the early positions hold most rejections
+    g.sums = kStageSums && is_target && i == n;  // row n: keep its sub-range masses
     g.c0 = seg * kSegChunks;
     g.c1 = min(g.c0 + kSegChunks, A.nch);
     g.nseg = A.nseg;
@@ -606,12 +620,13 @@ struct SampleOp {
   // K = ceil(m*s), the sum of 2^(z*s - K) (logits two at a time: packed fp32x2 FMA and adds,
   // two SFU exp2 per pair, a pairwise tree), then folded into the lane's running pair after
   // rescaling the side with the smaller reference by an exact power of two.
-  __device__ static __forceinline__ void warp_slice(const Args& A, const Seg&, int64_t,
+  __device__ static __forceinline__ void warp_slice(const Args& A, const Seg& g, int64_t j0,
                                                     const uint4 (&v)[T::kStageVec],
                                                     bool poison, Acc& acc) {
     constexpr int kStageVec = T::kStageVec;
     const float m = E::max_lane(v);
     acc.bad |= poison;
+    float Ks = -INFINITY, ssum = 0.0f;  // the lane's stage sum, in units of 2^Ks
     if (m > -INFINITY && m < INFINITY) {
       const float s = A.s;
       const float K = ceilf(m * s);
@@ -637,7 +652,9 @@ struct SampleOp {
         for (int l = 0; l < q; ++l) part[l] = __fadd2_rn(part[l], part[l + q]);
       const float Kn = fmaxf(K, acc.K);
       const float sa = pow2_nonpos(acc.K - Kn);
-      const float sum = (part[0].x + part[0].y) * pow2_nonpos(K - Kn);
+      Ks = K;
+      ssum = part[0].x + part[0].y;
+      const float sum = ssum * pow2_nonpos(K - Kn);
       float hi, e;
       two_sum(acc.hi * sa, sum, hi, e);
       acc.lo = fmaf(acc.lo, sa, e);
@@ -651,6 +668,22 @@ struct SampleOp {
       acc.bad |= nan;
     } else {
       acc.bad = true;  // +inf, or nothing but NaN
+    }
+    if (kStageSums && g.sums) stage_mass(A, g, j0, Ks, ssum);
+  }
+
+  // Row n's stage (one chunk): the warp's sub-range mass, every lane's stage sum scaled to
+  // the warp's largest reference (exact), with a compensated warp sum; lane 0 stores it. A
+  // row with NaN or +inf logits never draws, so what its lanes give is never used.
+  __device__ static __forceinline__ void stage_mass(const Args& A, const Seg& g, int64_t j0,
+                                                    float Ks, float ssum) {
+    const float Kw = warp_max_f(Ks);
+    float hi = Ks > -INFINITY ? ssum * pow2_nonpos(Ks - Kw) : 0.0f, lo = 0.0f;
+    warp_sum_compensated(hi, lo);
+    if ((threadIdx.x & 31) == 0) {
+      const int64_t c = j0 / E::kChunk;
+      *reinterpret_cast<float4*>(A.bmass + ((int64_t)g.r * A.nch + c) * kWarps +
+                                 (threadIdx.x >> 5)) = make_float4(Kw, hi, lo, 0.0f);
     }
   }
 
@@ -685,11 +718,22 @@ struct SampleOp {
                                         Ring& ring);
   template <class VW>
   __device__ static int draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
-                             Ring& ring, int& t, DF& W);
+                             Ring& ring, int& t, DF& W, bool kept = false);
   template <class VW>
   __device__ static int draw_select(const Args& A, const VW& vw, DF* part, bool landed, float u,
                                     Smem& sm, Ring& ring, int& t, DF& W);
   __device__ static void emit(const Args& A, int r, int a, int n, int t, DF W, int st);
+  // Row n's sub-range masses as pass 1 kept them, chunks [c0, c1), into part[c * kWarps + w]
+  // in units of 2^K (K: row n's reference; exact power-of-two scaling). Every thread calls
+  // this.
+  __device__ static void kept_masses(const Args& A, int r, float K, int c0, int c1, DF* part) {
+    const float4* src = reinterpret_cast<const float4*>(A.bmass + (int64_t)r * A.nch * kWarps);
+    for (int i = c0 * kWarps + threadIdx.x; i < c1 * kWarps; i += kThreads) {
+      const float4 m = __ldcg(src + i);
+      const float sc = m.x > -INFINITY ? pow2_nonpos(m.x - K) : 0.0f;
+      part[i] = DF{m.y * sc, m.z * sc};
+    }
+  }
   template <class F>
   __device__ static void with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
                                            F&& f);
@@ -763,21 +807,22 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   finish_request(A, r, n, n_ok, sm, ring);
 }
 
-// One inverse-CDF draw with the weights vw: per-chunk masses, their total W, the chunk in
-// which u*W falls (one warp scans the chunk masses), then that chunk scanned in vocabulary
-// order, from the ring when the rows are aligned (the chunk of row i staged into stage i by
-// one bulk copy each). Every thread calls this. Returns a DrawStatus; t is the drawn token.
+// One inverse-CDF draw with the weights vw: per-chunk masses (already in part when kept),
+// their total W, the chunk in which u*W falls (one warp scans the chunk masses), then that
+// chunk scanned in vocabulary order, from the ring when the rows are aligned (the chunk of
+// row i staged into stage i by one bulk copy each). Every thread calls this. Returns a
+// DrawStatus; t is the drawn token.
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
-                                  Ring& ring, int& t, DF& W) {
+                                  Ring& ring, int& t, DF& W, bool kept) {
   using DR = DrawRing<VW, T::kRingBytes>;
   // the masses' layouts (Smem::cm, the workspace's resid region, draw_kernel's copy) hold
   // 2 * kWarps sub-ranges per chunk: a ring whose pieces are smaller than that would overflow
   // them, so such a shape does not build
   static_assert(DR::kPiecesPerChunk * kWarps <= 2 * kWarps,
                 "the draw's pieces give more sub-ranges per chunk than the masses' layout holds");
-  const bool landed = chunk_masses<E, T::kRingBytes>(0, A.nch, A.V, vw, part, ring);
+  const bool landed = kept || chunk_masses<E, T::kRingBytes>(0, A.nch, A.V, vw, part, ring);
   __syncthreads();
   return draw_select(A, vw, part, landed, u, sm, ring, t, W);
 }
@@ -967,11 +1012,13 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
         st = draw(A, vw, part, uk, sm, ring, t, W);
       });
     if (st == kDrawNoMass) {
-      // the bonus draw from p (row n after full acceptance; row a if the residual vanished
-      // through rounding)
+      // the bonus draw from p (row n after full acceptance, from the masses pass 1 kept; row
+      // a if the residual vanished through rounding, with a pass of its own)
       DF Wb;
+      const bool kept = kStageSums && a == n;
+      if (kept) kept_masses(A, r, ld_row(A.row + (int64_t)r * R + n).K, 0, A.nch, part);
       with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
-        st = draw(A, vw, part, uk, sm, ring, t, Wb);
+        st = draw(A, vw, part, uk, sm, ring, t, Wb, kept);
       });
       if (st == kDrawNoMass) st = kDrawFailed;
     }
@@ -1013,9 +1060,13 @@ __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
   Ring ring{ring_buf, full, released, 0u, ctl, A.aligned};
   DF* gpart = A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
   bool landed = true;
-  Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
-    landed = chunk_masses<E, Op::T::kRingBytes>(c, c + 1, A.V, vw, gpart, ring);
-  });
+  if (Op::kStageSums && a == n) {  // the bonus draw: row n's masses are pass 1's
+    Op::kept_masses(A, r, ld_row(A.row + (int64_t)r * (2 * A.k + 1) + n).K, c, c + 1, gpart);
+  } else {
+    Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
+      landed = chunk_masses<E, Op::T::kRingBytes>(c, c + 1, A.V, vw, gpart, ring);
+    });
+  }
   __syncthreads();  // every warp's masses are stored
   if (tid == 0) sm.req_last = arrive_last(A.draw_cnt + r, (unsigned)A.nch);
   __syncthreads();
@@ -1393,6 +1444,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.part = reinterpret_cast<WarpSoftmax*>(ws + L.part);
   A.row = reinterpret_cast<RowSoftmax*>(ws + L.row);
   A.resid = reinterpret_cast<DF*>(ws + L.resid);
+  A.bmass = reinterpret_cast<WarpSoftmax*>(ws + L.bmass);
   A.row_cnt = reinterpret_cast<unsigned int*>(ws + L.row_cnt);
   A.req_cnt = reinterpret_cast<unsigned int*>(ws + L.req_cnt);
   A.draw_a = reinterpret_cast<int*>(ws + L.draw_a);

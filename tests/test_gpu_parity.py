@@ -49,6 +49,8 @@ SMALL = [
     (5, 3, 777, "bf16", 50.0, True, 2.0, 1.0, 1.0),        # very high temperature
     (6, 3, 151936, "bf16", 0.8, True, 2.0, 1.0, 1.0),      # 10 chunks: two segments per row
     (4, 2, 200003, "bf16", 1.0, False, 2.0, 0.7, 1.0),     # two segments, rows not aligned
+    (3, 2, 600000, "bf16", 1.0, True, 2.0, 1.0, 1.0),      # 37 chunks: the draw's masses in
+    (2, 3, 300001, "f32", 0.7, False, 2.0, 0.8, 1.0),      # the workspace (aligned / not)
 ]
 
 
@@ -61,9 +63,9 @@ def test_sample_small(case):
     check_flags(f"B={B} k={k} V={V} {dt} T={T}", stats, orc, range(B))
 
 
-@pytest.mark.parametrize("B,k,V", [(32, 6, 20000), (6, 3, 151936)])
+@pytest.mark.parametrize("B,k,V", [(32, 6, 20000), (6, 3, 151936), (3, 2, 600000)])
 def test_sample_draft_equals_target_accepts_all(B, k, V):
-    # every draft accepted: the bonus draw from row k (one and two segments per row)
+    # every draft accepted: the bonus draw from row k (one, two and five segments per row)
     d = synth.sample_inputs(B, k, V, "bf16", 0.9, device=DEV, seed=3)
     d["draft"] = d["target"][:, :k].contiguous()
     g = torch.Generator(device=DEV).manual_seed(4)
