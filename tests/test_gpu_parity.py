@@ -63,10 +63,13 @@ def test_sample_small(case):
     check_flags(f"B={B} k={k} V={V} {dt} T={T}", stats, orc, range(B))
 
 
-@pytest.mark.parametrize("B,k,V", [(32, 6, 20000), (6, 3, 151936), (3, 2, 600000)])
-def test_sample_draft_equals_target_accepts_all(B, k, V):
-    # every draft accepted: the bonus draw from row k (one, two and five segments per row)
-    d = synth.sample_inputs(B, k, V, "bf16", 0.9, device=DEV, seed=3)
+@pytest.mark.parametrize("B,k,V,dt", [(32, 6, 20000, "bf16"), (6, 3, 151936, "bf16"),
+                                      (3, 2, 600000, "bf16"), (32, 6, 20000, "f32"),
+                                      (6, 3, 151936, "f32"), (3, 2, 300001, "f32")])
+def test_sample_draft_equals_target_accepts_all(B, k, V, dt):
+    # every draft accepted: the bonus draw from row k (one to five segments per row; for fp32
+    # from the sub-range masses pass 1 kept, rows aligned and not)
+    d = synth.sample_inputs(B, k, V, dt, 0.9, device=DEV, seed=3)
     d["draft"] = d["target"][:, :k].contiguous()
     g = torch.Generator(device=DEV).manual_seed(4)
     zq = d["draft"].float() / 0.9
