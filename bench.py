@@ -825,8 +825,8 @@ def reference_arm(args, rank, world):
 
 
 def kernels_once():
-    """Two rounds of one launch of each secondary call, on workloads past L2, and nothing
-    timed: the command line for an ncu capture of those kernels. Round order: logit_gap_gate
+    """Two passes of one launch of each secondary call, on workloads past L2, and nothing
+    timed: the command line for an ncu capture of those kernels. Order in each pass: logit_gap_gate
     (1280 fp32 rows of V=151936), spec_verify_greedy, draft_confidence_stop (top probability,
     then inverse entropy) and conformal_admit (K=4) on the B=256 k=8 V=128256 bf16 batch,
     conformal_residual (its draft rows against target rows 0..k-1), gate_risk_coverage (16M
