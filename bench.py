@@ -56,10 +56,37 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments and blank lines removed (string and character
+    literals kept), so that a digest of it changes with the code and not with the
+    comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_digest(unit: str = "sv_verify.cu") -> str:
-    """sha256 prefix of what the profiled kernel is built from: its translation unit, every
-    header it includes from the package or `include/` (recursively), and the statements of
-    the build script that set the compiler flags (ARCH, NVCC_FLAGS)."""
+    """sha256 prefix of what the profiled kernel is built from: the code (comments removed)
+    of its translation unit and of every header it includes from the package or `include/`
+    (recursively), and the statements of the build script that set the compiler flags (ARCH,
+    NVCC_FLAGS)."""
     pkg = os.path.join(ROOT, "speculative_decoding_verification_17_gb300")
     dirs = [os.path.join(pkg, "csrc"), os.path.join(ROOT, "include")]
     seen, todo = [], [unit]
@@ -76,11 +103,11 @@ def source_digest(unit: str = "sv_verify.cu") -> str:
     h = hashlib.sha256()
     for name in sorted(seen):
         path = next(os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name)))
-        with open(path, "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     with open(os.path.join(pkg, "_native.py")) as f:
         build = f.read()
-    flags = re.findall(r"^(?:ARCH|NVCC_FLAGS) = .*?\n(?=\S|\n)", build, re.M | re.S)
+    flags = re.findall(r"^(?:ARCH|NVCC_FLAGS) = .*?\n(?=\S|\n|\Z)", build, re.M | re.S)
     h.update(b"_native.py\0" + "".join(flags).encode())
     return h.hexdigest()[:16]
 

@@ -12,27 +12,29 @@
 //
 // One kernel launch per call (after a small kernel that clears the call's counters), plus, for
 // rows of at least 8 chunks, a second one (draw_kernel) for the draws of the batch's last
-// requests, split over their chunks. Unit = (request
-// r, row slot, segment of up to kSegChunks 32 KiB chunks), one CTA each (sv_stream.cuh); a
-// request has 2k+1 row slots in the sampled verify (target rows 0..k, then draft rows
-// 0..k-1) and k+1 in the greedy verify. Units of rows a request does not need (past its n_r)
-// exit at once.
+// requests, split over their chunks. Unit = (request r, row slot, segment of up to
+// kSegChunks 32 KiB chunks), one CTA each (sv_stream.cuh); a request has 2k+1 row slots in
+// the sampled verify (target rows 0..k, then draft rows 0..k-1) and k+1 in the greedy
+// verify. Units of rows a request does not need (past its n_r) exit at once.
 //
 //  pass 1 (each lane, over its share of the segment)  per ring stage the lane maximum m, the
 //                           integer-valued reference K = ceil(m*s) with s = log2(e)/T in
 //                           fp32 and the sum of 2^(z*s - K) in fp32, folded into a running
 //                           compensated pair; per segment one warp reduction to a partial
-//                           (K, hi, lo); in the greedy verify the running argmax.
+//                           (K, hi, lo); for fp32 rows, row n also keeps each stage's warp
+//                           sums (its bonus draw's sub-range masses); in the greedy verify the
+//                           running argmax.
 //  row finish (the CTA that completes the row)  K_row = max K; S = sum of partial sums times
 //                           2^(K - K_row), exact powers of two, in float-float; the row
 //                           publishes S, K_row and its draft token's logit z_x.
-//  request finish (the CTA that completes the request)  the accept tests u_i < p_i/q_i, as
-//                           u*S_p < 2^(y_p - y_q)*S_q with y = z_x*s - K (fp32 with a double
-//                           re-test near the decision boundary),
-//                           the accepted prefix a, then one draw: the residual
-//                           max(0, p_a - q_a) or the bonus p_n, each as one pass over its
-//                           row (pair) for per-chunk masses, then one chunk scanned in
-//                           vocabulary order (float-float sums throughout).
+//  request finish (the CTA that completes the request)  the accept tests u_i < p_i/q_i with
+//                           p = 2^y/S, y = z_x*s - K (an fp32 ratio, re-tested exactly in
+//                           double near the decision boundary), the accepted prefix a, then
+//                           one draw: the residual max(0, p_a - q_a) or the bonus p_n, as the
+//                           masses of every 4 KiB-or-smaller sub-range (one pass over the
+//                           pair or row; for an fp32 bonus, pass 1's), the sub-range where u*W
+//                           falls (one warp), and that sub-range scanned in vocabulary order
+//                           (float-float sums throughout).
 #include <algorithm>
 #include <atomic>
 #include <cmath>
