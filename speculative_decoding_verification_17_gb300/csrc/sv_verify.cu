@@ -328,17 +328,18 @@ struct BonusScan {
   }
 };
 
-// The chunk [j0, j1) of the rows of VW staged in the ring, row i in stage i, read back for
-// the in-chunk scan with the same weights.
+// Logits [j0, j1) of the rows of VW in shared memory (staged for the scan, or a piece the mass
+// pass left in the ring), read back for the in-sub-range scan with the same weights.
 template <typename E, class VW>
 struct StagedScan {
   const VW* vw;
-  const unsigned char* buf;
+  const unsigned char* buf;  // logit j0 of row 0; row i starts `stride` bytes after row i-1
+  int stride;
   int64_t j0, j1;
   using Raw = typename VW::Raw;
   __device__ __forceinline__ Raw load(int64_t j) const {
     if (j >= j1) return vw->pad();
-    return vw->lds(buf, kChunkBytes, (int)((j - j0) / E::kPerVec));
+    return vw->lds(buf, stride, (int)((j - j0) / E::kPerVec));
   }
   __device__ __forceinline__ void weights(const Raw& r, float (&w)[E::kPerVec]) const {
     vw->weights(r, w);
@@ -549,6 +550,7 @@ struct SampleOp {
     int a, err, chunk, take_last;
     DF W;
     DF before;
+    RowSoftmax ra, qa, rn;  // the statistics of target row a, draft row a and target row n
     ScanSmem scan;
     DF cm[kSmemChunks * (2 * kWarps + 1)];  // the draw's sub-range masses, then chunk masses
   };
@@ -723,7 +725,8 @@ struct SampleOp {
                              Ring& ring, int& t, DF& W, bool kept = false);
   template <class VW>
   __device__ static int draw_select(const Args& A, const VW& vw, DF* part, bool landed, float u,
-                                    Smem& sm, Ring& ring, int& t, DF& W);
+                                    Smem& sm, Ring& ring, int& t, DF& W, int res_lo = 0,
+                                    int res_hi = 0);
   __device__ static void emit(const Args& A, int r, int a, int n, int t, DF W, int st);
   // Row n's sub-range masses as pass 1 kept them, chunks [c0, c1), into part[c * kWarps + w]
   // in units of 2^K (K: row n's reference; exact power-of-two scaling). Every thread calls
@@ -738,7 +741,8 @@ struct SampleOp {
   }
   template <class F>
   __device__ static void with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
-                                           F&& f);
+                                           F&& f, const RowSoftmax* tp_pre = nullptr,
+                                           const RowSoftmax* dq_pre = nullptr);
 };
 
 template <typename ET>
@@ -826,7 +830,11 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
                 "the draw's pieces give more sub-ranges per chunk than the masses' layout holds");
   const bool landed = kept || chunk_masses<E, T::kRingBytes>(0, A.nch, A.V, vw, part, ring);
   __syncthreads();
-  return draw_select(A, vw, part, landed, u, sm, ring, t, W);
+  // the mass pass through the ring leaves its last two pieces there
+  const int np = A.nch * DR::kPiecesPerChunk;
+  const bool in_ring = !kept && landed && ring.usable && SV_RESID_RING;
+  return draw_select(A, vw, part, landed, u, sm, ring, t, W, in_ring ? max(0, np - 2) : 0,
+                     in_ring ? np : 0);
 }
 
 // The rest of a draw, from the sub-range masses in part (every chunk's, in vocabulary
@@ -835,7 +843,8 @@ __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, bool landed,
-                                         float u, Smem& sm, Ring& ring, int& t, DF& W) {
+                                         float u, Smem& sm, Ring& ring, int& t, DF& W,
+                                         int res_lo, int res_hi) {
   const int tid = threadIdx.x, lane = tid & 31;
   using DR = DrawRing<VW, T::kRingBytes>;
   constexpr int kSubs = DR::kPiecesPerChunk * kWarps;  // sub-ranges of a chunk
@@ -867,6 +876,16 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
     t = scan_sub<E, DR::kVecPerLane>(s0, sm.before, sm.take_last != 0, sq, sm.scan);
     return kDrawOk;
   }
+  // the mass pass left its last pieces [res_lo, res_hi) in the ring (piece h in half h & 1,
+  // row i at i * kPieceBytes): a sub-range inside one of them is scanned from there
+  const int h = c * DR::kPiecesPerChunk + q / kWarps;
+  if (h >= res_lo && h < res_hi) {
+    const StagedScan<E, VW> rs{&sq, ring.buf + (h & 1) * DR::kHalf, DR::kPieceBytes,
+                               (int64_t)c * E::kChunk + (int64_t)(q / kWarps) * kPieceElems,
+                               sq.j1};
+    t = scan_sub<E, DR::kVecPerLane>(s0, sm.before, sm.take_last != 0, rs, sm.scan);
+    return kDrawOk;
+  }
   // nobody reads the ring any more (the barrier above): stage the sub-range of every row
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)((sq.j1 - s0) * (16 / E::kPerVec));
@@ -882,7 +901,7 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
   bool ok = true;
 #pragma unroll
   for (int i = 0; i < VW::kRows; ++i) ok &= ring_wait(ring, i);
-  const StagedScan<E, VW> ss{&sq, ring.buf, s0, sq.j1};
+  const StagedScan<E, VW> ss{&sq, ring.buf, kChunkBytes, s0, sq.j1};
   t = scan_sub<E, DR::kVecPerLane>(s0, sm.before, sm.take_last != 0, ss, sm.scan);
   if (!__syncthreads_and(ok)) {
     if (tid == 0) atomicOr(&ring.ctl->error, 1u);
@@ -893,15 +912,18 @@ __device__ int SampleOp<ET>::draw_select(const Args& A, const VW& vw, DF* part, 
 
 // The weights of request r's draw, handed to f: the residual max(0, p_a - q_a) (a < n, not
 // bonus), or the bonus draw from p of target row a (a = n after full acceptance, or a row
-// whose residual vanished through rounding), in units of 2^K of that row.
+// whose residual vanished through rounding), in units of 2^K of that row. The rows'
+// statistics come from tp_pre (target row a) and dq_pre (draft row a) when the caller holds
+// them, else from the workspace.
 template <typename ET>
 template <class F>
 __device__ void SampleOp<ET>::with_draw_weights(const Args& A, int r, int a, int n, bool bonus,
-                                                F&& f) {
+                                                F&& f, const RowSoftmax* tp_pre,
+                                                const RowSoftmax* dq_pre) {
   const int R = 2 * A.k + 1;
   if (a < n && !bonus) {
-    const RowSoftmax tp = ld_row(A.row + (int64_t)r * R + a);
-    const RowSoftmax dq = ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
+    const RowSoftmax tp = tp_pre ? *tp_pre : ld_row(A.row + (int64_t)r * R + a);
+    const RowSoftmax dq = dq_pre ? *dq_pre : ld_row(A.row + (int64_t)r * R + A.k + 1 + a);
     ResidScan<E> rs;
     rs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
     rs.rq = row_ptr<E>(A.draft, (int64_t)r * A.k + a, A.V);
@@ -914,7 +936,7 @@ __device__ void SampleOp<ET>::with_draw_weights(const Args& A, int r, int a, int
     rs.wf.iq = 1.0f / dq.S_hi;
     f(rs);
   } else {
-    const RowSoftmax rw = ld_row(A.row + (int64_t)r * R + a);
+    const RowSoftmax rw = tp_pre ? *tp_pre : ld_row(A.row + (int64_t)r * R + a);
     BonusScan<E> bs;
     bs.rp = row_ptr<E>(A.target, (int64_t)r * (A.k + 1) + a, A.V);
     bs.j1 = A.V;
@@ -958,14 +980,16 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   const int R = 2 * A.k + 1;
   const float* u = A.uniforms + (int64_t)r * (A.k + 1);
 
-  // ---- accept tests (warp 0; lane i is draft position i) ----
+  // ---- accept tests (warp 0; lane i is draft position i); the statistics of the rows the
+  //      draw uses stay in shared memory ----
   if (tid < 32) {
     bool bad = !n_ok;
     bool reject = false;
     float pt = 0.0f, pq = 0.0f;
+    RowSoftmax t{}, q{};
     if (n_ok && lane < n) {
-      const RowSoftmax t = ld_row(A.row + (int64_t)r * R + lane);
-      const RowSoftmax q = ld_row(A.row + (int64_t)r * R + A.k + 1 + lane);
+      t = ld_row(A.row + (int64_t)r * R + lane);
+      q = ld_row(A.row + (int64_t)r * R + A.k + 1 + lane);
       const float ui = __ldg(u + lane);
       bad = t.status != 0 || q.status != 0 || !(ui >= 0.0f && ui < 1.0f);
       reject = !accept_test(ui, t, q, A.s);
@@ -974,13 +998,18 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       pq = ex2(fmaf(q.zx, A.s, -q.K)) / q.S_hi;
     }
     if (n_ok && lane == 0) {
-      const RowSoftmax t = ld_row(A.row + (int64_t)r * R + n);
+      const RowSoftmax tn = ld_row(A.row + (int64_t)r * R + n);
       const float uk = __ldg(u + A.k);
-      bad = bad || t.status != 0 || !(uk >= 0.0f && uk < 1.0f);
+      bad = bad || tn.status != 0 || !(uk >= 0.0f && uk < 1.0f);
+      sm.rn = tn;
     }
     const bool err = __any_sync(0xffffffffu, bad);
     const unsigned rej = __ballot_sync(0xffffffffu, reject);
     const int a = rej ? __ffs(rej) - 1 : n;
+    if (lane == a && a < n) {
+      sm.ra = t;
+      sm.qa = q;
+    }
     if (lane < A.k) {
       const float nan = __int_as_float(0x7fc00000);
       if (A.out_p) A.out_p[(int64_t)r * A.k + lane] = err ? nan : (lane < n ? pt : 0.0f);
@@ -1010,18 +1039,19 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
                        : A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
     st = kDrawNoMass;
     if (a < n)  // the residual norm(max(0, p_a - q_a))
-      with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
-        st = draw(A, vw, part, uk, sm, ring, t, W);
-      });
+      with_draw_weights(
+          A, r, a, n, false,
+          [&](const auto& vw) { st = draw(A, vw, part, uk, sm, ring, t, W); }, &sm.ra, &sm.qa);
     if (st == kDrawNoMass) {
       // the bonus draw from p (row n after full acceptance, from the masses pass 1 kept; row
       // a if the residual vanished through rounding, with a pass of its own)
       DF Wb;
       const bool kept = kStageSums && a == n;
-      if (kept) kept_masses(A, r, ld_row(A.row + (int64_t)r * R + n).K, 0, A.nch, part);
-      with_draw_weights(A, r, a, n, true, [&](const auto& vw) {
-        st = draw(A, vw, part, uk, sm, ring, t, Wb, kept);
-      });
+      if (kept) kept_masses(A, r, sm.rn.K, 0, A.nch, part);
+      with_draw_weights(
+          A, r, a, n, true,
+          [&](const auto& vw) { st = draw(A, vw, part, uk, sm, ring, t, Wb, kept); },
+          a == n ? &sm.rn : &sm.ra);
       if (st == kDrawNoMass) st = kDrawFailed;
     }
   }
