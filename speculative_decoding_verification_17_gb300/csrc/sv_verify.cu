@@ -986,11 +986,20 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
     bool bad = !n_ok;
     bool reject = false;
     float pt = 0.0f, pq = 0.0f;
-    RowSoftmax t{}, q{};
-    if (n_ok && lane < n) {
+    // every load first (one round trip), then the tests
+    RowSoftmax t{}, q{}, tn{};
+    float ui = 0.0f, uk = 0.0f;
+    const bool pos = n_ok && lane < n;
+    if (pos) {
       t = ld_row(A.row + (int64_t)r * R + lane);
       q = ld_row(A.row + (int64_t)r * R + A.k + 1 + lane);
-      const float ui = __ldg(u + lane);
+      ui = __ldg(u + lane);
+    }
+    if (n_ok && lane == 0) {
+      tn = ld_row(A.row + (int64_t)r * R + n);
+      uk = __ldg(u + A.k);
+    }
+    if (pos) {
       bad = t.status != 0 || q.status != 0 || !(ui >= 0.0f && ui < 1.0f);
       reject = !accept_test(ui, t, q, A.s);
       // the optional p and q outputs, in fp32
@@ -998,8 +1007,6 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
       pq = ex2(fmaf(q.zx, A.s, -q.K)) / q.S_hi;
     }
     if (n_ok && lane == 0) {
-      const RowSoftmax tn = ld_row(A.row + (int64_t)r * R + n);
-      const float uk = __ldg(u + A.k);
       bad = bad || tn.status != 0 || !(uk >= 0.0f && uk < 1.0f);
       sm.rn = tn;
     }
