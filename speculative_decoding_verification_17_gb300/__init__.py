@@ -33,8 +33,8 @@ Ready-distribution cache (C ABI in ``include/specverify_cache.h``), through
 
 Workspaces: pass ``workspace=`` (a uint8 CUDA tensor of at least the size the matching
 ``*_workspace`` query returns, 256-byte aligned, not shared by calls in flight at the same
-time; it needs no initialisation), or let the binding keep one cached per (device, call)
-that it grows as needed.
+time; it needs no initialisation), or let the binding keep one cached per (device, stream,
+call) that it grows as needed: calls in flight on different streams never share one.
 """
 from __future__ import annotations
 
@@ -133,8 +133,10 @@ _ws_cache: dict = {}
 
 
 def _workspace(kind: str, nbytes: int, device, stream):
-    """Cached zero-filled workspace for (device, kind) of at least ``nbytes`` bytes."""
-    key = (kind, device)
+    """Cached zero-filled workspace for (device, stream, kind) of at least ``nbytes`` bytes.
+    Calls on one stream run in order, so they may share it; calls on two streams may overlap,
+    so each stream has its own."""
+    key = (kind, device, stream.cuda_stream)
     with _ws_lock:
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < nbytes:

@@ -119,6 +119,32 @@ def test_sample_empty_batch_and_repeat_calls():
         assert torch.equal(x, y)
 
 
+def test_sample_concurrent_streams_keep_their_own_workspaces():
+    # two batches verified at the same time on two streams, each with the binding's cached
+    # workspace: the cache gives each stream its own, so both equal their one-at-a-time runs
+    ds = [synth.sample_inputs(48, 4, 30000, "bf16", 0.8, device=DEV, seed=s, ragged=True)
+          for s in (31, 32)]
+    ref = []
+    for d in ds:
+        ref.append(sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"],
+                                         d["uniforms"], d["T"], d["num_draft"]))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    got = [None, None]
+    for rep in range(4):
+        for i, (d, st) in enumerate(zip(ds, streams)):
+            with torch.cuda.stream(st):
+                got[i] = sv.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"],
+                                               d["uniforms"], d["T"], d["num_draft"],
+                                               stream=st)
+    torch.cuda.synchronize()
+    for a, b in zip(ref, got):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("off", [0, 1])
 def test_sample_deferred_draws(off):
     # rows of 15 fp32 chunks: the batch's last requests draw in the second launch, split over
