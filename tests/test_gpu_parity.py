@@ -51,6 +51,8 @@ SMALL = [
     (4, 2, 200003, "bf16", 1.0, False, 2.0, 0.7, 1.0),     # two segments, rows not aligned
     (3, 2, 600000, "bf16", 1.0, True, 2.0, 1.0, 1.0),      # 37 chunks: the draw's masses in
     (2, 3, 300001, "f32", 0.7, False, 2.0, 0.8, 1.0),      # the workspace (aligned / not)
+    (3, 2, 262144, "f32", 1.0, True, 2.0, 1.0, 1.0),       # 32 chunks: the most whose masses
+    (3, 2, 262145, "f32", 1.0, True, 2.0, 1.0, 1.0),       # stay in shared memory; 33
 ]
 
 
@@ -78,6 +80,23 @@ def test_sample_draft_equals_target_accepts_all(B, k, V, dt):
     stats, gpu, _ = run_sample(d)
     assert (gpu["accept_len"] == k).all()
     assert (gpu["resid"] == 0).all()
+
+
+def test_sample_masked_draft_token_accepts():
+    # a drafted token the draft itself masks (q(x) = 0): the ratio p/q is +inf and the
+    # position accepts whatever u is; one the target masks (p(x) = 0) rejects
+    B, k, V = 6, 3, 3000
+    d = synth.sample_inputs(B, k, V, "f32", 1.0, device=DEV, seed=41)
+    x = d["draft_tokens"]
+    for r in range(3):
+        d["draft"][r, 0, x[r, 0]] = float("-inf")
+    for r in range(3, 6):
+        d["target"][r, 1, x[r, 1]] = float("-inf")
+    d["uniforms"][:, :k] = 0.999
+    stats, gpu, orc = run_sample(d)
+    assert (gpu["accept_len"][:3] >= 1).all()
+    assert (gpu["accept_len"][3:] <= 1).all()
+    assert (gpu["q"][:3, 0] == 0).all() and (gpu["p"][3:, 1] == 0).all()
 
 
 def test_sample_data_errors_and_masks():
