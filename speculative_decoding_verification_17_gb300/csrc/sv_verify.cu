@@ -241,6 +241,7 @@ struct SampleArgs {
   int keep_pos;             // rows of draft positions < keep_pos are copied with evict_last
   int defer;                // the last `defer` requests draw in draw_kernel
   int* draw_a;              // [B] their accepted prefix, or -1 for a data error
+  int dcpc;                 // chunks per draw_kernel CTA
   unsigned int* draw_cnt;   // [B] their arrival counters in draw_kernel
 };
 
@@ -1066,11 +1067,12 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
 }
 
 // The draws of the deferred requests (the last `defer` of the batch), one CTA per (request,
-// chunk): each computes the sub-range masses of its chunk of the request's draw rows, as the
-// request's own finisher would, and the CTA that completes the request takes the rest of the
-// draw (the same code on the same masses, so the same token) and writes its outputs. Launched
-// right after segment_kernel<SampleOp> on the same stream, which wrote each deferred request's
-// accepted prefix (or -1 for a data error) and every row's statistics.
+// run of A.dcpc chunks): each computes the sub-range masses of its chunks of the request's
+// draw rows, as the request's own finisher would, and the CTA that completes the request
+// takes the rest of the draw (the same code on the same masses, so the same token) and
+// writes its outputs. Launched right after segment_kernel<SampleOp> on the same stream,
+// which wrote each deferred request's accepted prefix (or -1 for a data error) and every
+// row's statistics.
 template <typename E>
 __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
     draw_kernel(const SampleArgs A, CallCtl* ctl) {
@@ -1082,8 +1084,10 @@ __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
   __shared__ typename Op::Smem sm;
   // the verify launch before this one must be complete, its writes visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int r = A.B - A.defer + (int)(blockIdx.x / (unsigned)A.nch);
-  const int c = (int)(blockIdx.x % (unsigned)A.nch);
+  const int nct = (A.nch + A.dcpc - 1) / A.dcpc;  // CTAs per request
+  const int r = A.B - A.defer + (int)(blockIdx.x / (unsigned)nct);
+  const int c0 = (int)(blockIdx.x % (unsigned)nct) * A.dcpc;
+  const int c1 = min(c0 + A.dcpc, A.nch);
   const int a = __ldcg(A.draw_a + r);
   if (a < 0) return;  // a data error: the verify wrote the sentinel
   bool n_ok;
@@ -1100,14 +1104,14 @@ __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
   DF* gpart = A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
   bool landed = true;
   if (Op::kStageSums && a == n) {  // the bonus draw: row n's masses are pass 1's
-    Op::kept_masses(A, r, ld_row(A.row + (int64_t)r * (2 * A.k + 1) + n).K, c, c + 1, gpart);
+    Op::kept_masses(A, r, ld_row(A.row + (int64_t)r * (2 * A.k + 1) + n).K, c0, c1, gpart);
   } else {
     Op::with_draw_weights(A, r, a, n, false, [&](const auto& vw) {
-      landed = chunk_masses<E, Op::T::kRingBytes>(c, c + 1, A.V, vw, gpart, ring);
+      landed = chunk_masses<E, Op::T::kRingBytes>(c0, c1, A.V, vw, gpart, ring);
     });
   }
   __syncthreads();  // every warp's masses are stored
-  if (tid == 0) sm.req_last = arrive_last(A.draw_cnt + r, (unsigned)A.nch);
+  if (tid == 0) sm.req_last = arrive_last(A.draw_cnt + r, (unsigned)nct);
   __syncthreads();
   if (!sm.req_last) return;
   __threadfence();
@@ -1382,7 +1386,22 @@ int keep_positions(int k, int nseg, int V, sv_dtype d) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(p, k));
 }
 
-// Launch draw_kernel for the deferred requests (one CTA per request and chunk).
+// Chunks per draw_kernel CTA: one, unless the deferred requests' chunks outnumber the CTA
+// slots of one wave; then as many as make them fit one (each CTA streams its chunks through
+// its ring, which keeps two pieces in flight across them): the kernel is latency-bound, and a
+// second or third wave waits for the first.
+#ifndef SV_DRAW_ONE_WAVE
+#define SV_DRAW_ONE_WAVE 1
+#endif
+int draw_chunks_per_cta(int defer, int64_t nch) {
+  if (defer <= 0 || !SV_DRAW_ONE_WAVE) return 1;
+  const int64_t slots = (int64_t)device_sm_count() * SampleOp<F32>::T::kCtasPerSm;
+  const int64_t units = (int64_t)defer * nch;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(nch, (units + slots - 1) / slots));
+}
+
+// Launch draw_kernel for the deferred requests (CTAs of draw_chunks_per_cta chunks of one
+// request).
 template <typename E>
 sv_status launch_draws(const SampleArgs& A, CallCtl* ctl, cudaStream_t st) {
   constexpr int kRingBytes = SampleOp<E>::T::kRingBytes;
@@ -1403,7 +1422,7 @@ sv_status launch_draws(const SampleArgs& A, CallCtl* ctl, cudaStream_t st) {
   // programmatic serialization: the CTAs may become resident while the verify launch
   // finishes, and wait in griddepcontrol.wait for its completion
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)A.defer * A.nch), 1, 1);
+  cfg.gridDim = dim3((unsigned)((int64_t)A.defer * ((A.nch + A.dcpc - 1) / A.dcpc)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kRingBytes;
   cfg.stream = st;
@@ -1489,6 +1508,7 @@ extern "C" sv_status spec_verify_sample(const void* target_logits, const void* d
   A.draw_a = reinterpret_cast<int*>(ws + L.draw_a);
   A.draw_cnt = reinterpret_cast<unsigned int*>(ws + L.draw_cnt);
   A.defer = deferred_requests(B, k, nseg, nch);
+  A.dcpc = draw_chunks_per_cta(A.defer, nch);
   A.keep_pos = keep_positions(k, nseg, V, dtype);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the control word and the counters (the last regions) start every call at zero
