@@ -121,9 +121,10 @@ sv_status conformal_residual(const void* draft_logits, const void* true_logits,
  * Three passes of a radix select over the scores' order-preserving 32-bit keys (11, 11 and 10
  * bits). Up to 8192 scores: one CTA, the keys in shared memory. Beyond that: one cooperative
  * launch (cudaLaunchCooperativeKernel; every CTA resident at once) whose passes meet at grid
- * barriers. A barrier wait is bounded (2 s, never reached when the launch is cooperative);
- * if one runs out, out_q is the quiet NaN with payload 1 (bits 0x7fc00001), which no score
- * produces (a NaN score gives 0x7fc00000).
+ * barriers (the CTA that arrives last picks the pass's digit and publishes it to the others).
+ * A barrier wait is bounded (2 s, never reached when the launch is cooperative); if one runs
+ * out, out_q is the quiet NaN with payload 1 (bits 0x7fc00001), which no score produces (a
+ * NaN score gives 0x7fc00000).
  * ---------------------------------------------------------------------------------------- */
 size_t conformal_quantile_workspace(int n);
 sv_status conformal_quantile(const float* resid, int n, double q, float* out_q,

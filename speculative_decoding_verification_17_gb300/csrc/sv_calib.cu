@@ -19,8 +19,9 @@
 //  conformal_quantile  the split-conformal quantile of those scores: a radix select over the
 //                      scores' order-preserving keys in three passes (11, 11, 10 bits); up to
 //                      8192 scores in one CTA with the keys in shared memory, beyond that one
-//                      cooperative launch whose passes meet at grid barriers, after each of
-//                      which every CTA picks the digit from the pass's global histogram.
+//                      cooperative launch whose passes each end in a grid-wide rendezvous:
+//                      the CTA whose arrival completes the pass picks the digit from the
+//                      pass's global histogram and publishes it to the others.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -540,6 +541,7 @@ constexpr unsigned int kSelTimedOut = 0x7fc00001u;  // quiet NaN, payload 1
 
 struct SelectState {
   unsigned int cnt[4];     // CTA arrivals at each pass's grid barrier
+  unsigned int pick[kSelectPasses][4];  // per pass: the digit, the keys below it, published
   unsigned int hist[kSelectPasses][kSelBins];
 };
 
@@ -553,42 +555,16 @@ __device__ __forceinline__ float key_float(unsigned int k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Grid barrier of a cooperative launch (every CTA resident): each CTA adds one to *count
-// (release, after the CTA's earlier writes) and waits until `target` have (acquire; target is
-// gridDim.x, or more in the barrier self-test), for at most limit_ns. False, for the whole
-// CTA, if the wait ran out.
-__device__ bool grid_barrier(unsigned int* count, unsigned int target, uint64_t limit_ns) {
-  __shared__ int ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    unsigned int seen;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(seen)
-                 : "l"(count)
-                 : "memory");
-    ++seen;
-    const uint64_t t0 = globaltimer_ns();
-    while (seen < target) {
-      if (globaltimer_ns() - t0 > limit_ns) break;
-      __nanosleep(64);
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(count) : "memory");
-    }
-    __threadfence();
-    ok = seen >= target;
-  }
-  __syncthreads();
-  return ok != 0;
-}
-
 // The whole radix select in one cooperative launch. Each pass: every CTA counts the keys that
 // share the prefix chosen so far into a shared histogram of the next digit (sixteen scores per
 // thread and step, four 16-byte loads in flight) and adds it to the pass's global histogram;
-// after a grid barrier, every CTA reads that histogram and picks the same digit d, the one
-// with (keys below it) < want <= (keys below it) + count(d). The first two passes load the
-// scores with an L2 evict-last policy, so the next pass finds them in L2. Each barrier waits
-// for gridDim.x + extra arrivals (extra = 0; 1 only in the barrier self-test, where no
-// barrier can complete) for at most limit_ns.
+// the CTA whose arrival completes the pass reads that histogram and picks the digit d, the
+// one with (keys below it) < want <= (keys below it) + count(d), and publishes it; the other
+// CTAs wait for it (one reader of the histogram: all of them reading its 8 KB at once made
+// the pick take ~6 us a pass). The first two passes load the scores with an L2 evict-last
+// policy, so the next pass finds them in L2. A pass completes at gridDim.x + extra arrivals
+// (extra = 0; 1 only in the barrier self-test, where no pass can complete); every wait is
+// bounded by limit_ns.
 __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int n, int64_t rank,
                                                              SelectState* st, float* out,
                                                              unsigned int extra,
@@ -596,6 +572,7 @@ __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int
   __shared__ unsigned int h[kSelBins];
   __shared__ unsigned int warp_tot[kCalThreads / 32];
   __shared__ unsigned int s_digit, s_before;
+  __shared__ int s_last, s_ok;
   const int64_t stride = (int64_t)gridDim.x * kCalThreads;
   const int64_t tid = (int64_t)blockIdx.x * kCalThreads + threadIdx.x;
   const int64_t n4 = (reinterpret_cast<uintptr_t>(r) % 16 == 0) ? n / 4 : 0;
@@ -641,30 +618,68 @@ __global__ void __launch_bounds__(kCalThreads) select_kernel(const float* r, int
     __syncthreads();
     for (int b = threadIdx.x; b <= (int)mask; b += kCalThreads)
       if (h[b]) atomicAdd(&st->hist[pass][b], h[b]);
-    if (!grid_barrier(&st->cnt[pass], gridDim.x + extra, limit_ns)) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) *out = __uint_as_float(kSelTimedOut);
-      return;
+    // arrival: release this CTA's histogram adds; the last arrival acquires every CTA's
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      unsigned int seen;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(seen)
+                   : "l"(&st->cnt[pass])
+                   : "memory");
+      s_last = seen + 1 == gridDim.x + extra;
     }
-    for (int b = threadIdx.x; b < kSelBins; b += kCalThreads)
-      h[b] = b <= (int)mask ? __ldcg(&st->hist[pass][b]) : 0u;
     __syncthreads();
-    // counts before the prefix sums, kept per thread for the check below
-    constexpr int per = kSelBins / kCalThreads;
-    unsigned int own[per];
+    if (s_last) {
+      // the pass is complete: this CTA picks the digit for every CTA
+      for (int b = threadIdx.x; b < kSelBins; b += kCalThreads)
+        h[b] = b <= (int)mask ? __ldcg(&st->hist[pass][b]) : 0u;
+      __syncthreads();
+      // counts before the prefix sums, kept per thread for the check below
+      constexpr int per = kSelBins / kCalThreads;
+      unsigned int own[per];
 #pragma unroll
-    for (int i = 0; i < per; ++i) own[i] = h[threadIdx.x * per + i];
-    __syncthreads();
-    block_prefix_sums(h, kSelBins, warp_tot);
+      for (int i = 0; i < per; ++i) own[i] = h[threadIdx.x * per + i];
+      __syncthreads();
+      block_prefix_sums(h, kSelBins, warp_tot);
 #pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int b = threadIdx.x * per + i;
-      const unsigned int before = h[b];
-      if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
-        s_digit = (unsigned int)b;
-        s_before = before;
+      for (int i = 0; i < per; ++i) {
+        const int b = threadIdx.x * per + i;
+        const unsigned int before = h[b];
+        if (b <= (int)mask && own[i] > 0 && before < want && want <= before + own[i]) {
+          s_digit = (unsigned int)b;
+          s_before = before;
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        st->pick[pass][0] = s_digit;
+        st->pick[pass][1] = s_before;
+        asm volatile("st.release.gpu.global.u32 [%0], 1;" ::"l"(&st->pick[pass][2]) : "memory");
+      }
+    } else if (threadIdx.x == 0) {
+      // wait (bounded) for the last arrival to publish the digit
+      unsigned int done = 0;
+      const uint64_t t0 = globaltimer_ns();
+      while (true) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                     : "=r"(done)
+                     : "l"(&st->pick[pass][2])
+                     : "memory");
+        if (done || globaltimer_ns() - t0 > limit_ns) break;
+        __nanosleep(128);
+      }
+      s_ok = done != 0;
+      if (done) {
+        s_digit = __ldcg(&st->pick[pass][0]);
+        s_before = __ldcg(&st->pick[pass][1]);
       }
     }
     __syncthreads();
+    if (!s_last && !s_ok) {  // the wait ran out: the timeout sentinel
+      if (blockIdx.x == 0 && threadIdx.x == 0) *out = __uint_as_float(kSelTimedOut);
+      return;
+    }
     prefix = (prefix << width) | s_digit;
     want -= s_before;
     __syncthreads();
