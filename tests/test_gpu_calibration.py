@@ -317,6 +317,27 @@ def test_quantile_random(n, q):
     assert _same_f32(got.cpu().numpy(), [want]), (got.item(), want)
 
 
+@pytest.mark.parametrize("kind", ["all_equal", "two_values", "sorted", "all_nan", "all_inf",
+                                  "denormals"])
+def test_quantile_degenerate_score_sets(kind):
+    # more than 8192 scores: the cooperative radix select, where every pass's digit comes
+    # from the CTA whose arrival completes the pass; here one bin holds every key (or most)
+    n = 50021
+    rng = np.random.default_rng(17)
+    r = {"all_equal": np.full(n, 0.25, np.float32),
+         "two_values": np.where(rng.random(n) < 0.3, 1.0, 2.0).astype(np.float32),
+         "sorted": np.sort(rng.standard_normal(n)).astype(np.float32),
+         "all_nan": np.full(n, np.nan, np.float32),
+         "all_inf": np.full(n, np.inf, np.float32),
+         "denormals": (rng.integers(1, 1 << 20, n) * np.float32(1e-45)).astype(np.float32),
+         }[kind]
+    for q in (1e-6, 0.3, 0.9, 1.0):
+        got = sv.conformal_quantile(_dev(r), q)
+        torch.cuda.synchronize()
+        want = oracle.conformal_quantile(r, q)
+        assert _same_f32(got.cpu().numpy(), [want]), (kind, q, got.item(), want)
+
+
 def test_quantile_of_scores_off_the_16_byte_grid():
     rng = np.random.default_rng(4)
     r = rng.exponential(1.0, 100003).astype(np.float32)
