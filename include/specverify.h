@@ -134,7 +134,7 @@ size_t spec_verify_sample_workspace(int B, int k, int V, sv_dtype dtype);
 /* The number of kernel launches one spec_verify_sample call of this shape makes on the
  * current device: 2 (the clear of its counters and the verify), or 3 when the rows are long
  * enough (at least 8 chunks of 32 KiB, and at most 32) for the draws of the batch's last
- * requests to run in a third launch split over their chunks; 0 for B = 0 or an invalid
+ * requests to run in a third launch split over runs of their chunks; 0 for B = 0 or an invalid
  * shape. The outputs do not depend on it. A library query; the pages have no counterpart. */
 int spec_verify_sample_launches(int B, int k, int V, sv_dtype dtype);
 
