@@ -814,11 +814,10 @@ __device__ void SampleOp<ET>::finish(const Args& A, const Seg& g, Smem& sm, Ring
   finish_request(A, r, n, n_ok, sm, ring);
 }
 
-// One inverse-CDF draw with the weights vw: per-chunk masses (already in part when kept),
-// their total W, the chunk in which u*W falls (one warp scans the chunk masses), then that
-// chunk scanned in vocabulary order, from the ring when the rows are aligned (the chunk of
-// row i staged into stage i by one bulk copy each). Every thread calls this. Returns a
-// DrawStatus; t is the drawn token.
+// One inverse-CDF draw with the weights vw: the masses of every sub-range (one pass over the
+// rows through the ring, or already in part when kept), then draw_select: their total W, the
+// sub-range in which u*W falls, and that sub-range scanned in vocabulary order. Every thread
+// calls this. Returns a DrawStatus; t is the drawn token.
 template <typename ET>
 template <class VW>
 __device__ int SampleOp<ET>::draw(const Args& A, const VW& vw, DF* part, float u, Smem& sm,
