@@ -129,7 +129,7 @@ inline SampleLayout sample_layout(int B, int k, int V, sv_dtype d) {
   size_t o = 0;
   L.part = o;    o = round_up(o + B * R * nseg * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.row = o;     o = round_up(o + B * R * sizeof(RowSoftmax), 256);
-  L.resid = o;   o = round_up(o + B * nch * (2 * kWarpsPerChunk + 1) * sizeof(double), 256);
+  L.resid = o;   o = round_up(o + B * nch * 2 * kWarpsPerChunk * sizeof(double), 256);
   L.bmass = o;   o = round_up(o + B * nch * kWarpsPerChunk * sizeof(WarpSoftmax), 256);
   L.draw_a = o;  o = round_up(o + B * sizeof(int), 256);
   L.ctl = o;     o = round_up(o + sizeof(CallCtl), 256);

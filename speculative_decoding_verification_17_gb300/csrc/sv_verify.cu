@@ -233,7 +233,7 @@ struct SampleArgs {
   float* out_resid;
   WarpSoftmax* part;  // [B * (2k+1)][nseg][kWarps]
   RowSoftmax* row;
-  DF* resid;          // [B][nch * (2 * kWarps + 1)] sub-range then chunk masses of a draw
+  DF* resid;          // [B][nch * 2 * kWarps] the sub-range masses of a request's draw
   WarpSoftmax* bmass;  // [B][nch * kWarps] pass 1's masses of every 4 KiB sub-range of each
                        // request's target row n, (K, hi, lo): its bonus draw's masses
   unsigned int* row_cnt;
@@ -553,7 +553,7 @@ struct SampleOp {
     DF before;
     RowSoftmax ra, qa, rn;  // the statistics of target row a, draft row a and target row n
     ScanSmem scan;
-    DF cm[kSmemChunks * (2 * kWarps + 1)];  // the draw's sub-range masses, then chunk masses
+    DF cm[kSmemChunks * 2 * kWarps];  // the draw's sub-range masses
   };
   // One lane's running softmax sum over the segment: hi + lo (an unevaluated pair) in units
   // of 2^K, K an integer with K >= s * (the largest logit seen), and whether it saw a NaN,
@@ -1041,9 +1041,9 @@ __device__ void SampleOp<ET>::finish_request(const Args& A, int r, int n, bool n
   int st = kDrawFailed;
   if (!sm.err) {
     const float uk = __ldg(u + A.k);
-    DF* part = A.nch <= kSmemChunks  // [nch][up to 2 * kWarps], then [nch]
+    DF* part = A.nch <= kSmemChunks  // [nch][up to 2 * kWarps]
                        ? sm.cm
-                       : A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
+                       : A.resid + (int64_t)r * A.nch * (2 * kWarps);
     st = kDrawNoMass;
     if (a < n)  // the residual norm(max(0, p_a - q_a))
       with_draw_weights(
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, SampleOp<E>::T::kCtasPerSm)
   }
   __syncthreads();
   Ring ring{ring_buf, full, released, 0u, ctl, A.aligned};
-  DF* gpart = A.resid + (int64_t)r * A.nch * (2 * kWarps + 1);
+  DF* gpart = A.resid + (int64_t)r * A.nch * (2 * kWarps);
   bool landed = true;
   if (Op::kStageSums && a == n) {  // the bonus draw: row n's masses are pass 1's
     Op::kept_masses(A, r, ld_row(A.row + (int64_t)r * (2 * A.k + 1) + n).K, c0, c1, gpart);
